@@ -1,0 +1,113 @@
+"""FP64 CPU oracle for the all-pairs softened-gravity sum and leapfrog step.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; the GPU library never uses it and
+shares no code with it.  The arithmetic lives in ``nbody_oracle.c`` (plain
+double loops, j ascending); this module only marshals NumPy arrays.
+
+Sources: "CUDA N-Body Simulation" (LienoPC/N-BodySimulation README) §1.2 for
+the softened sum with G = 1, §1.3 for the half-kick + drift step with
+accelerations from the start-of-step coordinates.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bodies64(pos_mass) -> np.ndarray:
+    pm = np.asarray(pos_mass)
+    if pm.ndim != 2 or pm.shape[1] != 4:
+        raise ValueError("pos_mass must be (n, 4) rows of x, y, z, m")
+    return np.ascontiguousarray(pm, dtype=np.float64)
+
+
+class Oracle:
+    """A loaded copy of the oracle library (the default one, or a test build)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        d, i64, i32, p = ctypes.c_double, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.oracle_threads.argtypes = [i32]
+        lib.oracle_threads.restype = i32
+        lib.oracle_accel.argtypes = [p, i64, d, p, i64, p, i32]
+        lib.oracle_accel.restype = i32
+        lib.oracle_leapfrog.argtypes = [p, p, p, i64, d, d, i32, i32]
+        lib.oracle_leapfrog.restype = i32
+        self.lib = lib
+        self.path = path
+
+    def threads(self, requested: int = 0) -> int:
+        """Threads a call with ``requested`` threads (0 = all cores) uses."""
+        return int(self.lib.oracle_threads(int(requested)))
+
+    def accel(self, pos_mass, eps2: float, idx=None, threads: int = 0) -> np.ndarray:
+        """FP64 accelerations a_i = sum_j m_j r_ij / (|r_ij|^2 + eps2)^(3/2).
+
+        ``pos_mass``: (n, 4) rows (x, y, z, m), any float dtype (widened to
+        fp64).  ``idx``: optional indices of the target bodies; every source
+        body is always summed.  Returns (len(idx) or n, 3) float64.
+        """
+        pm = _bodies64(pos_mass)
+        n = pm.shape[0]
+        if idx is None:
+            idx_arr, n_idx = None, n
+        else:
+            idx_arr = np.ascontiguousarray(idx, dtype=np.int64)
+            n_idx = idx_arr.shape[0]
+        out = np.zeros((n_idx, 3), dtype=np.float64)
+        rc = self.lib.oracle_accel(_ptr(pm), n, float(eps2),
+                                   None if idx_arr is None else _ptr(idx_arr), n_idx,
+                                   _ptr(out), int(threads))
+        if rc < 0:
+            raise ValueError("oracle_accel: bad argument")
+        return out
+
+    def leapfrog(self, pos_mass, vel, eps2: float, dt: float, steps: int,
+                 threads: int = 0):
+        """FP64 leapfrog: per step a = A(x) for all bodies, then v += dt/2 a, x += dt v.
+
+        ``vel`` may be (n, 3) or (n, 4) (only xyz is used).  Returns
+        ``(pos_mass (n,4), vel (n,3), acc (n,3))`` in float64; ``acc`` is the
+        acceleration of the last step (zeros when ``steps`` is 0).
+        """
+        pm = _bodies64(pos_mass).copy()
+        v = np.ascontiguousarray(np.asarray(vel, dtype=np.float64)[:, :3]).copy()
+        n = pm.shape[0]
+        if v.shape[0] != n:
+            raise ValueError("vel must have one row per body")
+        acc = np.zeros((n, 3), dtype=np.float64)
+        rc = self.lib.oracle_leapfrog(_ptr(pm), _ptr(v), _ptr(acc), n, float(eps2),
+                                      float(dt), int(steps), int(threads))
+        if rc < 0:
+            raise ValueError("oracle_leapfrog: bad argument")
+        return pm, v, acc
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(_build.build())
+    return _default
+
+
+def threads(requested: int = 0) -> int:
+    return default().threads(requested)
+
+
+def accel(pos_mass, eps2: float, idx=None, threads: int = 0) -> np.ndarray:
+    return default().accel(pos_mass, eps2, idx, threads)
+
+
+def leapfrog(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int = 0):
+    return default().leapfrog(pos_mass, vel, eps2, dt, steps, threads)

@@ -1,0 +1,131 @@
+/*
+ * FP64 CPU oracle for the all-pairs softened-gravity acceleration and the
+ * leapfrog kick/drift step that consumes it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The GPU library never links, loads or calls this
+ * file, and shares no source with it.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg use it.
+ *
+ * It is deliberately plain: an outer loop over target bodies i and an inner
+ * loop over source bodies j in ascending order, every operation in IEEE
+ * double, no blocking and no reordering.  It is built with
+ * -ffp-contract=off, so no multiply-add is fused and results are the same on
+ * every host.  OpenMP splits only the independent outer loop.
+ *
+ * Sources (page, section):
+ *   "CUDA N-Body Simulation" (LienoPC/N-BodySimulation README)
+ *     §1.2 Gravitational Softening: the softened sum over all j with G = 1,
+ *          r_ij = x_j - x_i, and the remark that the self term is zero.
+ *     §1.3 Numerical Time Integration: the half-step velocity kick with
+ *          a(x(t)) followed by the full-step drift with the kicked velocity;
+ *          accelerations come from the coordinates at the start of the step.
+ *   "Cuda Nbody Notes": the per-pair interaction (r, |r|^2 + eps^2, the
+ *          inverse 3/2 power, the mass factor, the accumulation).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Number of OpenMP threads a call with `requested` threads would use. */
+int oracle_threads(int requested)
+{
+#ifdef _OPENMP
+    return requested > 0 ? requested : omp_get_max_threads();
+#else
+    (void)requested;
+    return 1;
+#endif
+}
+
+/*
+ * Softened acceleration on one target body i, G = 1:
+ *   a_i = sum_{j=0}^{n-1} m_j (x_j - x_i) / (|x_j - x_i|^2 + eps2)^(3/2)
+ * ("CUDA N-Body Simulation" §1.2).  The j = i term has r = 0 and adds exactly
+ * zero while eps2 > 0.  pos_mass rows are (x, y, z, m).
+ */
+static void accel_of_body(const double *pm, int64_t n, double eps2, int64_t i,
+                          double a[3])
+{
+    const double xi = pm[4 * i + 0];
+    const double yi = pm[4 * i + 1];
+    const double zi = pm[4 * i + 2];
+    double ax = 0.0, ay = 0.0, az = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        const double rx = pm[4 * j + 0] - xi;
+        const double ry = pm[4 * j + 1] - yi;
+        const double rz = pm[4 * j + 2] - zi;
+        const double d = rx * rx + ry * ry + rz * rz + eps2;
+        const double w = pm[4 * j + 3] / (d * sqrt(d));
+        ax += w * rx;
+        ay += w * ry;
+        az += w * rz;
+    }
+    a[0] = ax;
+    a[1] = ay;
+    a[2] = az;
+}
+
+/*
+ * Accelerations of the bodies listed in idx[0..n_idx) (all n bodies in order
+ * when idx is NULL, in which case n_idx must equal n), each summed over every
+ * one of the n source bodies.  acc is n_idx rows of (ax, ay, az).
+ * Returns the number of threads used, or -1 on a bad argument.
+ */
+int oracle_accel(const double *pos_mass, int64_t n, double eps2,
+                 const int64_t *idx, int64_t n_idx, double *acc, int threads)
+{
+    if (n < 0 || n_idx < 0 || (idx == NULL && n_idx != n))
+        return -1;
+    if (n_idx > 0 && (pos_mass == NULL || acc == NULL))
+        return -1;
+    if (idx != NULL)
+        for (int64_t k = 0; k < n_idx; ++k)
+            if (idx[k] < 0 || idx[k] >= n)
+                return -1;
+    const int nt = oracle_threads(threads);
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
+    for (int64_t k = 0; k < n_idx; ++k) {
+        const int64_t i = idx ? idx[k] : k;
+        accel_of_body(pos_mass, n, eps2, i, acc + 3 * k);
+    }
+    return nt;
+}
+
+/*
+ * `steps` leapfrog kick/drift steps in place ("CUDA N-Body Simulation" §1.3):
+ *   for every body:  a_i = A_i(x(t))           (all from the same x(t))
+ *   then for every body:
+ *       v_i <- v_i + (dt/2) a_i
+ *       x_i <- x_i + dt v_i
+ * Masses (pos_mass column 3) are never changed.  pos_mass is n rows of
+ * (x, y, z, m), vel n rows of (vx, vy, vz), acc n rows of (ax, ay, az); on
+ * return acc holds the accelerations of the last step, i.e. at the positions
+ * before its drift.  Returns the number of threads used, or -1 on a bad
+ * argument.
+ */
+int oracle_leapfrog(double *pos_mass, double *vel, double *acc, int64_t n,
+                    double eps2, double dt, int steps, int threads)
+{
+    if (n < 0 || steps < 0)
+        return -1;
+    if (n > 0 && (pos_mass == NULL || vel == NULL || acc == NULL))
+        return -1;
+    const int nt = oracle_threads(threads);
+    for (int s = 0; s < steps; ++s) {
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
+        for (int64_t i = 0; i < n; ++i)
+            accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);
+#pragma omp parallel for schedule(static) num_threads(nt)
+        for (int64_t i = 0; i < n; ++i) {
+            for (int c = 0; c < 3; ++c) {
+                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];
+                pos_mass[4 * i + c] = pos_mass[4 * i + c] + dt * vel[3 * i + c];
+            }
+        }
+    }
+    return nt;
+}
