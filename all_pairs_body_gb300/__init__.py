@@ -1,0 +1,169 @@
+"""Python binding of the GB300 all-pairs softened-gravity library.
+
+Argument marshalling only.  Every step of the computation (the all-pairs
+acceleration sum, the second-pass reductions and the leapfrog kick/drift)
+runs in the CUDA kernels of ``libnbody_gb300.so``, whose C ABI is declared in
+``include/nbody.h``.  PyTorch supplies device memory and the current stream.
+There is no CPU fallback: every call raises if the compiled library is
+missing or no CUDA device is usable.
+
+    a_i = sum_j m_j (x_j - x_i) / (|x_j - x_i|^2 + eps2)^(3/2),  G = 1
+    step: v <- v + (dt/2) a(x);  x <- x + dt v
+
+("CUDA N-Body Simulation" §1.2 and §1.3.)  Bodies are float32 (n, 4) rows
+(x, y, z, m); velocities (vx, vy, vz, w); accelerations (ax, ay, az, 0).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libnbody_gb300.so")
+
+PATH_AUTO, PATH_TILED, PATH_SPLIT, PATH_WARP = 0, 1, 2, 3
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
+PLAN_FIELDS = ("path", "grid", "threads", "bodies_per_cta", "tile", "tiles", "units",
+               "second_pass", "launches_accel", "launches_step", "sms")
+
+EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
+           "nbody_leapfrog_step", "nbody_leapfrog_step_on_stream",
+           "nbody_leapfrog_step_with", "nbody_sync", "nbody_plan", "nbody_strerror",
+           "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
+           "nbody_profile_read")
+
+
+class NBodyError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with all_pairs_body_gb300.build.build() "
+                "(or __graft_entry__.build()); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+        sig = {
+            "nbody_accel": [p, p, i64, f32],
+            "nbody_accel_on_stream": [p, p, i64, f32, p],
+            "nbody_accel_with": [p, p, i64, f32, i32, i32, p],
+            "nbody_leapfrog_step": [p, p, p, i64, f32, f32, i32],
+            "nbody_leapfrog_step_on_stream": [p, p, p, i64, f32, f32, i32, p],
+            "nbody_leapfrog_step_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
+            "nbody_sync": [p],
+            "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
+            "nbody_selftest_timeout": [i32, p],
+            "nbody_profile_enable": [i32],
+            "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
+                                   ctypes.POINTER(i64)],
+            "nbody_strerror": [i32],
+            "nbody_release": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = i32
+        L.nbody_strerror.restype = ctypes.c_char_p
+        L.nbody_release.restype = None
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().nbody_strerror(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise NBodyError(rc, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _rows(t, n: int | None, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if t.dim() != 2 or t.shape[1] != 4 or (n is not None and t.shape[0] != n):
+        raise ValueError(f"{name} must have shape (n, 4)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def accel(pos_mass, eps2: float, out=None, path: int = PATH_AUTO, split: int = 0,
+          stream=None):
+    """Accelerations of all bodies; returns ``out`` (allocated if None)."""
+    import torch
+    n = int(pos_mass.shape[0])
+    if out is None:
+        out = torch.empty_like(pos_mass)
+    rc = lib().nbody_accel_with(_rows(pos_mass, None, "pos_mass"), _rows(out, n, "out"), n,
+                                float(eps2), int(path), int(split), _stream(stream))
+    _check(rc, "nbody_accel")
+    return out
+
+
+def leapfrog_step(pos_mass, vel, accel_out, eps2: float, dt: float, steps: int = 1,
+                  path: int = PATH_AUTO, split: int = 0, stream=None) -> None:
+    """``steps`` kick/drift steps in place on ``pos_mass`` and ``vel``; the last
+    step's accelerations go to ``accel_out``."""
+    n = int(pos_mass.shape[0])
+    rc = lib().nbody_leapfrog_step_with(
+        _rows(pos_mass, None, "pos_mass"), _rows(vel, n, "vel"), _rows(accel_out, n, "accel"),
+        n, float(eps2), float(dt), int(steps), int(path), int(split), _stream(stream))
+    _check(rc, "nbody_leapfrog_step")
+
+
+def sync(stream=None) -> None:
+    """Wait for the stream and raise if a kernel reported a device-side failure."""
+    _check(lib().nbody_sync(_stream(stream)), "nbody_sync")
+
+
+def plan(n: int, path: int = PATH_AUTO, split: int = 0) -> dict:
+    """Launch plan of a force pass over n bodies on the current device."""
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(lib().nbody_plan(int(n), int(path), int(split), out, len(PLAN_FIELDS)), "nbody_plan")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+def release() -> None:
+    """Free the library's cached scratch on every device."""
+    lib().nbody_release()
+
+
+def profile_enable(on: bool = True) -> None:
+    """Start (or stop) timing force-kernel launches and counting kernel launches."""
+    _check(lib().nbody_profile_enable(1 if on else 0), "nbody_profile_enable")
+
+
+def profile_read() -> tuple[float, int, int]:
+    """(force-kernel ms, force-kernel launches, all kernel launches) since the last read."""
+    ms = ctypes.c_double(0.0)
+    fl = ctypes.c_int64(0)
+    kl = ctypes.c_int64(0)
+    _check(lib().nbody_profile_read(ctypes.byref(ms), ctypes.byref(fl), ctypes.byref(kl)),
+           "nbody_profile_read")
+    return float(ms.value), int(fl.value), int(kl.value)
+
+
+def selftest_timeout(timeout_ms: int = 100, stream=None) -> int:
+    """Run the bounded-wait check; a correct build returns ETIMEOUT."""
+    return int(lib().nbody_selftest_timeout(int(timeout_ms), _stream(stream)))

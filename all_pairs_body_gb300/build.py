@@ -1,0 +1,48 @@
+"""Build the CUDA library in-tree: all_pairs_body_gb300/libnbody_gb300.so.
+
+One translation unit, one -gencode (sm_103a), compiled with nvcc directly
+(no cmake, no torch extension machinery), so it builds in well under a
+minute on x86-64 and on the aarch64 GPU hosts alike.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(HERE, "libnbody_gb300.so")
+SOURCES = ["nbody_api.cu"]
+DEPS = SOURCES + ["nbody_kernels.cuh"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-ftz=true", "-Xcompiler", "-fPIC",
+              "-shared", "-Xcompiler", "-Wall"]
+
+
+def nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
+    deps = [os.path.join(CSRC, s) for s in DEPS] + [os.path.join(INCLUDE, "nbody.h")]
+    if not force and os.path.exists(LIB):
+        t = os.path.getmtime(LIB)
+        if all(os.path.getmtime(d) <= t for d in deps):
+            return LIB
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = ([nvcc()] + ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra or [])
+           + ["-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcudart"])
+    if verbose:
+        print(" ".join(cmd), file=sys.stderr)
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    extra = ["-Xptxas", "-v"] if "-v" in sys.argv else None
+    print(build(force=True, verbose=True, extra=extra))

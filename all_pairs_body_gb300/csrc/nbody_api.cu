@@ -1,0 +1,595 @@
+// Host side of the all-pairs softened-gravity library: argument checks,
+// launch plans, cached scratch and the exported C ABI declared in nbody.h.
+//
+// Nothing here computes physics: every step of the path runs in the kernels
+// of nbody_kernels.cuh.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "nbody.h"
+#include "nbody_kernels.cuh"
+
+namespace nbody {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per tile copy: only a fault gets near it
+constexpr int kFinishThreads = 256;
+constexpr int kWarpKW = 8;
+constexpr int kWarpNW = 4;
+constexpr long long kWarpMaxN = 8192;  // AUTO uses the warp kernel up to this n
+
+using TiledKernel = void (*)(const TiledArgs, const Epilogue);
+
+struct TiledConfig {
+  int ki, nt, tj;
+  TiledKernel kernel;
+};
+
+// Target bodies per thread, threads per CTA, sources per tile.
+const TiledConfig kTiled[] = {
+    {8, 256, 256, force_tiled<8, 256, 256, 1>},
+    {4, 128, 128, force_tiled<4, 128, 128, 2>},
+    {2, 128, 64, force_tiled<2, 128, 64, 4>},
+};
+constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
+
+struct DeviceInfo {
+  int sms = 0;
+  int occupancy[kNumTiled] = {};
+};
+
+struct Plan {
+  int path = NBODY_PATH_AUTO;
+  int cfg = 0;
+  int threads = 0;
+  long long block = 0;  // targets per CTA
+  int tj = 0;           // sources per tile (tiled paths)
+  long long ntiles = 0, nblocks = 0, units = 0;
+  long long grid = 0;  // CTAs
+  bool second_pass = false;
+  int slices = 1;  // warp path
+  long long slice_len = 0;
+  long long npad = 0;  // ntiles * tj
+  int sms = 0;
+};
+
+struct Buf {
+  void* p = nullptr;
+  size_t bytes = 0;
+};
+
+struct Scratch {
+  Buf dup_a, dup_b, pos_alt, partial;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
+
+// measurement hooks (nbody_profile_enable / nbody_profile_read)
+struct Profile {
+  bool enabled = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> force_events;
+  long long kernel_launches = 0;
+};
+Profile g_prof;
+
+void count_launches(int k) {
+  if (g_prof.enabled) g_prof.kernel_launches += k;
+}
+
+// Record an event on `st` (profiling only); returns nullptr when disabled.
+cudaEvent_t prof_event(cudaStream_t st) {
+  if (!g_prof.enabled) return nullptr;
+  cudaEvent_t ev = nullptr;
+  if (cudaEventCreate(&ev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaEventRecord(ev, st);
+  return ev;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
+long long env_int(const char* name, long long dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || v[0] == '\0') return dflt;
+  return std::strtoll(v, nullptr, 10);
+}
+
+int device_info(int dev, DeviceInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    for (int c = 0; c < kNumTiled; ++c) {
+      int occ = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kTiled[c].kernel, kTiled[c].nt, 0) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return NBODY_ECUDA;
+      }
+      d.occupancy[c] = occ > 0 ? occ : 1;
+    }
+    it = g_devices.emplace(dev, d).first;
+  }
+  *out = it->second;
+  return NBODY_OK;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  return NBODY_OK;
+}
+
+// --------------------------------------------------------------------------
+// launch plans
+// --------------------------------------------------------------------------
+
+int auto_tiled_config(long long n) {
+  const long long forced = env_int("NBODY_TILED_CONFIG", -1);
+  if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
+  if (n >= 131072) return 0;
+  if (n >= 16384) return 1;
+  return 2;
+}
+
+bool streamk_needs_second_pass(long long units, long long grid, long long ntiles) {
+  for (long long c = 1; c < grid; ++c)
+    if (unit_begin(units, grid, c) % ntiles != 0) return true;
+  return false;
+}
+
+void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) {
+  p->cfg = auto_tiled_config(n);
+  const TiledConfig& tc = kTiled[p->cfg];
+  p->threads = tc.nt;
+  p->block = static_cast<long long>(tc.ki) * tc.nt;
+  p->tj = tc.tj;
+  p->ntiles = ceil_div(n, tc.tj);
+  p->npad = p->ntiles * tc.tj;
+  p->nblocks = ceil_div(n, p->block);
+  p->units = p->nblocks * p->ntiles;
+  if (path == NBODY_PATH_TILED) {
+    p->grid = p->nblocks;
+  } else if (path == NBODY_PATH_SPLIT && split > 0) {
+    p->grid = std::min(p->units, p->nblocks * static_cast<long long>(split));
+  } else {  // one full wave of CTAs, work divided evenly (stream-K)
+    const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.occupancy[p->cfg]);
+    p->grid = std::min(p->units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+  }
+  p->second_pass = streamk_needs_second_pass(p->units, p->grid, p->ntiles);
+}
+
+void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
+  p->threads = kWarpNW * 32;
+  p->block = kWarpKW;
+  p->nblocks = ceil_div(n, kWarpKW);
+  long long s = split;
+  if (s <= 0) {
+    s = std::min(ceil_div(4LL * d.sms, p->nblocks), ceil_div(n, 256));
+    s = std::max(1LL, s);
+  }
+  s = std::min(s, std::min(n, 65535LL));
+  p->slice_len = ceil_div(n, s);
+  p->slices = static_cast<int>(ceil_div(n, p->slice_len));
+  p->grid = p->nblocks * p->slices;
+  p->second_pass = p->slices > 1;
+}
+
+int make_plan(long long n, int path, int split, int dev, Plan* p) {
+  DeviceInfo d;
+  const int st = device_info(dev, &d);
+  if (st != NBODY_OK) return st;
+  *p = Plan();
+  p->sms = d.sms;
+  int resolved = path;
+  if (resolved == NBODY_PATH_AUTO) resolved = n <= kWarpMaxN ? NBODY_PATH_WARP : NBODY_PATH_SPLIT;
+  p->path = resolved;
+  if (resolved == NBODY_PATH_WARP)
+    plan_warp(n, split, d, p);
+  else
+    plan_tiled(n, resolved, path == NBODY_PATH_AUTO ? 0 : split, d, p);
+  return NBODY_OK;
+}
+
+int launches_accel(const Plan& p) {
+  if (p.path == NBODY_PATH_WARP) return 1 + (p.second_pass ? 1 : 0);
+  return 2 + (p.second_pass ? 1 : 0);
+}
+
+int launches_step1(const Plan& p) { return launches_accel(p); }
+
+// --------------------------------------------------------------------------
+// scratch
+// --------------------------------------------------------------------------
+
+int ensure(Buf& b, size_t bytes, cudaStream_t st) {
+  if (bytes == 0 || b.bytes >= bytes) return NBODY_OK;
+  if (env_flag("NBODY_FAULT_ALLOC")) return NBODY_ENOMEM;  // host-side fault injection
+  if (b.p != nullptr) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    cudaFree(b.p);
+    b.p = nullptr;
+    b.bytes = 0;
+  }
+  if (cudaMalloc(&b.p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    b.p = nullptr;
+    return NBODY_ENOMEM;
+  }
+  b.bytes = bytes;
+  return NBODY_OK;
+}
+
+int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapfrog,
+                Scratch** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Scratch& s = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
+  int rc = NBODY_OK;
+  if (p.path != NBODY_PATH_WARP) {
+    const size_t dup_bytes = static_cast<size_t>(p.npad) * 2 * sizeof(float4);
+    if (rc == NBODY_OK) rc = ensure(s.dup_a, dup_bytes, st);
+    if (rc == NBODY_OK && leapfrog) rc = ensure(s.dup_b, dup_bytes, st);
+    if (rc == NBODY_OK && p.second_pass)
+      rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
+  } else if (p.second_pass) {
+    rc = ensure(s.partial, static_cast<size_t>(p.slices) * n * sizeof(float4), st);
+  }
+  if (rc == NBODY_OK && leapfrog) rc = ensure(s.pos_alt, static_cast<size_t>(n) * sizeof(float4), st);
+  *out = &s;
+  return rc;
+}
+
+// --------------------------------------------------------------------------
+// argument checks
+// --------------------------------------------------------------------------
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+int check_scalars(int64_t n, float eps2, int path, int split) {
+  if (n < 0 || n > static_cast<int64_t>(INT32_MAX)) return NBODY_EINVAL;
+  if (!std::isfinite(eps2) || !(eps2 > 0.0f)) return NBODY_EINVAL;
+  if (path < NBODY_PATH_AUTO || path > NBODY_PATH_WARP) return NBODY_EINVAL;
+  if (split < 0) return NBODY_EINVAL;
+  return NBODY_OK;
+}
+
+int check_device_pointer(const void* p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_EINVAL;
+  }
+  if (at.type == cudaMemoryTypeManaged) return NBODY_OK;
+  if (at.type != cudaMemoryTypeDevice || at.device != dev) return NBODY_EINVAL;
+  return NBODY_OK;
+}
+
+int launch_status() {
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? NBODY_OK : NBODY_ECUDA;
+}
+
+// --------------------------------------------------------------------------
+// launch sequences
+// --------------------------------------------------------------------------
+
+void launch_expand(const float4* pos, float4* dup, float4* dup2, long long n, long long npad,
+                   cudaStream_t st) {
+  const long long blocks = ceil_div(npad, kFinishThreads);
+  count_launches(1);
+  expand_sources<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(pos, dup, dup2,
+                                                                           static_cast<int>(n), npad);
+}
+
+// One force pass (plus its second pass): sources and targets `pos`
+// (expanded copy `dup` for the tiled kernel), finished through `epi`.
+void launch_force(const Plan& p, const float4* pos, const float4* dup, long long n, float eps2,
+                  float4* partial, const Epilogue& epi, cudaStream_t st) {
+  if (p.path == NBODY_PATH_WARP) {
+    WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
+    dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
+    cudaEvent_t e0 = prof_event(st);
+    force_warp<kWarpKW, kWarpNW><<<grid, p.threads, 0, st>>>(a, epi);
+    cudaEvent_t e1 = prof_event(st);
+    if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+    count_launches(1 + (p.second_pass ? 1 : 0));
+    if (p.second_pass) {
+      const long long blocks = ceil_div(n, kFinishThreads);
+      finish_slices<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(
+          partial, static_cast<int>(n), p.slices, epi);
+    }
+    return;
+  }
+  TiledArgs a{pos, dup, static_cast<int>(n), eps2, p.ntiles, p.units, p.grid, partial, kWaitLimitNs, -1};
+  cudaEvent_t e0 = prof_event(st);
+  kTiled[p.cfg].kernel<<<static_cast<unsigned>(p.grid), p.threads, 0, st>>>(a, epi);
+  cudaEvent_t e1 = prof_event(st);
+  if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+  count_launches(1 + (p.second_pass ? 1 : 0));
+  if (p.second_pass) {
+    StreamkFinishArgs f{partial, static_cast<int>(n), p.block, p.ntiles, p.units, p.grid};
+    const long long blocks = ceil_div(n, kFinishThreads);
+    finish_streamk<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(f, epi);
+  }
+}
+
+int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int path, int split,
+               cudaStream_t st) {
+  int rc = check_scalars(n, eps2, path, split);
+  if (rc != NBODY_OK) return rc;
+  if (n == 0) return NBODY_OK;
+  if (pos_mass == nullptr || accel == nullptr) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !aligned16(accel)) return NBODY_EINVAL;
+  const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
+  if (overlaps(pos_mass, accel, bytes)) return NBODY_EINVAL;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
+  Plan p;
+  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
+  Scratch* s = nullptr;
+  if ((rc = get_scratch(dev, st, p, n, false, &s)) != NBODY_OK) return rc;
+
+  const float4* pos = reinterpret_cast<const float4*>(pos_mass);
+  float4* dup = static_cast<float4*>(s->dup_a.p);
+  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, 0.f, 0.f};
+  if (p.path != NBODY_PATH_WARP) launch_expand(pos, dup, nullptr, n, p.npad, st);
+  launch_force(p, pos, dup, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+  return launch_status();
+}
+
+int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
+                  int steps, int path, int split, cudaStream_t st) {
+  int rc = check_scalars(n, eps2, path, split);
+  if (rc != NBODY_OK) return rc;
+  if (!std::isfinite(dt) || steps < 0) return NBODY_EINVAL;
+  if (n == 0 || steps == 0) return NBODY_OK;
+  if (pos_mass == nullptr || vel == nullptr || accel == nullptr) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !aligned16(vel) || !aligned16(accel)) return NBODY_EINVAL;
+  const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
+  if (overlaps(pos_mass, accel, bytes) || overlaps(vel, accel, bytes) ||
+      overlaps(pos_mass, vel, bytes))
+    return NBODY_EINVAL;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(vel, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
+  Plan p;
+  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
+  Scratch* s = nullptr;
+  if ((rc = get_scratch(dev, st, p, n, true, &s)) != NBODY_OK) return rc;
+
+  float4* user = reinterpret_cast<float4*>(pos_mass);
+  float4* alt = static_cast<float4*>(s->pos_alt.p);
+  float4* cur = user;
+  float4* nxt = alt;
+  if (steps & 1) {  // an odd count then ends in the caller's buffer
+    if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    cur = alt;
+    nxt = user;
+  }
+  float4* dup_cur = static_cast<float4*>(s->dup_a.p);
+  float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
+  if (p.path != NBODY_PATH_WARP) launch_expand(cur, dup_cur, dup_nxt, n, p.npad, st);
+  const float half_dt = 0.5f * dt;
+  for (int k = 0; k < steps; ++k) {
+    const bool last = (k + 1 == steps);
+    Epilogue epi{cur, reinterpret_cast<float4*>(accel), reinterpret_cast<float4*>(vel), nxt,
+                 (p.path != NBODY_PATH_WARP && !last) ? dup_nxt : nullptr, half_dt, dt};
+    launch_force(p, cur, dup_cur, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+    std::swap(cur, nxt);
+    std::swap(dup_cur, dup_nxt);
+  }
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace nbody
+
+// ============================================================================
+// exported C ABI
+// ============================================================================
+
+extern "C" {
+
+int nbody_accel(const float* pos_mass, float* accel, int64_t n, float eps2) {
+  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0, nullptr);
+}
+
+int nbody_accel_on_stream(const float* pos_mass, float* accel, int64_t n, float eps2,
+                          void* cuda_stream) {
+  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0,
+                           static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_accel_with(const float* pos_mass, float* accel, int64_t n, float eps2, int path,
+                     int split, void* cuda_stream) {
+  return nbody::accel_impl(pos_mass, accel, n, eps2, path, split,
+                           static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_leapfrog_step(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
+                        float dt, int steps) {
+  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                              nullptr);
+}
+
+int nbody_leapfrog_step_on_stream(float* pos_mass, float* vel, float* accel, int64_t n,
+                                  float eps2, float dt, int steps, void* cuda_stream) {
+  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                              static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_leapfrog_step_with(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
+                             float dt, int steps, int path, int split, void* cuda_stream) {
+  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split,
+                              static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_sync(void* cuda_stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  int status = 0;
+  if (cudaMemcpyFromSymbol(&status, nbody::g_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  if (status != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(nbody::g_status, &zero, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+  }
+  return status;
+}
+
+int nbody_plan(int64_t n, int path, int split, int64_t* out, int len) {
+  int rc = nbody::check_scalars(n, 1.0f, path, split);
+  if (rc != NBODY_OK) return rc;
+  if (out == nullptr && len > 0) return NBODY_EINVAL;
+  int dev = 0;
+  if ((rc = nbody::current_device(&dev)) != NBODY_OK) return rc;
+  nbody::Plan p;
+  if ((rc = nbody::make_plan(n > 0 ? n : 1, path, split, dev, &p)) != NBODY_OK) return rc;
+  const int64_t v[] = {p.path,  p.grid,  p.threads, p.block,
+                       p.tj,    p.ntiles, p.units,  p.second_pass ? 1 : 0,
+                       nbody::launches_accel(p), nbody::launches_step1(p), p.sms};
+  const int nv = static_cast<int>(sizeof(v) / sizeof(v[0]));
+  for (int k = 0; k < len && k < nv; ++k) out[k] = v[k];
+  return NBODY_OK;
+}
+
+int nbody_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(nbody::g_mu);
+  nbody::g_prof.enabled = enable != 0;
+  return NBODY_OK;
+}
+
+int nbody_profile_read(double* force_ms, int64_t* force_launches, int64_t* kernel_launches) {
+  std::lock_guard<std::mutex> lk(nbody::g_mu);
+  double total = 0.0;
+  int rc = NBODY_OK;
+  for (auto& ev : nbody::g_prof.force_events) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(ev.second) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, ev.first, ev.second) != cudaSuccess) {
+      cudaGetLastError();
+      rc = NBODY_ECUDA;
+    }
+    total += ms;
+    cudaEventDestroy(ev.first);
+    cudaEventDestroy(ev.second);
+  }
+  if (force_ms != nullptr) *force_ms = total;
+  if (force_launches != nullptr) *force_launches = static_cast<int64_t>(nbody::g_prof.force_events.size());
+  if (kernel_launches != nullptr) *kernel_launches = nbody::g_prof.kernel_launches;
+  nbody::g_prof.force_events.clear();
+  nbody::g_prof.kernel_launches = 0;
+  return rc;
+}
+
+const char* nbody_strerror(int status) {
+  switch (status) {
+    case NBODY_OK: return "ok";
+    case NBODY_EINVAL: return "invalid argument";
+    case NBODY_ENOMEM: return "scratch allocation failed";
+    case NBODY_ECUDA: return "CUDA error (no usable device or a failed launch)";
+    case NBODY_ETIMEOUT: return "a bounded device-side wait expired";
+    default: return "unknown status";
+  }
+}
+
+void nbody_release(void) {
+  std::lock_guard<std::mutex> lk(nbody::g_mu);
+  int prev = -1;
+  const bool have_prev = cudaGetDevice(&prev) == cudaSuccess;
+  for (auto& kv : nbody::g_scratch) {
+    if (cudaSetDevice(kv.first.first) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    cudaDeviceSynchronize();
+    for (nbody::Buf* b : {&kv.second.dup_a, &kv.second.dup_b, &kv.second.pos_alt, &kv.second.partial}) {
+      if (b->p != nullptr) cudaFree(b->p);
+      b->p = nullptr;
+      b->bytes = 0;
+    }
+  }
+  nbody::g_scratch.clear();
+  if (have_prev) cudaSetDevice(prev);
+  cudaGetLastError();
+}
+
+int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
+  using namespace nbody;
+  if (timeout_ms <= 0) return NBODY_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  constexpr int kCfg = 2;  // smallest tiled kernel
+  const TiledConfig& tc = kTiled[kCfg];
+  const long long n = static_cast<long long>(tc.ki) * tc.nt;  // one i-block
+  const long long ntiles = ceil_div(n, tc.tj);
+  float4 *pos = nullptr, *dup = nullptr, *acc = nullptr;
+  const size_t pb = n * sizeof(float4), db = 2 * ntiles * tc.tj * sizeof(float4);
+  if (cudaMalloc(&pos, pb) != cudaSuccess || cudaMalloc(&dup, db) != cudaSuccess ||
+      cudaMalloc(&acc, pb) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(pos);
+    cudaFree(dup);
+    cudaFree(acc);
+    return NBODY_ENOMEM;
+  }
+  cudaMemsetAsync(pos, 0, pb, st);
+  cudaMemsetAsync(dup, 0, db, st);
+  TiledArgs a{pos, dup, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr,
+              static_cast<uint64_t>(timeout_ms) * 1000000ull, 0};
+  Epilogue epi{pos, acc, nullptr, nullptr, nullptr, 0.f, 0.f};
+  tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
+  int rc = launch_status();
+  const int srv = nbody_sync(cuda_stream);
+  if (rc == NBODY_OK) rc = srv;
+  cudaFree(pos);
+  cudaFree(dup);
+  cudaFree(acc);
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,499 @@
+// Device code of the all-pairs softened-gravity library (sm_103a).
+//
+// Computes a_i = sum_j m_j (x_j - x_i) / (|x_j - x_i|^2 + eps2)^(3/2), G = 1
+// ("CUDA N-Body Simulation", §1.2), and optionally fuses the leapfrog
+// half-kick + drift of §1.3 into the pass that completes each a_i.
+//
+// Kernels
+//   expand_sources      float4 (x,y,z,m) rows -> two rows (x,x,y,y),(z,z,m,m)
+//                       per body, zero-padded to whole tiles, so each source
+//                       component arrives as an already duplicated FP32 pair.
+//   force_tiled<KI,NT,TJ>
+//                       KI target bodies per thread in registers (KI/2 packed
+//                       FP32 pairs), source tiles of TJ bodies staged in
+//                       shared memory by 1-D TMA bulk copies on a two-stage
+//                       mbarrier pipeline, packed FFMA2/FADD2/FMUL2 + MUFU.RSQ
+//                       inner loop.  Work = (i-block, j-tile) units divided
+//                       evenly over the grid; a CTA that covers an i-block's
+//                       whole j range finishes it (accel or kick/drift), else
+//                       it writes a partial sum for the second pass.
+//   finish_streamk      second pass for the tiled kernel: sums the partials
+//                       of split i-blocks in CTA (= j) order and finishes.
+//   force_warp<KW,NW>   small-n kernel: a CTA owns KW targets; its NW*32
+//                       threads stride over one j slice; warp shuffles then
+//                       shared memory (fixed order) combine the threads.
+//   finish_slices       second pass for the warp kernel: sums S slices in order.
+//
+// The pages' tiled kernel ("CUDA N-Body Simulation" §3.1, "Cuda Nbody Notes"
+// calculate_forces, The CUDA Handbook ch. 14 shared-memory kernel) keeps one
+// target per thread and loads tiles with plain stores plus two barriers;
+// the design here keeps that tiling idea and replaces the rest.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nbody.h"
+
+namespace nbody {
+
+// Device-side status word: NBODY_OK or NBODY_ETIMEOUT (read and cleared by
+// nbody_sync on the host).  This header is compiled into one translation unit.
+__device__ int g_status = 0;
+
+// ---------------------------------------------------------------------------
+// small PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float rsqrt_approx(float x) {
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with `parity` of the mbarrier completes, for at most
+// timeout_ns of global time.  Returns false when the limit expired.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int k = 0; k < 16; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// 1-D TMA bulk copy global -> shared; completion counted on the mbarrier.
+// dst, src and bytes must all be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// the pair interaction, two target bodies at once
+// ---------------------------------------------------------------------------
+
+// One source body (X, Y, Z, M: each component duplicated in both halves)
+// against two target bodies whose NEGATED coordinates are (nx, ny, nz):
+//   r = x_j - x_i, d = |r|^2 + eps2, q = d^(-1/2), s = m_j q^3, a += s r.
+// 12 packed-pair FP32 instructions and 2 MUFU.RSQ for two interactions.
+__device__ __forceinline__ void interact2(float2 X, float2 Y, float2 Z, float2 M, float2 nx,
+                                          float2 ny, float2 nz, float2 e2, float2& ax, float2& ay,
+                                          float2& az) {
+  const float2 rx = __fadd2_rn(X, nx);
+  const float2 ry = __fadd2_rn(Y, ny);
+  const float2 rz = __fadd2_rn(Z, nz);
+  float2 d = __ffma2_rn(rx, rx, e2);
+  d = __ffma2_rn(ry, ry, d);
+  d = __ffma2_rn(rz, rz, d);
+  const float2 q = make_float2(rsqrt_approx(d.x), rsqrt_approx(d.y));
+  const float2 q2 = __fmul2_rn(q, q);
+  const float2 s = __fmul2_rn(__fmul2_rn(M, q), q2);
+  ax = __ffma2_rn(rx, s, ax);
+  ay = __ffma2_rn(ry, s, ay);
+  az = __ffma2_rn(rz, s, az);
+}
+
+// ---------------------------------------------------------------------------
+// finishing a body: write a_i, and for a leapfrog step kick and drift
+// ---------------------------------------------------------------------------
+
+struct Epilogue {
+  const float4* pos;  // start-of-step positions (x, y, z, m)
+  float4* accel;      // out: (ax, ay, az, 0)
+  float4* vel;        // leapfrog only (nullptr: acceleration only)
+  float4* pos_next;   // leapfrog: end-of-step positions
+  float4* dup_next;   // leapfrog, optional: expanded end-of-step sources
+  float half_dt;
+  float dt;
+};
+
+// v <- v + (dt/2) a ; x <- x + dt v   ("CUDA N-Body Simulation" §1.3)
+__device__ __forceinline__ void finish_body(const Epilogue& e, long long i, float ax, float ay,
+                                            float az) {
+  e.accel[i] = make_float4(ax, ay, az, 0.0f);
+  if (e.vel != nullptr) {
+    float4 v = e.vel[i];
+    float4 x = e.pos[i];
+    v.x = fmaf(e.half_dt, ax, v.x);
+    v.y = fmaf(e.half_dt, ay, v.y);
+    v.z = fmaf(e.half_dt, az, v.z);
+    x.x = fmaf(e.dt, v.x, x.x);
+    x.y = fmaf(e.dt, v.y, x.y);
+    x.z = fmaf(e.dt, v.z, x.z);
+    e.vel[i] = v;
+    e.pos_next[i] = x;
+    if (e.dup_next != nullptr) {
+      e.dup_next[2 * i] = make_float4(x.x, x.x, x.y, x.y);
+      e.dup_next[2 * i + 1] = make_float4(x.z, x.z, x.w, x.w);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// source expansion
+// ---------------------------------------------------------------------------
+
+// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,m,m) for i < n; zero rows for
+// n <= i < npad (zero mass adds exactly nothing).  dup2, when given, gets
+// the same zero padding (the other buffer of a multi-step call).
+__global__ void expand_sources(const float4* __restrict__ pos, float4* __restrict__ dup,
+                               float4* __restrict__ dup2, int n, long long npad) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= npad) return;
+  if (i < n) {
+    const float4 x = pos[i];
+    dup[2 * i] = make_float4(x.x, x.x, x.y, x.y);
+    dup[2 * i + 1] = make_float4(x.z, x.z, x.w, x.w);
+  } else {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    dup[2 * i] = z;
+    dup[2 * i + 1] = z;
+    if (dup2 != nullptr) {
+      dup2[2 * i] = z;
+      dup2[2 * i + 1] = z;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// tiled force kernel with an even (stream-K) division of the work
+// ---------------------------------------------------------------------------
+
+struct TiledArgs {
+  const float4* pos;  // n target rows (x, y, z, m)
+  const float4* dup;  // 2 * ntiles * TJ expanded source rows
+  int n;
+  float eps2;
+  long long ntiles;  // source tiles over n
+  long long units;   // i-blocks * ntiles
+  long long grid;    // CTAs launched
+  float4* partial;   // [grid][2][KI*NT] partial sums of split i-blocks
+  uint64_t timeout_ns;
+  long long withhold;  // failure-detection check only: this unit's copy is never issued (-1: none)
+};
+
+// First work unit of CTA c when `units` are divided over `grid` CTAs.
+__host__ __device__ __forceinline__ long long unit_begin(long long units, long long grid,
+                                                         long long c) {
+  return units * c / grid;
+}
+
+// CTA whose range holds unit u (inverse of unit_begin).
+__host__ __device__ __forceinline__ long long unit_owner(long long units, long long grid,
+                                                         long long u) {
+  return ((u + 1) * grid - 1) / units;
+}
+
+template <int KI, int NT, int TJ, int MINB>
+__global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const Epilogue e) {
+  static_assert(KI % 2 == 0, "targets are processed in packed pairs");
+  constexpr int P = KI / 2;
+  constexpr long long B = static_cast<long long>(KI) * NT;
+  constexpr uint32_t kTileBytes = TJ * 32u;
+
+  __shared__ __align__(128) float4 tile[2][2 * TJ];
+  __shared__ __align__(8) unsigned long long bar[2];
+
+  const int tid = threadIdx.x;
+  const long long c = blockIdx.x;
+  const long long u_lo = unit_begin(a.units, a.grid, c);
+  const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
+  // shared-memory addresses of stage s: base + s * stride
+  const uint32_t bar0 = smem_u32(&bar[0]);
+  const uint32_t tile0 = smem_u32(&tile[0][0]);
+  constexpr uint32_t kTileStride = sizeof(tile[0]);
+  auto bar_of = [&](long long k) { return bar0 + static_cast<uint32_t>(k & 1) * 8u; };
+  auto tile_of = [&](long long k) { return tile0 + static_cast<uint32_t>(k & 1) * kTileStride; };
+
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8u, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (count <= 0) return;
+
+  // Copy the source tile of local unit k into stage k & 1.
+  auto issue = [&](long long k) {
+    const long long t = (u_lo + k) % a.ntiles;
+    mbar_arrive_expect_tx(bar_of(k), kTileBytes);
+    bulk_copy_g2s(tile_of(k), a.dup + 2 * t * TJ, kTileBytes, bar_of(k));
+  };
+  if (tid == 0 && a.withhold != 0) issue(0);
+
+  const float2 e2 = make_float2(a.eps2, a.eps2);
+  float2 nx[P], ny[P], nz[P], ax[P], ay[P], az[P];
+  long long k = 0;
+  bool timed_out = false;
+
+  while (k < count) {
+    const long long u = u_lo + k;
+    const long long blk = u / a.ntiles;
+    const long long tb = u % a.ntiles;
+    const long long te = min(a.ntiles, tb + (count - k));
+    const bool first_segment = (k == 0);
+
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const long long i0 = blk * B + (2 * p) * NT + tid;
+      const long long i1 = i0 + NT;
+      const float4 q0 = a.pos[min(i0, static_cast<long long>(a.n - 1))];
+      const float4 q1 = a.pos[min(i1, static_cast<long long>(a.n - 1))];
+      nx[p] = make_float2(-q0.x, -q1.x);
+      ny[p] = make_float2(-q0.y, -q1.y);
+      nz[p] = make_float2(-q0.z, -q1.z);
+      ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+    }
+
+    for (long long t = tb; t < te; ++t, ++k) {
+      const int s = static_cast<int>(k & 1);
+      const uint32_t parity = static_cast<uint32_t>((k >> 1) & 1);
+      const bool ok = mbar_wait_bounded(bar_of(k), parity, a.timeout_ns);
+      // Every thread reaches this barrier in bounded time; it makes the
+      // timeout decision uniform and guarantees that all threads are done
+      // with stage s^1 (read in the previous iteration) before it is refilled.
+      if (!__syncthreads_and(ok)) {
+        timed_out = true;
+        break;
+      }
+      if (tid == 0 && k + 1 < count && k + 1 != a.withhold) issue(k + 1);
+
+      // Per-tile sums, folded into the running sums after the tile: the
+      // rounding error grows like sqrt(TJ) + sqrt(n / TJ), not sqrt(n).
+      float2 tx[P], ty[P], tz[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
+      const float4* src = tile[s];
+#pragma unroll 4
+      for (int j = 0; j < TJ; ++j) {
+        const float4 lo = src[2 * j];
+        const float4 hi = src[2 * j + 1];
+        const float2 X = make_float2(lo.x, lo.y);
+        const float2 Y = make_float2(lo.z, lo.w);
+        const float2 Z = make_float2(hi.x, hi.y);
+        const float2 M = make_float2(hi.z, hi.w);
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+          interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+      }
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        ax[p] = __fadd2_rn(ax[p], tx[p]);
+        ay[p] = __fadd2_rn(ay[p], ty[p]);
+        az[p] = __fadd2_rn(az[p], tz[p]);
+      }
+    }
+    if (timed_out) break;
+
+    const bool whole = (tb == 0 && te == a.ntiles);
+    const long long slot = (c * 2 + (first_segment ? 0 : 1)) * B;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const long long local = (2 * p + h) * NT + tid;
+        const long long i = blk * B + local;
+        if (i < a.n) {
+          const float fx = h ? ax[p].y : ax[p].x;
+          const float fy = h ? ay[p].y : ay[p].x;
+          const float fz = h ? az[p].y : az[p].x;
+          if (whole)
+            finish_body(e, i, fx, fy, fz);
+          else
+            a.partial[slot + local] = make_float4(fx, fy, fz, 0.f);
+        }
+      }
+    }
+  }
+
+  if (timed_out && tid == 0) {
+    atomicExch(&g_status, static_cast<int>(NBODY_ETIMEOUT));
+    // The copy of unit k may still be landing in shared memory: give it a
+    // bounded wait before the CTA (and its shared memory) goes away.
+    if (k != a.withhold)
+      (void)mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
+  }
+}
+
+// Second pass of the tiled kernel: one thread per body; bodies of i-blocks
+// that one CTA covered whole were finished already and return at once.
+struct StreamkFinishArgs {
+  const float4* partial;
+  int n;
+  long long block;  // target bodies per i-block (KI * NT)
+  long long ntiles;
+  long long units;
+  long long grid;
+};
+
+__global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  const long long blk = i / a.block;
+  const long long u0 = blk * a.ntiles;
+  const long long c0 = unit_owner(a.units, a.grid, u0);
+  const long long c1 = unit_owner(a.units, a.grid, u0 + a.ntiles - 1);
+  if (c0 == c1) return;
+  const long long local = i - blk * a.block;
+  float sx = 0.f, sy = 0.f, sz = 0.f;
+  for (long long c = c0; c <= c1; ++c) {
+    // the block's segment is CTA c's first segment unless c started earlier
+    const int side = unit_begin(a.units, a.grid, c) >= u0 ? 0 : 1;
+    const float4 p = a.partial[(c * 2 + side) * a.block + local];
+    sx += p.x;
+    sy += p.y;
+    sz += p.z;
+  }
+  finish_body(e, i, sx, sy, sz);
+}
+
+// ---------------------------------------------------------------------------
+// small-n warp-split kernel
+// ---------------------------------------------------------------------------
+
+struct WarpArgs {
+  const float4* pos;  // n rows (x, y, z, m): targets and sources
+  int n;
+  float eps2;
+  int slices;          // S: j slices (gridDim.y)
+  long long slice_len; // sources per slice
+  float4* partial;     // [S][n] when S > 1
+};
+
+template <int KW, int NW>
+__global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Epilogue e) {
+  static_assert(KW % 2 == 0, "targets are processed in packed pairs");
+  constexpr int P = KW / 2;
+  constexpr int NTH = NW * 32;
+  __shared__ float red[NW][3 * KW];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const long long i_base = static_cast<long long>(blockIdx.x) * KW;
+  const long long j_begin = static_cast<long long>(blockIdx.y) * a.slice_len;
+  const long long j_end = min(static_cast<long long>(a.n), j_begin + a.slice_len);
+
+  const float2 e2 = make_float2(a.eps2, a.eps2);
+  float2 nx[P], ny[P], nz[P], ax[P], ay[P], az[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const float4 q0 = a.pos[min(i_base + 2 * p, static_cast<long long>(a.n - 1))];
+    const float4 q1 = a.pos[min(i_base + 2 * p + 1, static_cast<long long>(a.n - 1))];
+    nx[p] = make_float2(-q0.x, -q1.x);
+    ny[p] = make_float2(-q0.y, -q1.y);
+    nz[p] = make_float2(-q0.z, -q1.z);
+    ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+  }
+#pragma unroll 2
+  for (long long j = j_begin + tid; j < j_end; j += NTH) {
+    const float4 b = a.pos[j];
+    const float2 X = make_float2(b.x, b.x);
+    const float2 Y = make_float2(b.y, b.y);
+    const float2 Z = make_float2(b.z, b.z);
+    const float2 M = make_float2(b.w, b.w);
+#pragma unroll
+    for (int p = 0; p < P; ++p) interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, ax[p], ay[p], az[p]);
+  }
+
+  // Combine the 32 lanes with a butterfly of shuffles (every lane ends with
+  // the same bits: each step adds the same two values), then the warps in
+  // ascending order through shared memory.
+  float v[3 * KW];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    v[6 * p + 0] = ax[p].x;
+    v[6 * p + 1] = ay[p].x;
+    v[6 * p + 2] = az[p].x;
+    v[6 * p + 3] = ax[p].y;
+    v[6 * p + 4] = ay[p].y;
+    v[6 * p + 5] = az[p].y;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int q = 0; q < 3 * KW; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < 3 * KW; ++q) red[warp][q] = v[q];
+  }
+  __syncthreads();
+  if (tid < KW) {
+    float sx = 0.f, sy = 0.f, sz = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      sx += red[w][3 * tid + 0];
+      sy += red[w][3 * tid + 1];
+      sz += red[w][3 * tid + 2];
+    }
+    const long long i = i_base + tid;
+    if (i < a.n) {
+      if (a.slices == 1)
+        finish_body(e, i, sx, sy, sz);
+      else
+        a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
+    }
+  }
+}
+
+// Second pass of the warp kernel: a_i = sum over slices s = 0..S-1 in order.
+__global__ void finish_slices(const float4* __restrict__ partial, int n, int slices,
+                              const Epilogue e) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float sx = 0.f, sy = 0.f, sz = 0.f;
+  for (int s = 0; s < slices; ++s) {
+    const float4 p = partial[static_cast<long long>(s) * n + i];
+    sx += p.x;
+    sy += p.y;
+    sz += p.z;
+  }
+  finish_body(e, i, sx, sy, sz);
+}
+
+}  // namespace nbody

@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Throughput of the all-pairs softened-gravity step on GB300, one JSON line.
+
+Workload (default): 2^20 bodies uniform in the unit ball with log-normal
+masses (total 1), seed 3, eps2 = 1e-3.  One step = one leapfrog kick/drift
+step through the C ABI: the all-pairs acceleration over every (i, j) pair
+plus the fused half-kick and drift ("CUDA N-Body Simulation" §1.2-1.3), i.e.
+N^2 body-body interactions per step.
+
+    value    = interactions of all ranks / max-over-ranks device time,
+               in billions of interactions per second (CUDA events on the
+               launching stream; L2 flushed by a 256 MiB write between steps)
+    e2e      = the same metric with host (pinned) buffers: each step copies
+               positions and velocities in, runs the step and copies
+               positions, velocities and accelerations back
+    roofline = the force kernel alone against the FP32 issue roofline
+               SMs x f_SM x 128 lanes / 12 FP32 lane-ops per interaction
+    cpu_baseline = the FP64 CPU oracle on a bounded sample of the same bodies
+
+``--impl reference`` times the FP64 CPU oracle on the host cores instead.
+Multi-GPU (torchrun) runs independent replicas, one per rank.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "body-body interactions/s (billions) at N=2^20 FP32; % of FFMA/MUFU roofline"
+UNIT = "Ginteractions/s"
+DEFAULT_WORKLOAD = "ball-lognormal-1048576"
+FLOP_PER_INTERACTION = 20  # bodybodyinteraction FLOP comments, "Cuda Nbody Notes"
+FP32_OPS_PER_INTERACTION = 12  # 3 FADD + 3 FFMA (|r|^2+eps2) + 3 FMUL (m q^3) + 3 FFMA (a += s r)
+FP32_LANES_PER_SM = 128  # per clock: 4 SM sub-partitions x 32 FP32 lanes
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "force_tiled_ball-lognormal-1048576.md")
+KERNEL_SOURCE = os.path.join(ROOT, "all_pairs_body_gb300", "csrc", "nbody_kernels.cuh")
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", choices=("step", "accel"), default="step",
+                    help="step: one leapfrog kick/drift step; accel: acceleration only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local, world
+
+
+def init_dist(world: int, use_cuda: bool):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+    return dist
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (the value itself without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def aggregate_value(per_rank_interactions: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput (billions/s): every rank does the same work."""
+    return world * per_rank_interactions / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+
+def gpu_selector(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis.strip():
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+class ClockSampler:
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.gpu],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_lines(out.splitlines())
+
+
+def parse_clock_lines(lines) -> dict | None:
+    sm, smax, power, reasons = [], [], [], set()
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax.append(float(f[2]))
+            power.append(float(f[3]))
+        except ValueError:
+            continue
+        for name, val in zip(REASON_NAMES, f[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm),
+            "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# roofline
+# ---------------------------------------------------------------------------
+
+
+def measured_sm_max_mhz(clocks: dict | None) -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["sm_max_mhz"])
+            return v, "MEASURED_PEAKS.json sm_max_mhz"
+    except (OSError, KeyError, ValueError, TypeError):
+        pass
+    if clocks and clocks.get("sm_max_mhz"):
+        return float(clocks["sm_max_mhz"]), "nvidia-smi clocks.max.sm"
+    return 2070.0, "fallback maximum SM clock"
+
+
+def alu_peak_ginter(sms: int, mhz: float) -> float:
+    """FP32 issue roofline in billions of interactions/s."""
+    return sms * mhz * 1e6 * FP32_LANES_PER_SM / FP32_OPS_PER_INTERACTION / 1e9
+
+
+def kernel_source_digest() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(n: int) -> float | None:
+    """DRAM bytes per force-kernel launch from the committed ncu summary,
+    scaled to n bodies, or None if the kernel changed since the capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    try:
+        if fields.get("kernel_source_sha256_16") != kernel_source_digest():
+            return None
+        bytes_captured = float(fields["dram_bytes_per_launch"])
+        n_captured = float(fields["n_captured"])
+    except (KeyError, ValueError):
+        return None
+    return bytes_captured * n / n_captured  # traffic grows with n (sources stay in L2)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+
+def oracle_sample_rate(pos_mass, eps2: float, seconds: float, seed: int):
+    """FP64 oracle on seeded target samples x all sources; returns
+    (Ginteractions/s, targets, threads, wall seconds)."""
+    import numpy as np
+
+    import oracle
+    n = pos_mass.shape[0]
+    rng = np.random.default_rng(seed)
+    probe = np.sort(rng.choice(n, size=min(64, n), replace=False))
+    t0 = time.perf_counter()
+    oracle.accel(pos_mass, eps2, idx=probe)
+    per_target = (time.perf_counter() - t0) / len(probe)
+    k = int(max(64, min(n, seconds / max(per_target, 1e-9))))
+    idx = np.sort(rng.choice(n, size=k, replace=False))
+    t0 = time.perf_counter()
+    oracle.accel(pos_mass, eps2, idx=idx)
+    wall = time.perf_counter() - t0
+    return k * n / wall / 1e9, k, oracle.threads(), wall
+
+
+def workload_config(w, mode: str, world: int) -> dict:
+    what = ("one leapfrog kick/drift step (all-pairs acceleration + fused half-kick and drift, "
+            f"dt={w.dt:g})" if mode == "step" else "one all-pairs acceleration evaluation")
+    return {
+        "workload": f"{w.name}: N={w.n} bodies, eps2={w.eps2:g}, seed {w.seed}; each step is {what}; "
+                    f"N^2 interactions per step",
+        "n_bodies": w.n,
+        "l2": "flushed between timed steps (256 MiB write); sources 16N bytes",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import workloads
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, True)
+    __graft_entry__.build()
+    import all_pairs_body_gb300 as nb
+
+    w = workloads.by_name(args.workload)
+    n = w.n
+    dt = w.dt
+    pm = torch.from_numpy(w.pos_mass).cuda()
+    vel = torch.from_numpy(w.vel).cuda()
+    acc = torch.empty_like(pm)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if args.mode == "step":
+            nb.leapfrog_step(pm, vel, acc, w.eps2, dt, 1)
+        else:
+            nb.accel(pm, w.eps2, out=acc)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    nb.sync()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    plan = nb.plan(n)
+
+    sampler = ClockSampler(gpu_selector(local)).start()
+    nb.profile_enable(True)
+    nb.profile_read()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    nb.sync()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    force_ms, force_launches, launches = nb.profile_read()
+    nb.profile_enable(False)
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, device="cuda")
+    interactions = float(n) * float(n)
+    value = aggregate_value(interactions * args.steps, world, total_s)
+
+    # end to end through the same API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_pm = torch.from_numpy(w.pos_mass).pin_memory()
+        h_v = torch.from_numpy(w.vel).pin_memory()
+        o_pm = torch.empty_like(h_pm).pin_memory()
+        o_v = torch.empty_like(h_v).pin_memory()
+        o_a = torch.empty_like(h_pm).pin_memory()
+        d_pm = torch.empty_like(pm)
+        d_v = torch.empty_like(vel)
+        d_a = torch.empty_like(acc)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for _ in range(args.steps):
+            d_pm.copy_(h_pm, non_blocking=True)
+            d_v.copy_(h_v, non_blocking=True)
+            if args.mode == "step":
+                nb.leapfrog_step(d_pm, d_v, d_a, w.eps2, dt, 1)
+            else:
+                nb.accel(d_pm, w.eps2, out=d_a)
+            o_pm.copy_(d_pm, non_blocking=True)
+            o_v.copy_(d_v, non_blocking=True)
+            o_a.copy_(d_a, non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        nb.sync()
+        e2e_s = reduce_max(e_start.elapsed_time(e_end) / 1e3, dist, device="cuda")
+        assert np.all(np.isfinite(o_a.numpy()))
+        e2e = {"value": aggregate_value(interactions * args.steps, world, e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * 16 * n, "d2h_bytes_per_step": 3 * 16 * n,
+               "ms_per_step": 1e3 * e2e_s / args.steps}
+
+    # roofline of the force kernel
+    sms = plan["sms"]
+    f_max, f_src = measured_sm_max_mhz(clocks)
+    achieved = interactions / (force_ms / 1e3 / force_launches) / 1e9 if force_launches else None
+    peak = alu_peak_ginter(sms, f_max)
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
+            "frac": (achieved / peak) if achieved else None,
+            "traffic": profiled_traffic(n),
+            "peak_basis": f"{sms} SMs x {f_max:g} MHz ({f_src}) x {FP32_LANES_PER_SM} FP32 lanes"
+                          f" / {FP32_OPS_PER_INTERACTION} FP32 ops per interaction",
+            "kernel": "force_tiled" if plan["path"] != nb.PATH_WARP else "force_warp",
+            "force_ms_per_launch": force_ms / force_launches if force_launches else None}
+    if clocks and achieved:
+        pc = alu_peak_ginter(sms, clocks["sm_mhz"])
+        roof["peak_at_measured_clock"] = pc
+        roof["frac_at_measured_clock"] = achieved / pc
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, k, cores, wall = oracle_sample_rate(w.pos_mass, w.eps2, args.cpu_seconds, 12345)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{k} seeded target bodies x all {n} sources, FP64, one acceleration "
+                         f"evaluation ({wall:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(w, args.mode, world),
+        "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "plan": plan, "impl": "ours",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the FP64 CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    w = workloads.by_name(args.workload)
+    n = w.n
+    # size one step so warm-up + timed steps end within a few minutes
+    per_step_s = min(8.0, 150.0 / max(1, args.steps + args.warmup))
+    rng = np.random.default_rng(777)
+    probe = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    t0 = time.perf_counter()
+    oracle.accel(w.pos_mass, w.eps2, idx=probe)
+    per_target = (time.perf_counter() - t0) / len(probe)
+    k = int(max(16, min(n, per_step_s / max(per_target, 1e-9))))
+    samples = [np.sort(rng.choice(n, size=k, replace=False)) for _ in range(args.steps + args.warmup)]
+    for s in samples[:args.warmup]:
+        oracle.accel(w.pos_mass, w.eps2, idx=s)
+    t0 = time.perf_counter()
+    for s in samples[args.warmup:]:
+        oracle.accel(w.pos_mass, w.eps2, idx=s)
+    wall = time.perf_counter() - t0
+    value = k * n * args.steps / wall / 1e9
+    sample = (f"each step: {k} seeded target bodies x all {n} sources, FP64 oracle, one "
+              f"acceleration evaluation")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args.mode, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

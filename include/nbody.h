@@ -1,0 +1,194 @@
+/*
+ * nbody.h - C ABI of the GB300 (sm_103a) all-pairs softened-gravity library.
+ *
+ * What it computes
+ *   Softened all-pairs acceleration, G = 1 ("CUDA N-Body Simulation",
+ *   §1.2 Gravitational Softening, the softened equation):
+ *       a_i = sum_{j=0}^{n-1} m_j (x_j - x_i) / (|x_j - x_i|^2 + eps2)^(3/2)
+ *   The j = i term is zero because x_i - x_i = 0 while eps2 > 0 (same
+ *   section, the remark after bodyInteractions).  One pair costs the 20
+ *   conventional FLOP counted in the comments of bodybodyinteraction
+ *   ("Cuda Nbody Notes").
+ *
+ *   Leapfrog kick/drift step ("CUDA N-Body Simulation", §1.3 Numerical Time
+ *   Integration, the two update equations):
+ *       a_i = A_i(x(t))                 for every body, from the same x(t)
+ *       v_i <- v_i + (dt/2) a_i         half-step velocity kick
+ *       x_i <- x_i + dt v_i             full-step drift with the kicked v
+ *   The section keeps the kicked velocity across launches and shows no
+ *   closing half-kick; a step here is exactly the two updates above.
+ *
+ * Data layout (all arrays are float4 rows, 16-byte aligned, row i = body i;
+ * "CUDA N-Body Simulation" §2.2 Data Structures and Memory Alignment):
+ *   pos_mass  (x, y, z, m)      FP32; m is never modified.
+ *   vel       (vx, vy, vz, w)   FP32; w is never read or modified.
+ *   accel     (ax, ay, az, 0)   FP32; written, w set to 0
+ *                               ("Cuda Nbody Notes", calculate_forces).
+ *
+ * Pointers are DEVICE pointers on the calling thread's current CUDA device
+ * (cudaMalloc / cudaMallocAsync / managed memory); host pointers are
+ * rejected with NBODY_EINVAL.  The caller owns every array it passes.  The
+ * library owns only its cached scratch (an expanded copy of the sources,
+ * the ping-pong positions of a multi-step call and the split-j partial
+ * sums), allocated on first use per (device, stream) and freed by
+ * nbody_release().
+ *
+ * Execution is asynchronous: a call validates its arguments, enqueues its
+ * kernels on the stream and returns.  NBODY_OK means "enqueued"; a device
+ * side failure (a bounded wait that expired) is reported by nbody_sync().
+ * Results are bitwise deterministic for a given (n, path, split, device
+ * model, library build): every sum runs in a fixed order and no atomics
+ * take part in any reduction.  Calls on different streams use different
+ * scratch and may run concurrently; the caller orders calls that share a
+ * stream, as usual.
+ *
+ * Errors (every entry point returns one of these codes):
+ *   NBODY_EINVAL    n < 0 or n > 2^31-1; eps2 not finite or <= 0; dt not
+ *                   finite; steps < 0; a NULL, misaligned (not 16-byte) or
+ *                   non-device pointer; accel overlapping pos_mass or vel;
+ *                   pos_mass overlapping vel; unknown path; split < 0.
+ *                   Nothing is enqueued.
+ *   NBODY_ENOMEM    scratch allocation failed.  Nothing is enqueued.
+ *   NBODY_ECUDA     no usable CUDA device, or a launch failed.
+ *   NBODY_ETIMEOUT  (nbody_sync only) a kernel's bounded wait for a tile
+ *                   copy expired; the kernel stopped and its outputs are
+ *                   undefined.  The CUDA context stays usable.
+ *   n == 0 and steps == 0 are valid no-ops that return NBODY_OK.
+ */
+#ifndef NBODY_H
+#define NBODY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nbody_status {
+    NBODY_OK = 0,
+    NBODY_EINVAL = 1,
+    NBODY_ENOMEM = 2,
+    NBODY_ECUDA = 3,
+    NBODY_ETIMEOUT = 4
+} nbody_status;
+
+/* Force-pass path for the *_with entry points. */
+typedef enum nbody_path {
+    /* Library's choice: the tiled kernel with its work (i-block, j-tile
+       pairs) divided evenly over one wave of CTAs (stream-K), or the
+       warp-split kernel for small n. */
+    NBODY_PATH_AUTO = 0,
+    /* One CTA per i-block over the whole j range; no second pass.  The
+       pages' tiled design ("CUDA N-Body Simulation" §3.1). */
+    NBODY_PATH_TILED = 1,
+    /* The j range of every i-block is cut into `split` slices handled by
+       different CTAs; a second pass sums the slices in fixed order
+       ("CUDA N-Body Simulation" §3.2-3.3, without the N x N matrix). */
+    NBODY_PATH_SPLIT = 2,
+    /* Small-n kernel: the 32 lanes of a warp share target bodies and
+       stride over sources; lanes combine by warp shuffles, warps through
+       shared memory in fixed order, CTAs through the second pass. */
+    NBODY_PATH_WARP = 3
+} nbody_path;
+
+/*
+ * accel[i] = (a_i, 0) for every i < n, a_i as defined above.
+ *   pos_mass  in   n rows (x, y, z, m); only read.
+ *   accel     out  n rows; must not overlap pos_mass.
+ *   n         number of bodies, 0 <= n <= 2^31 - 1.
+ *   eps2      softening length squared, finite and > 0.
+ * Enqueued on the legacy default stream.
+ */
+int nbody_accel(const float *pos_mass, float *accel, int64_t n, float eps2);
+
+/* nbody_accel on an explicit stream (a cudaStream_t; NULL = legacy stream). */
+int nbody_accel_on_stream(const float *pos_mass, float *accel, int64_t n,
+                          float eps2, void *cuda_stream);
+
+/*
+ * `steps` leapfrog kick/drift steps, updated in place from the caller's
+ * point of view.
+ *   pos_mass  in/out  n rows; xyz advanced, m unchanged.
+ *   vel       in/out  n rows; xyz kicked, w unchanged.
+ *   accel     out     n rows; the accelerations of the last step, i.e. at
+ *                     the positions before its drift (w = 0).
+ *   eps2, dt          finite; eps2 > 0.  steps >= 0.
+ * Within a step every acceleration uses the start-of-step positions (the
+ * new positions go to a second buffer), so no body sees a half-updated
+ * neighbour.
+ */
+int nbody_leapfrog_step(float *pos_mass, float *vel, float *accel, int64_t n,
+                        float eps2, float dt, int steps);
+
+int nbody_leapfrog_step_on_stream(float *pos_mass, float *vel, float *accel,
+                                  int64_t n, float eps2, float dt, int steps,
+                                  void *cuda_stream);
+
+/*
+ * The two calls above with an explicit force-pass path (nbody_path) and,
+ * for NBODY_PATH_SPLIT / NBODY_PATH_WARP, the number of j slices per
+ * i-block (`split` = 0 lets the library choose).  Every path computes the
+ * same sums in a different fixed order.
+ */
+int nbody_accel_with(const float *pos_mass, float *accel, int64_t n,
+                     float eps2, int path, int split, void *cuda_stream);
+
+int nbody_leapfrog_step_with(float *pos_mass, float *vel, float *accel,
+                             int64_t n, float eps2, float dt, int steps,
+                             int path, int split, void *cuda_stream);
+
+/*
+ * Wait for the stream, then report and clear the device-side status of
+ * this device: NBODY_OK, NBODY_ETIMEOUT, or NBODY_ECUDA if the stream
+ * reported a CUDA error.
+ */
+int nbody_sync(void *cuda_stream);
+
+/*
+ * Describe the launch plan a force pass over n bodies would use on the
+ * current device.  out[0..len) receives, as far as len allows:
+ *   [0] path actually used (nbody_path value)   [1] grid (CTAs)
+ *   [2] threads per CTA                         [3] target bodies per CTA
+ *   [4] source bodies per tile                  [5] tiles over n
+ *   [6] work units (i-blocks x tiles)           [7] 1 if a second pass runs
+ *   [8] kernel launches of one nbody_accel call
+ *   [9] kernel launches of one nbody_leapfrog_step call with steps = 1
+ *  [10] streaming multiprocessors on the device
+ * Returns NBODY_OK, NBODY_EINVAL or NBODY_ECUDA.
+ */
+int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
+
+/*
+ * Measurement hooks.  While enabled (nonzero), every force-kernel launch is
+ * bracketed by a pair of CUDA events recorded on its own stream, and every
+ * kernel launch of the library is counted.  nbody_profile_read waits for the
+ * recorded events and returns, since the last read (or the enable), the
+ * summed force-kernel time in milliseconds, the number of force-kernel
+ * launches and the number of all kernel launches; then it starts a new
+ * interval.  Any output pointer may be NULL.  Not thread-safe with
+ * concurrent calls on other host threads.
+ */
+int nbody_profile_enable(int enable);
+int nbody_profile_read(double *force_ms, int64_t *force_launches,
+                       int64_t *kernel_launches);
+
+/* Text of a status code (static storage; never NULL). */
+const char *nbody_strerror(int status);
+
+/* Free all cached scratch on every device (synchronises those devices). */
+void nbody_release(void);
+
+/*
+ * Failure-detection check: runs the force kernel on a tiny private problem
+ * with one tile copy deliberately never issued and a wait limit of
+ * `timeout_ms`, then waits for the stream.  A correct build returns
+ * NBODY_ETIMEOUT (the kernel gave up and returned; the context stays
+ * usable).  Allocates and frees its own small buffers.
+ */
+int nbody_selftest_timeout(int timeout_ms, void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NBODY_H */

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: exports, status texts and host-side argument checks.
+
+Every check here happens before the library touches CUDA, so these tests run
+on a machine with no GPU.  Pointers are plain integers that are never
+dereferenced (validation rejects the call first).
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import all_pairs_body_gb300 as nb
+from all_pairs_body_gb300 import build as nbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "nbody.h")
+A, B, C = 0x10000, 0x20000, 0x30000  # 16-byte aligned fake addresses, far apart
+S = ctypes.c_void_p(0)
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:  # noqa: BLE001
+        return False
+
+
+@pytest.fixture(scope="module")
+def L():
+    nbuild.build()
+    return nb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nbody_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_functions():
+    assert declared_functions() == sorted(nb.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_strerror(L):
+    for code in (nb.OK, nb.EINVAL, nb.ENOMEM, nb.ECUDA, nb.ETIMEOUT):
+        assert L.nbody_strerror(code)
+    assert nb.strerror(nb.EINVAL) == "invalid argument"
+    assert L.nbody_strerror(99) == b"unknown status"
+
+
+def accel(L, pos, acc, n, eps2, path=0, split=0):
+    return L.nbody_accel_with(ctypes.c_void_p(pos), ctypes.c_void_p(acc), n, eps2, path, split, S)
+
+
+def step(L, pos, vel, acc, n, eps2, dt, steps, path=0, split=0):
+    return L.nbody_leapfrog_step_with(ctypes.c_void_p(pos), ctypes.c_void_p(vel),
+                                      ctypes.c_void_p(acc), n, eps2, dt, steps, path, split, S)
+
+
+@pytest.mark.parametrize("n,eps2", [(-1, 0.1), (2 ** 31, 0.1), (10, 0.0), (10, -1e-3),
+                                    (10, math.nan), (10, math.inf)])
+def test_accel_bad_scalars(L, n, eps2):
+    assert accel(L, A, B, n, eps2) == nb.EINVAL
+
+
+@pytest.mark.parametrize("path,split", [(-1, 0), (4, 0), (0, -1)])
+def test_accel_bad_path(L, path, split):
+    assert accel(L, A, B, 10, 0.1, path, split) == nb.EINVAL
+
+
+@pytest.mark.parametrize("pos,acc", [(0, B), (A, 0), (A + 4, B), (A, B + 8)])
+def test_accel_bad_pointers(L, pos, acc):
+    assert accel(L, pos, acc, 10, 0.1) == nb.EINVAL
+
+
+def test_accel_overlap(L):
+    assert accel(L, A, A, 10, 0.1) == nb.EINVAL
+    assert accel(L, A, A + 16 * 9, 10, 0.1) == nb.EINVAL  # last row shared
+    assert accel(L, A + 16 * 9, A, 10, 0.1) == nb.EINVAL
+
+
+def test_accel_empty_is_noop(L):
+    assert accel(L, 0, 0, 0, 0.1) == nb.OK
+    assert L.nbody_accel(None, None, 0, ctypes.c_float(0.1)) == nb.OK
+
+
+@pytest.mark.parametrize("n,eps2,dt,steps", [(-1, 0.1, 0.1, 1), (10, 0.0, 0.1, 1),
+                                             (10, 0.1, math.nan, 1), (10, 0.1, math.inf, 1),
+                                             (10, 0.1, 0.1, -1)])
+def test_step_bad_scalars(L, n, eps2, dt, steps):
+    assert step(L, A, B, C, n, eps2, dt, steps) == nb.EINVAL
+
+
+def test_step_bad_pointers_and_overlap(L):
+    assert step(L, 0, B, C, 10, 0.1, 0.1, 1) == nb.EINVAL
+    assert step(L, A, B + 4, C, 10, 0.1, 0.1, 1) == nb.EINVAL
+    assert step(L, A, A, C, 10, 0.1, 0.1, 1) == nb.EINVAL  # pos and vel alias
+    assert step(L, A, B, B, 10, 0.1, 0.1, 1) == nb.EINVAL  # vel and accel alias
+    assert step(L, A, B, A + 16, 10, 0.1, 0.1, 1) == nb.EINVAL  # pos and accel overlap
+
+
+def test_step_noops(L):
+    assert step(L, 0, 0, 0, 0, 0.1, 0.1, 3) == nb.OK
+    assert step(L, A, B, C, 10, 0.1, 0.1, 0) == nb.OK
+    assert step(L, 0, 0, 0, 10, 0.1, 0.1, 0) == nb.OK
+    assert L.nbody_leapfrog_step(None, None, None, 0, ctypes.c_float(0.1),
+                                 ctypes.c_float(0.1), 1) == nb.OK
+
+
+def test_plan_rejects_bad_arguments(L):
+    out = (ctypes.c_int64 * 4)()
+    assert L.nbody_plan(-5, 0, 0, out, 4) == nb.EINVAL
+    assert L.nbody_plan(10, 7, 0, out, 4) == nb.EINVAL
+    assert L.nbody_plan(10, 0, 0, None, 4) == nb.EINVAL
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
+def test_no_device_is_ecuda(L):
+    assert accel(L, A, B, 10, 0.1) == nb.ECUDA
+    assert step(L, A, B, C, 10, 0.1, 0.1, 1) == nb.ECUDA
+    out = (ctypes.c_int64 * 4)()
+    assert L.nbody_plan(10, 0, 0, out, 4) == nb.ECUDA
+    assert L.nbody_selftest_timeout(10, S) in (nb.ENOMEM, nb.ECUDA)
+    L.nbody_release()  # nothing cached: must not fail
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(nb, "_lib", None)
+    monkeypatch.setattr(nb, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        nb.lib()

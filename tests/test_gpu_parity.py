@@ -1,0 +1,261 @@
+"""CUDA path against the FP64 oracle, element by element, through the C ABI.
+
+Workloads: the five benchmark configurations (full oracle up to 131072
+bodies, 4096 seeded sampled bodies above), every force-pass path forced on
+the same inputs, ragged sizes around every tile and block width, the
+degenerate cases (one body, coincident bodies, zero steps), determinism and
+step composition.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from parity import ACC_TOL, POS_TOL, VEL_TOL, gpu_accel, gpu_leapfrog, rel_err
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [(0, 0), (1, 0), (2, 0), (2, 1), (2, 3), (2, 7), (3, 0), (3, 1), (3, 5)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    from all_pairs_body_gb300 import build as nbuild
+    nbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+
+
+_REF = {}
+
+
+def oracle_accel_cached(w):
+    key = (w.name, w.n)
+    if key not in _REF:
+        _REF[key] = oracle.accel(w.pos_mass, w.eps2, idx=w.sample)
+    return _REF[key]
+
+
+def check_accel(w, path=0, split=0, tol=ACC_TOL):
+    a = gpu_accel(w.pos_mass, w.eps2, path, split)
+    assert np.all(np.isfinite(a))
+    assert np.all(a[:, 3] == 0.0), "accel.w must be 0"
+    ref = oracle_accel_cached(w)
+    got = a if w.sample is None else a[w.sample]
+    err = rel_err(got, ref)
+    assert err <= tol, f"{w.name} path={path} split={split}: err {err:.3e}"
+    return a, err
+
+
+# ---------------------------------------------------------------------------
+# the benchmark workloads
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("name", ["uniform-cube-1024", "plummer-16384", "two-plummer-131072",
+                                  "ball-lognormal-1048576", "cube-sweep-1000",
+                                  "cube-sweep-4097", "cube-sweep-65537", "cube-sweep-500000",
+                                  "cube-sweep-4194304"])
+def test_accel_workload(name):
+    check_accel(W.by_name(name))
+
+
+def test_uniform_cube_1024_step():
+    w = W.uniform_cube_1024()
+    p, v, a = gpu_leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, w.steps)
+    rp, rv, ra = oracle.leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, w.steps)
+    assert rel_err(a, ra) <= ACC_TOL
+    assert rel_err(v, rv) <= VEL_TOL
+    assert rel_err(p, rp) <= POS_TOL
+    # from rest: v_1 = (dt/2) a_0 exactly in the oracle's arithmetic
+    assert rel_err(v, 0.5 * w.dt * ra) <= VEL_TOL
+
+
+@pytest.mark.parametrize("name", ["plummer-16384", "two-plummer-131072"])
+def test_trajectory_10_steps(name):
+    w = W.by_name(name)
+    p, v, a = gpu_leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, w.steps)
+    rp, rv, ra = oracle.leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, w.steps)
+    assert rel_err(p, rp) <= POS_TOL
+    assert rel_err(v, rv) <= VEL_TOL
+    assert rel_err(a, ra) <= ACC_TOL
+    # displacement over the run, a far stricter view of the positions
+    d_gpu = p[:, :3].astype(np.float64) - w.pos_mass[:, :3]
+    d_ref = rp[:, :3] - w.pos_mass[:, :3].astype(np.float64)
+    assert rel_err(d_gpu, d_ref) <= 1e-3
+    assert np.array_equal(p[:, 3], w.pos_mass[:, 3]), "masses changed"
+    assert np.array_equal(v[:, 3], w.vel[:, 3]), "vel.w changed"
+
+
+# ---------------------------------------------------------------------------
+# every path on the same inputs
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("path,split", PATHS)
+@pytest.mark.parametrize("n", [1000, 4097, 16384, 20000])
+def test_paths_accel(n, path, split):
+    w = W.cube_sweep(n) if n != 16384 else W.plummer_16384()
+    check_accel(w, path, split)
+
+
+@pytest.mark.parametrize("path,split", PATHS)
+def test_paths_leapfrog(path, split):
+    n = 5000
+    pm = W.random_bodies(n, 21)
+    v = W.random_velocities(n, 21)
+    p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, 3, path, split)
+    rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 3)
+    assert rel_err(a, ra) <= ACC_TOL
+    assert rel_err(vv, rv) <= VEL_TOL
+    assert rel_err(p, rp) <= POS_TOL
+    assert np.array_equal(vv[:, 3], v[:, 3]) and np.array_equal(p[:, 3], pm[:, 3])
+
+
+RAGGED = [1, 2, 3, 7, 8, 9, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 513,
+          1023, 1025, 2047, 2049, 4095, 4097]
+
+
+@pytest.mark.parametrize("n", RAGGED)
+@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 0), (2, 3), (3, 0), (3, 2)])
+def test_ragged_sizes(n, path, split):
+    pm = W.random_bodies(n, 1000 + n)
+    a = gpu_accel(pm, 1e-2, path, split)
+    ref = oracle.accel(pm, 1e-2)
+    if n == 1:
+        assert np.all(a == 0.0)
+    else:
+        assert rel_err(a, ref) <= ACC_TOL, (n, path, split)
+
+
+# ---------------------------------------------------------------------------
+# closed forms and invariants on the GPU
+# ---------------------------------------------------------------------------
+
+
+def test_two_body_closed_form():
+    pm = np.array([[0.0, 0.0, 0.0, 2.0], [1.0, 0.5, -0.25, 3.0]], dtype=np.float32)
+    a = gpu_accel(pm, 0.01).astype(np.float64)
+    r = pm[1, :3].astype(np.float64) - pm[0, :3]
+    f = (r @ r + 0.01) ** -1.5
+    assert np.allclose(a[0, :3], 3.0 * f * r, rtol=2e-6, atol=0)
+    assert np.allclose(a[1, :3], -2.0 * f * r, rtol=2e-6, atol=0)
+
+
+def test_coincident_and_single_bodies():
+    pm = np.array([[0.5, 0.5, 0.5, 1.0]] * 5, dtype=np.float32)
+    for path, split in [(0, 0), (1, 0), (3, 0)]:
+        assert np.all(gpu_accel(pm, 1e-3, path, split)[:, :3] == 0.0)
+
+
+def test_momentum_invariant():
+    w = W.plummer_16384()
+    a = gpu_accel(w.pos_mass, w.eps2).astype(np.float64)
+    m = w.pos_mass[:, 3:4].astype(np.float64)
+    net = np.abs(np.sum(m * a[:, :3], axis=0)).max()
+    assert net <= 1e-5 * float(np.sum(m[:, 0] * np.linalg.norm(a[:, :3], axis=1)))
+
+
+# ---------------------------------------------------------------------------
+# determinism, composition, streams
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 5), (3, 0)])
+def test_bitwise_deterministic(path, split):
+    pm = W.cube_sweep(65537).pos_mass
+    a1 = gpu_accel(pm, 1e-3, path, split)
+    a2 = gpu_accel(pm, 1e-3, path, split)
+    assert np.array_equal(a1, a2)
+
+
+@pytest.mark.parametrize("n", [3000, 40000])
+def test_steps_compose(n):
+    pm = W.random_bodies(n, 5)
+    v = W.random_velocities(n, 5)
+    p10, v10, a10 = gpu_leapfrog(pm, v, 1e-3, 1e-3, 10)
+    p4, v4, _ = gpu_leapfrog(pm, v, 1e-3, 1e-3, 4)
+    p46, v46, a46 = gpu_leapfrog(p4, v4, 1e-3, 1e-3, 6)
+    assert np.array_equal(p10, p46) and np.array_equal(v10, v46) and np.array_equal(a10, a46)
+
+
+def test_zero_steps_is_noop():
+    pm = W.random_bodies(100, 2)
+    v = W.random_velocities(100, 2)
+    p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, 0)
+    assert np.array_equal(p, pm) and np.array_equal(vv, v) and np.all(np.isnan(a))
+
+
+def test_side_stream_matches_default_stream():
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = torch.from_numpy(W.cube_sweep(4097).pos_mass).cuda()
+    ref = nb.accel(pm, 1e-3)
+    nb.sync()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = nb.accel(pm, 1e-3)
+        nb.sync()
+    assert torch.equal(out, ref)
+
+
+def test_plan_is_consistent():
+    import all_pairs_body_gb300 as nb
+    for n in (1000, 16384, 1048576):
+        p = nb.plan(n)
+        assert p["sms"] > 0 and p["grid"] >= 1 and p["threads"] % 32 == 0
+        assert p["launches_accel"] >= 1
+    p = nb.plan(1048576, path=nb.PATH_TILED)
+    assert p["second_pass"] == 0 and p["grid"] * p["bodies_per_cta"] >= 1048576
+
+
+# ---------------------------------------------------------------------------
+# errors seen from the GPU side
+# ---------------------------------------------------------------------------
+
+
+def test_rejects_host_and_misaligned_pointers():
+    import ctypes
+    import torch
+    import all_pairs_body_gb300 as nb
+    L = nb.lib()
+    dev = torch.zeros((64, 4), device="cuda")
+    host = torch.zeros((64, 4))
+    pinned = torch.zeros((64, 4)).pin_memory()
+    out = torch.zeros((64, 4), device="cuda")
+    P = ctypes.c_void_p
+    s = P(torch.cuda.current_stream().cuda_stream)
+    assert L.nbody_accel_with(P(host.data_ptr()), P(out.data_ptr()), 64, 0.1, 0, 0, s) == nb.EINVAL
+    assert L.nbody_accel_with(P(pinned.data_ptr()), P(out.data_ptr()), 64, 0.1, 0, 0, s) == nb.EINVAL
+    flat = torch.zeros(64 * 4 + 1, device="cuda")
+    assert L.nbody_accel_with(P(flat.data_ptr() + 4), P(out.data_ptr()), 64, 0.1, 0, 0, s) == nb.EINVAL
+    assert L.nbody_accel_with(P(dev.data_ptr()), P(out.data_ptr()), 64, 0.1, 0, 0, s) == nb.OK
+    nb.sync()
+
+
+def test_allocation_failure_is_enomem(monkeypatch):
+    import torch
+    import all_pairs_body_gb300 as nb
+    nb.release()
+    pm = torch.from_numpy(W.cube_sweep(20000).pos_mass).cuda()
+    monkeypatch.setenv("NBODY_FAULT_ALLOC", "1")
+    with pytest.raises(nb.NBodyError) as ei:
+        nb.accel(pm, 1e-3)
+    assert ei.value.status == nb.ENOMEM
+    monkeypatch.delenv("NBODY_FAULT_ALLOC")
+    out = nb.accel(pm, 1e-3)
+    nb.sync()
+    assert torch.isfinite(out).all()
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    import torch
+    import all_pairs_body_gb300 as nb
+    assert nb.selftest_timeout(50) == nb.ETIMEOUT
+    nb.sync()  # status was cleared by the self test
+    pm = W.cube_sweep(4097)
+    a = gpu_accel(pm.pos_mass, pm.eps2)
+    assert rel_err(a, oracle.accel(pm.pos_mass, pm.eps2)) <= ACC_TOL
+    assert torch.cuda.is_available()

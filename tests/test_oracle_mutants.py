@@ -56,7 +56,10 @@ MUTANTS = {
     "half_drift": [("+ dt * vel[3 * i + c]", "+ 0.5 * dt * vel[3 * i + c]")],
     "drift_before_kick": [(KICK_DRIFT, DRIFT_KICK)],
     "in_place_update_race": [(STEP_LOOPS, FUSED_IN_PLACE)],
-    "mass_drifted": [("for (int c = 0; c < 3; ++c) {", "for (int c = 0; c < 4; ++c) {")],
+    # (stays in bounds: widening the drift loop to 4 columns would write past vel)
+    "mass_drifted": [("for (int c = 0; c < 3; ++c) {",
+                      "pos_mass[4 * i + 3] = pos_mass[4 * i + 3] + dt * vel[3 * i];\n"
+                      "            for (int c = 0; c < 3; ++c) {")],
     "sample_index_ignored": [("const int64_t i = idx ? idx[k] : k;", "const int64_t i = k;")],
 }
 
