@@ -33,11 +33,21 @@ struct TiledConfig {
   TiledKernel kernel;
 };
 
-// Target bodies per thread, threads per CTA, sources per tile.
+// Target bodies per thread, threads per CTA, sources per tile (kernel
+// template: + minimum CTAs per SM for the register cap, + j unroll).
 const TiledConfig kTiled[] = {
-    {8, 256, 256, force_tiled<8, 256, 256, 1>},
-    {4, 128, 128, force_tiled<4, 128, 128, 2>},
-    {2, 128, 64, force_tiled<2, 128, 64, 4>},
+    {8, 256, 256, force_tiled<8, 256, 256, 1, 4>},
+    {4, 128, 128, force_tiled<4, 128, 128, 2, 4>},
+    {2, 128, 64, force_tiled<2, 128, 64, 4, 4>},
+    {8, 128, 256, force_tiled<8, 128, 256, 2, 4>},
+    {8, 128, 256, force_tiled<8, 128, 256, 3, 4>},
+    {6, 256, 256, force_tiled<6, 256, 256, 1, 4>},
+    {4, 256, 256, force_tiled<4, 256, 256, 2, 4>},
+    {8, 256, 256, force_tiled<8, 256, 256, 1, 2>},
+    {8, 256, 256, force_tiled<8, 256, 256, 1, 8>},
+    {4, 256, 256, force_tiled<4, 256, 256, 2, 8>},
+    {6, 128, 256, force_tiled<6, 128, 256, 3, 4>},
+    {4, 128, 256, force_tiled<4, 128, 256, 4, 4>},
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
@@ -150,7 +160,7 @@ int current_device(int* dev) {
 int auto_tiled_config(long long n) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n >= 131072) return 0;
+  if (n >= 131072) return 7;  // fastest at 2^20 in a sweep of the table
   if (n >= 16384) return 1;
   return 2;
 }
@@ -563,7 +573,7 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   using namespace nbody;
   if (timeout_ms <= 0) return NBODY_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  constexpr int kCfg = 2;  // smallest tiled kernel
+  constexpr int kCfg = 2;  // smallest tiled kernel (4 KB tiles)
   const TiledConfig& tc = kTiled[kCfg];
   const long long n = static_cast<long long>(tc.ki) * tc.nt;  // one i-block
   const long long ntiles = ceil_div(n, tc.tj);

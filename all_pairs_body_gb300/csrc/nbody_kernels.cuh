@@ -8,7 +8,7 @@
 //   expand_sources      float4 (x,y,z,m) rows -> two rows (x,x,y,y),(z,z,m,m)
 //                       per body, zero-padded to whole tiles, so each source
 //                       component arrives as an already duplicated FP32 pair.
-//   force_tiled<KI,NT,TJ>
+//   force_tiled<KI,NT,TJ,MINB,UNR>
 //                       KI target bodies per thread in registers (KI/2 packed
 //                       FP32 pairs), source tiles of TJ bodies staged in
 //                       shared memory by 1-D TMA bulk copies on a two-stage
@@ -228,7 +228,7 @@ __host__ __device__ __forceinline__ long long unit_owner(long long units, long l
   return ((u + 1) * grid - 1) / units;
 }
 
-template <int KI, int NT, int TJ, int MINB>
+template <int KI, int NT, int TJ, int MINB, int UNR>
 __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const Epilogue e) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KI / 2;
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
 #pragma unroll
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
       const float4* src = tile[s];
-#pragma unroll 4
+#pragma unroll UNR
       for (int j = 0; j < TJ; ++j) {
         const float4 lo = src[2 * j];
         const float4 hi = src[2 * j + 1];

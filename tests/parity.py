@@ -26,6 +26,26 @@ def rel_err(got, ref) -> float:
     return float(diff.max(initial=0.0)) / rms
 
 
+EPS32 = 2.0 ** -23  # one float32 ulp at 1.0
+
+
+def displacement_err(p_gpu, p_ref, p0, steps: int) -> float:
+    """Displacement error over a run, beyond the float32 storage floor.
+
+    The GPU stores positions in float32 after every step, so even exact
+    arithmetic leaves up to ~one ulp of |x| per step and component.  The
+    excess of |dx_gpu - dx_ref| over steps * ulp(|x_ref|) is returned as a
+    fraction of RMS |dx_ref|.
+    """
+    p0 = np.asarray(p0, dtype=np.float64)[:, :3]
+    d_gpu = np.asarray(p_gpu, dtype=np.float64)[:, :3] - p0
+    d_ref = np.asarray(p_ref, dtype=np.float64)[:, :3] - p0
+    floor = steps * EPS32 * np.sqrt(3.0) * np.linalg.norm(np.asarray(p_ref)[:, :3], axis=1)
+    excess = np.maximum(np.linalg.norm(d_gpu - d_ref, axis=1) - floor, 0.0)
+    rms = float(np.sqrt(np.mean(np.sum(d_ref * d_ref, axis=1))))
+    return float(excess.max(initial=0.0)) / rms
+
+
 def gpu_accel(pos_mass_np, eps2, path=0, split=0):
     import torch
     import all_pairs_body_gb300 as nb
