@@ -30,7 +30,8 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_leapfrog_step", "nbody_leapfrog_step_on_stream",
            "nbody_leapfrog_step_with", "nbody_sync", "nbody_plan", "nbody_strerror",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
-           "nbody_profile_read")
+           "nbody_profile_read", "nbody_accel_noalloc")
+NOALLOC_MAX_N = 65536
 
 
 class NBodyError(RuntimeError):
@@ -56,6 +57,7 @@ def lib() -> ctypes.CDLL:
             "nbody_accel": [p, p, i64, f32],
             "nbody_accel_on_stream": [p, p, i64, f32, p],
             "nbody_accel_with": [p, p, i64, f32, i32, i32, p],
+            "nbody_accel_noalloc": [p, p, i64, f32, p],
             "nbody_leapfrog_step": [p, p, p, i64, f32, f32, i32],
             "nbody_leapfrog_step_on_stream": [p, p, p, i64, f32, f32, i32, p],
             "nbody_leapfrog_step_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
@@ -118,6 +120,21 @@ def accel(pos_mass, eps2: float, out=None, path: int = PATH_AUTO, split: int = 0
     rc = lib().nbody_accel_with(_rows(pos_mass, None, "pos_mass"), _rows(out, n, "out"), n,
                                 float(eps2), int(path), int(split), _stream(stream))
     _check(rc, "nbody_accel")
+    return out
+
+
+def accel_noalloc(pos_mass, out, eps2: float, stream=None):
+    """Accelerations into ``out`` without any allocation by the library.
+
+    For callers that must not allocate device memory when they ask for
+    accelerations; the work memory is one fixed 8 MiB array per GPU that the
+    library holds until exit.  n <= NOALLOC_MAX_N.  Calls must not overlap on
+    the GPU (they share the array).  ``out`` must be allocated by the caller.
+    """
+    n = int(pos_mass.shape[0])
+    rc = lib().nbody_accel_noalloc(_rows(pos_mass, None, "pos_mass"), _rows(out, n, "out"), n,
+                                   float(eps2), _stream(stream))
+    _check(rc, "nbody_accel_noalloc")
     return out
 
 

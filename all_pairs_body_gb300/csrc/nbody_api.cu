@@ -11,6 +11,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <algorithm>
 #include <utility>
 #include <vector>
 
@@ -433,6 +434,111 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
 }  // namespace nbody
 
 // ============================================================================
+// no-allocation variant: scratch in one fixed device array
+// ============================================================================
+
+namespace nbody {
+namespace {
+// force_tiled<4, 128, 128, 2, 4>: 512 targets per i-block, 128-source tiles.
+constexpr int kNoAllocCfg = 1;
+constexpr long long kNoAllocMaxGrid = 384;
+constexpr long long kNoAllocDupRows = 2LL * NBODY_NOALLOC_MAX_N;  // 128 divides 65536
+constexpr long long kNoAllocPartialRows = kNoAllocMaxGrid * 2 * 512;
+constexpr long long kNoAllocRows = kNoAllocDupRows + kNoAllocPartialRows;  // 8 MiB of float4
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  float4* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sms = 0;
+  int occupancy = 0;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];  // fixed table: no allocation
+}  // namespace
+}  // namespace nbody
+
+// Working memory of nbody_accel_noalloc: expanded sources, then partial sums.
+static __device__ __align__(256) float4 g_noalloc_scratch[nbody::kNoAllocRows];
+
+namespace nbody {
+namespace {
+
+// Once per device, with that device current: the device address of the
+// array (its name in host code is only a host-side stand-in), SM count and
+// the kernel's occupancy.
+int noalloc_setup(int dev, NoAllocDevice* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    int sms = 0, occ = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kTiled[kNoAllocCfg].kernel,
+                                                      kTiled[kNoAllocCfg].nt, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    d.scratch = static_cast<float4*>(ptr);
+    d.sms = sms;
+    d.occupancy = occ > 0 ? occ : 1;
+    d.ready = true;
+  }
+  *out = d;
+  return NBODY_OK;
+}
+
+int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps2,
+                       cudaStream_t st) {
+  int rc = check_scalars(n, eps2, NBODY_PATH_AUTO, 0);
+  if (rc != NBODY_OK) return rc;
+  if (n > NBODY_NOALLOC_MAX_N) return NBODY_EINVAL;
+  if (n == 0) return NBODY_OK;
+  if (pos_mass == nullptr || accel == nullptr) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !aligned16(accel)) return NBODY_EINVAL;
+  if (overlaps(pos_mass, accel, static_cast<size_t>(n) * sizeof(float4))) return NBODY_EINVAL;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return NBODY_ECUDA;
+  if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
+  NoAllocDevice d;
+  if ((rc = noalloc_setup(dev, &d)) != NBODY_OK) return rc;
+
+  const TiledConfig& tc = kTiled[kNoAllocCfg];
+  const long long block = static_cast<long long>(tc.ki) * tc.nt;
+  const long long ntiles = ceil_div(n, tc.tj);
+  const long long npad = ntiles * tc.tj;
+  const long long units = ceil_div(n, block) * ntiles;
+  // whole CTAs per SM so that every SM gets the same share, within the array
+  const long long per_sm = std::max(1LL, std::min<long long>(d.occupancy, kNoAllocMaxGrid / d.sms));
+  const long long grid = std::min(units, std::min(kNoAllocMaxGrid, per_sm * d.sms));
+  const bool second = streamk_needs_second_pass(units, grid, ntiles);
+
+  const float4* pos = reinterpret_cast<const float4*>(pos_mass);
+  float4* dup = d.scratch;
+  float4* partial = d.scratch + kNoAllocDupRows;
+  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, 0.f, 0.f};
+  // rewrites every expanded row the force kernel reads, zero padding included
+  expand_sources<<<static_cast<unsigned>(ceil_div(npad, kFinishThreads)), kFinishThreads, 0, st>>>(
+      pos, dup, nullptr, static_cast<int>(n), npad);
+  TiledArgs a{pos, dup, static_cast<int>(n), eps2, ntiles, units, grid, partial, kWaitLimitNs, -1};
+  tc.kernel<<<static_cast<unsigned>(grid), tc.nt, 0, st>>>(a, epi);
+  if (second) {
+    StreamkFinishArgs f{partial, static_cast<int>(n), block, ntiles, units, grid};
+    finish_streamk<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0, st>>>(f,
+                                                                                               epi);
+  }
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace nbody
+
+// ============================================================================
 // exported C ABI
 // ============================================================================
 
@@ -452,6 +558,11 @@ int nbody_accel_with(const float* pos_mass, float* accel, int64_t n, float eps2,
                      int split, void* cuda_stream) {
   return nbody::accel_impl(pos_mass, accel, n, eps2, path, split,
                            static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_accel_noalloc(const float* pos_mass, float* accel, int64_t n, float eps2,
+                        void* cuda_stream) {
+  return nbody::accel_noalloc_impl(pos_mass, accel, n, eps2, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_leapfrog_step(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,

@@ -145,6 +145,42 @@ int nbody_leapfrog_step_with(float *pos_mass, float *vel, float *accel,
 int nbody_sync(void *cuda_stream);
 
 /*
+ * Largest n that nbody_accel_noalloc accepts.
+ */
+#define NBODY_NOALLOC_MAX_N 65536
+
+/*
+ * nbody_accel without any memory allocation (the paper has no counterpart;
+ * this entry point exists for callers of this library).
+ *
+ * Some callers cannot allocate GPU memory at the point where they need the
+ * accelerations: code running inside a region where the CUDA allocator is
+ * off limits (for example while a stream is being captured), hosts that
+ * hand every byte of device memory to their own pool and forbid other
+ * allocations, and real-time or certified loops that ban allocation after
+ * start-up because cudaMalloc may block or synchronise.  This call computes
+ * the same accelerations as nbody_accel_on_stream, with the same argument
+ * rules, but keeps its working memory (the expanded source tiles and the
+ * split-j partial sums) in one fixed array that the library holds on every
+ * GPU that loads it, until the process exits: 8 MiB of device memory.  It
+ * calls no allocation routine of CUDA, PyTorch or the C/C++ runtime.
+ *
+ *   n must be <= NBODY_NOALLOC_MAX_N; larger n returns NBODY_EINVAL and
+ *   enqueues nothing.  All other arguments as for nbody_accel_on_stream.
+ *
+ * The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture.  All calls on a device share the one array,
+ * which keeps whatever the last call left in it; every call rewrites the
+ * parts it reads, including the zero padding of the last source tile.
+ * Two calls whose kernels overlap on the same GPU (for example on two
+ * streams without ordering between them) race on the array and give wrong
+ * results; order them (same stream, or an event).
+ */
+int nbody_accel_noalloc(const float *pos_mass, float *accel, int64_t n,
+                        float eps2, void *cuda_stream);
+
+/*
  * Describe the launch plan a force pass over n bodies would use on the
  * current device.  out[0..len) receives, as far as len allows:
  *   [0] path actually used (nbody_path value)   [1] grid (CTAs)
