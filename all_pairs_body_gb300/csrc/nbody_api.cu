@@ -31,24 +31,31 @@ using TiledKernel = void (*)(const TiledArgs, const Epilogue);
 
 struct TiledConfig {
   int ki, nt, tj;
+  int form;  // 0: rsqrt loop; 1: logarithmic loop (exact loop for flagged tiles)
   TiledKernel kernel;
 };
 
 // Target bodies per thread, threads per CTA, sources per tile (kernel
 // template: + minimum CTAs per SM for the register cap, + j unroll).
 const TiledConfig kTiled[] = {
-    {8, 256, 256, force_tiled<8, 256, 256, 1, 4>},
-    {4, 128, 128, force_tiled<4, 128, 128, 2, 4>},
-    {2, 128, 64, force_tiled<2, 128, 64, 4, 4>},
-    {8, 128, 256, force_tiled<8, 128, 256, 2, 4>},
-    {8, 128, 256, force_tiled<8, 128, 256, 3, 4>},
-    {6, 256, 256, force_tiled<6, 256, 256, 1, 4>},
-    {4, 256, 256, force_tiled<4, 256, 256, 2, 4>},
-    {8, 256, 256, force_tiled<8, 256, 256, 1, 2>},
-    {8, 256, 256, force_tiled<8, 256, 256, 1, 8>},
-    {4, 256, 256, force_tiled<4, 256, 256, 2, 8>},
-    {6, 128, 256, force_tiled<6, 128, 256, 3, 4>},
-    {4, 128, 256, force_tiled<4, 128, 256, 4, 4>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 4, 0>},
+    {4, 128, 128, 0, force_tiled<4, 128, 128, 2, 4, 0>},
+    {2, 128, 64, 0, force_tiled<2, 128, 64, 4, 4, 0>},
+    {8, 128, 256, 0, force_tiled<8, 128, 256, 2, 4, 0>},
+    {8, 128, 256, 0, force_tiled<8, 128, 256, 3, 4, 0>},
+    {6, 256, 256, 0, force_tiled<6, 256, 256, 1, 4, 0>},
+    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 4, 0>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 2, 0>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 8, 0>},
+    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 8, 0>},
+    {6, 128, 256, 0, force_tiled<6, 128, 256, 3, 4, 0>},
+    {4, 128, 256, 0, force_tiled<4, 128, 256, 4, 4, 0>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 2, 1>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 4, 1>},
+    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 2, 1>},
+    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1>},
+    {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1>},
+    {4, 256, 256, 1, force_tiled<4, 256, 256, 2, 4, 1>},
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
@@ -78,7 +85,7 @@ struct Buf {
 };
 
 struct Scratch {
-  Buf dup_a, dup_b, pos_alt, partial;
+  Buf dup_a, dup_b, pos_alt, partial, tile_exact;
 };
 
 std::mutex g_mu;
@@ -268,6 +275,8 @@ int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapf
     if (rc == NBODY_OK && leapfrog) rc = ensure(s.dup_b, dup_bytes, st);
     if (rc == NBODY_OK && p.second_pass)
       rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
+    if (rc == NBODY_OK && kTiled[p.cfg].form == 1)
+      rc = ensure(s.tile_exact, static_cast<size_t>(p.ntiles) * sizeof(int), st);
   } else if (p.second_pass) {
     rc = ensure(s.partial, static_cast<size_t>(p.slices) * n * sizeof(float4), st);
   }
@@ -315,18 +324,23 @@ int launch_status() {
 // launch sequences
 // --------------------------------------------------------------------------
 
-void launch_expand(const float4* pos, float4* dup, float4* dup2, long long n, long long npad,
-                   cudaStream_t st) {
-  const long long blocks = ceil_div(npad, kFinishThreads);
+void launch_expand(const Plan& p, const float4* pos, float4* dup, float4* dup2, int* tile_exact,
+                   long long n, cudaStream_t st) {
   count_launches(1);
-  expand_sources<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(pos, dup, dup2,
-                                                                           static_cast<int>(n), npad);
+  if (kTiled[p.cfg].form == 1) {  // one CTA per source tile
+    expand_sources<1><<<static_cast<unsigned>(p.ntiles), p.tj, 0, st>>>(
+        pos, dup, dup2, tile_exact, static_cast<int>(n), p.npad);
+  } else {
+    const long long blocks = ceil_div(p.npad, kFinishThreads);
+    expand_sources<0><<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(
+        pos, dup, dup2, nullptr, static_cast<int>(n), p.npad);
+  }
 }
 
 // One force pass (plus its second pass): sources and targets `pos`
 // (expanded copy `dup` for the tiled kernel), finished through `epi`.
-void launch_force(const Plan& p, const float4* pos, const float4* dup, long long n, float eps2,
-                  float4* partial, const Epilogue& epi, cudaStream_t st) {
+void launch_force(const Plan& p, const float4* pos, const float4* dup, const int* tile_exact,
+                  long long n, float eps2, float4* partial, const Epilogue& epi, cudaStream_t st) {
   if (p.path == NBODY_PATH_WARP) {
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
@@ -342,7 +356,8 @@ void launch_force(const Plan& p, const float4* pos, const float4* dup, long long
     }
     return;
   }
-  TiledArgs a{pos, dup, static_cast<int>(n), eps2, p.ntiles, p.units, p.grid, partial, kWaitLimitNs, -1};
+  TiledArgs a{pos,   dup,     static_cast<int>(n), eps2,         p.ntiles, p.units,
+              p.grid, partial, tile_exact,          kWaitLimitNs, -1};
   cudaEvent_t e0 = prof_event(st);
   kTiled[p.cfg].kernel<<<static_cast<unsigned>(p.grid), p.threads, 0, st>>>(a, epi);
   cudaEvent_t e1 = prof_event(st);
@@ -375,9 +390,10 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
 
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   float4* dup = static_cast<float4*>(s->dup_a.p);
-  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, 0.f, 0.f};
-  if (p.path != NBODY_PATH_WARP) launch_expand(pos, dup, nullptr, n, p.npad, st);
-  launch_force(p, pos, dup, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+  int* flags = static_cast<int*>(s->tile_exact.p);
+  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  if (p.path != NBODY_PATH_WARP) launch_expand(p, pos, dup, nullptr, flags, n, st);
+  launch_force(p, pos, dup, flags, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
   return launch_status();
 }
 
@@ -417,13 +433,15 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
   }
   float4* dup_cur = static_cast<float4*>(s->dup_a.p);
   float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
-  if (p.path != NBODY_PATH_WARP) launch_expand(cur, dup_cur, dup_nxt, n, p.npad, st);
+  int* flags = static_cast<int*>(s->tile_exact.p);
+  if (p.path != NBODY_PATH_WARP) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
   const float half_dt = 0.5f * dt;
   for (int k = 0; k < steps; ++k) {
     const bool last = (k + 1 == steps);
+    const bool chain = p.path != NBODY_PATH_WARP && !last;
     Epilogue epi{cur, reinterpret_cast<float4*>(accel), reinterpret_cast<float4*>(vel), nxt,
-                 (p.path != NBODY_PATH_WARP && !last) ? dup_nxt : nullptr, half_dt, dt};
-    launch_force(p, cur, dup_cur, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+                 chain ? dup_nxt : nullptr, chain ? dup_cur : nullptr, half_dt, dt};
+    launch_force(p, cur, dup_cur, flags, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
     std::swap(cur, nxt);
     std::swap(dup_cur, dup_nxt);
   }
@@ -439,7 +457,7 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
 
 namespace nbody {
 namespace {
-// force_tiled<4, 128, 128, 2, 4>: 512 targets per i-block, 128-source tiles.
+// force_tiled<4, 128, 128, 2, 4, 0>: 512 targets per i-block, 128-source tiles.
 constexpr int kNoAllocCfg = 1;
 constexpr long long kNoAllocMaxGrid = 384;
 constexpr long long kNoAllocDupRows = 2LL * NBODY_NOALLOC_MAX_N;  // 128 divides 65536
@@ -521,11 +539,11 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   float4* dup = d.scratch;
   float4* partial = d.scratch + kNoAllocDupRows;
-  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, 0.f, 0.f};
+  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
   // rewrites every expanded row the force kernel reads, zero padding included
-  expand_sources<<<static_cast<unsigned>(ceil_div(npad, kFinishThreads)), kFinishThreads, 0, st>>>(
-      pos, dup, nullptr, static_cast<int>(n), npad);
-  TiledArgs a{pos, dup, static_cast<int>(n), eps2, ntiles, units, grid, partial, kWaitLimitNs, -1};
+  expand_sources<0><<<static_cast<unsigned>(ceil_div(npad, kFinishThreads)), kFinishThreads, 0, st>>>(
+      pos, dup, nullptr, nullptr, static_cast<int>(n), npad);
+  TiledArgs a{pos, dup, static_cast<int>(n), eps2, ntiles, units, grid, partial, nullptr, kWaitLimitNs, -1};
   tc.kernel<<<static_cast<unsigned>(grid), tc.nt, 0, st>>>(a, epi);
   if (second) {
     StreamkFinishArgs f{partial, static_cast<int>(n), block, ntiles, units, grid};
@@ -669,7 +687,8 @@ void nbody_release(void) {
       continue;
     }
     cudaDeviceSynchronize();
-    for (nbody::Buf* b : {&kv.second.dup_a, &kv.second.dup_b, &kv.second.pos_alt, &kv.second.partial}) {
+    for (nbody::Buf* b : {&kv.second.dup_a, &kv.second.dup_b, &kv.second.pos_alt, &kv.second.partial,
+                          &kv.second.tile_exact}) {
       if (b->p != nullptr) cudaFree(b->p);
       b->p = nullptr;
       b->bytes = 0;
@@ -700,9 +719,9 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   }
   cudaMemsetAsync(pos, 0, pb, st);
   cudaMemsetAsync(dup, 0, db, st);
-  TiledArgs a{pos, dup, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr,
+  TiledArgs a{pos, dup, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr, nullptr,
               static_cast<uint64_t>(timeout_ms) * 1000000ull, 0};
-  Epilogue epi{pos, acc, nullptr, nullptr, nullptr, 0.f, 0.f};
+  Epilogue epi{pos, acc, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
   tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
   int rc = launch_status();
   const int srv = nbody_sync(cuda_stream);

@@ -8,7 +8,7 @@
 //   expand_sources      float4 (x,y,z,m) rows -> two rows (x,x,y,y),(z,z,m,m)
 //                       per body, zero-padded to whole tiles, so each source
 //                       component arrives as an already duplicated FP32 pair.
-//   force_tiled<KI,NT,TJ,MINB,UNR>
+//   force_tiled<KI,NT,TJ,MINB,UNR,FORM>
 //                       KI target bodies per thread in registers (KI/2 packed
 //                       FP32 pairs), source tiles of TJ bodies staged in
 //                       shared memory by 1-D TMA bulk copies on a two-stage
@@ -52,6 +52,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ float rsqrt_approx(float x) {
   float r;
   asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
 
@@ -137,6 +149,29 @@ __device__ __forceinline__ void interact2(float2 X, float2 Y, float2 Z, float2 M
   az = __ffma2_rn(rz, s, az);
 }
 
+// The same interaction with the mass factor and the inverse 3/2 power taken
+// through base-2 logarithms: s = m_j d^(-3/2) = 2^(L_j - 1.5 log2 d), where
+// L = (log2 m_j, log2 m_j) is stored with the source.  10 packed-pair FP32
+// instructions and 4 MUFU (2 LG2, 2 EX2) for two interactions: it moves two
+// FP32 operations per interaction onto the MUFU pipe, which has room for them.
+// Zero mass is L = -inf, which gives s = +0 exactly.
+__device__ __forceinline__ void interact2_log(float2 X, float2 Y, float2 Z, float2 L, float2 nx,
+                                              float2 ny, float2 nz, float2 e2, float2& ax,
+                                              float2& ay, float2& az) {
+  const float2 rx = __fadd2_rn(X, nx);
+  const float2 ry = __fadd2_rn(Y, ny);
+  const float2 rz = __fadd2_rn(Z, nz);
+  float2 d = __ffma2_rn(rx, rx, e2);
+  d = __ffma2_rn(ry, ry, d);
+  d = __ffma2_rn(rz, rz, d);
+  const float2 lg = make_float2(lg2_approx(d.x), lg2_approx(d.y));
+  const float2 t = __ffma2_rn(lg, make_float2(-1.5f, -1.5f), L);
+  const float2 s = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+  ax = __ffma2_rn(rx, s, ax);
+  ay = __ffma2_rn(ry, s, ay);
+  az = __ffma2_rn(rz, s, az);
+}
+
 // ---------------------------------------------------------------------------
 // finishing a body: write a_i, and for a leapfrog step kick and drift
 // ---------------------------------------------------------------------------
@@ -147,6 +182,7 @@ struct Epilogue {
   float4* vel;        // leapfrog only (nullptr: acceleration only)
   float4* pos_next;   // leapfrog: end-of-step positions
   float4* dup_next;   // leapfrog, optional: expanded end-of-step sources
+  const float4* dup;  // with dup_next: the current expanded sources (mass encoding)
   float half_dt;
   float dt;
 };
@@ -166,9 +202,10 @@ __device__ __forceinline__ void finish_body(const Epilogue& e, long long i, floa
     x.z = fmaf(e.dt, v.z, x.z);
     e.vel[i] = v;
     e.pos_next[i] = x;
-    if (e.dup_next != nullptr) {
+    if (e.dup_next != nullptr) {  // masses do not move: keep this body's mass encoding
+      const float4 enc = e.dup[2 * i + 1];
       e.dup_next[2 * i] = make_float4(x.x, x.x, x.y, x.y);
-      e.dup_next[2 * i + 1] = make_float4(x.z, x.z, x.w, x.w);
+      e.dup_next[2 * i + 1] = make_float4(x.z, x.z, enc.z, enc.w);
     }
   }
 }
@@ -177,25 +214,38 @@ __device__ __forceinline__ void finish_body(const Epilogue& e, long long i, floa
 // source expansion
 // ---------------------------------------------------------------------------
 
-// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,m,m) for i < n; zero rows for
-// n <= i < npad (zero mass adds exactly nothing).  dup2, when given, gets
-// the same zero padding (the other buffer of a multi-step call).
+// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,w,w) for i < npad, where w encodes
+// the mass m (zero for the padding rows n <= i < npad, which add exactly
+// nothing):
+//   FORM 0: w = m.
+//   FORM 1: w = log2 m (-inf for m = 0), for the logarithmic inner loop;
+//           one CTA per source tile (blockDim.x == tile width), and a tile
+//           holding any negative or NaN mass keeps w = m and sets
+//           tile_exact[tile] = 1 so the force kernel takes the exact loop.
+// dup2, when given, receives the same padding rows (the other buffer of a
+// multi-step call, whose real rows the step epilogue writes).
+template <int FORM>
 __global__ void expand_sources(const float4* __restrict__ pos, float4* __restrict__ dup,
-                               float4* __restrict__ dup2, int n, long long npad) {
+                               float4* __restrict__ dup2, int* __restrict__ tile_exact, int n,
+                               long long npad) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool live = i < n;
+  const float4 x = live ? pos[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float w = x.w;
+  if (FORM == 1) {
+    const bool odd_mass = live && !(x.w >= 0.0f);  // negative or NaN
+    const bool exact = __syncthreads_or(odd_mass) != 0;
+    if (threadIdx.x == 0) tile_exact[blockIdx.x] = exact ? 1 : 0;
+    if (!exact) w = x.w > 0.0f ? log2f(x.w) : -INFINITY;
+  }
   if (i >= npad) return;
-  if (i < n) {
-    const float4 x = pos[i];
-    dup[2 * i] = make_float4(x.x, x.x, x.y, x.y);
-    dup[2 * i + 1] = make_float4(x.z, x.z, x.w, x.w);
-  } else {
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    dup[2 * i] = z;
-    dup[2 * i + 1] = z;
-    if (dup2 != nullptr) {
-      dup2[2 * i] = z;
-      dup2[2 * i + 1] = z;
-    }
+  const float4 r0 = make_float4(x.x, x.x, x.y, x.y);
+  const float4 r1 = make_float4(x.z, x.z, w, w);
+  dup[2 * i] = r0;
+  dup[2 * i + 1] = r1;
+  if (!live && dup2 != nullptr) {
+    dup2[2 * i] = r0;
+    dup2[2 * i + 1] = r1;
   }
 }
 
@@ -212,6 +262,7 @@ struct TiledArgs {
   long long units;   // i-blocks * ntiles
   long long grid;    // CTAs launched
   float4* partial;   // [grid][2][KI*NT] partial sums of split i-blocks
+  const int* tile_exact;  // FORM 1: per source tile, 1 = take the exact loop
   uint64_t timeout_ns;
   long long withhold;  // failure-detection check only: this unit's copy is never issued (-1: none)
 };
@@ -228,7 +279,7 @@ __host__ __device__ __forceinline__ long long unit_owner(long long units, long l
   return ((u + 1) * grid - 1) / units;
 }
 
-template <int KI, int NT, int TJ, int MINB, int UNR>
+template <int KI, int NT, int TJ, int MINB, int UNR, int FORM>
 __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const Epilogue e) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KI / 2;
@@ -308,17 +359,32 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
 #pragma unroll
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
       const float4* src = tile[s];
+      if (FORM == 1 && a.tile_exact[t] == 0) {
 #pragma unroll UNR
-      for (int j = 0; j < TJ; ++j) {
-        const float4 lo = src[2 * j];
-        const float4 hi = src[2 * j + 1];
-        const float2 X = make_float2(lo.x, lo.y);
-        const float2 Y = make_float2(lo.z, lo.w);
-        const float2 Z = make_float2(hi.x, hi.y);
-        const float2 M = make_float2(hi.z, hi.w);
+        for (int j = 0; j < TJ; ++j) {
+          const float4 lo = src[2 * j];
+          const float4 hi = src[2 * j + 1];
+          const float2 X = make_float2(lo.x, lo.y);
+          const float2 Y = make_float2(lo.z, lo.w);
+          const float2 Z = make_float2(hi.x, hi.y);
+          const float2 L = make_float2(hi.z, hi.w);
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-          interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+          for (int p = 0; p < P; ++p)
+            interact2_log(X, Y, Z, L, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+        }
+      } else {
+#pragma unroll UNR
+        for (int j = 0; j < TJ; ++j) {
+          const float4 lo = src[2 * j];
+          const float4 hi = src[2 * j + 1];
+          const float2 X = make_float2(lo.x, lo.y);
+          const float2 Y = make_float2(lo.z, lo.w);
+          const float2 Z = make_float2(hi.x, hi.y);
+          const float2 M = make_float2(hi.z, hi.w);
+#pragma unroll
+          for (int p = 0; p < P; ++p)
+            interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+        }
       }
 #pragma unroll
       for (int p = 0; p < P; ++p) {
