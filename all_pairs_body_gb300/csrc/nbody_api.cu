@@ -31,31 +31,33 @@ using TiledKernel = void (*)(const TiledArgs, const Epilogue);
 
 struct TiledConfig {
   int ki, nt, tj;
-  int form;  // 0: rsqrt loop; 1: logarithmic loop (exact loop for flagged tiles)
+  int form;  // 0: rsqrt loop; 1: mixed rsqrt/logarithmic loop (rsqrt for flagged tiles)
   TiledKernel kernel;
 };
 
 // Target bodies per thread, threads per CTA, sources per tile (kernel
 // template: + minimum CTAs per SM for the register cap, + j unroll).
 const TiledConfig kTiled[] = {
-    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 4, 0>},
-    {4, 128, 128, 0, force_tiled<4, 128, 128, 2, 4, 0>},
-    {2, 128, 64, 0, force_tiled<2, 128, 64, 4, 4, 0>},
-    {8, 128, 256, 0, force_tiled<8, 128, 256, 2, 4, 0>},
-    {8, 128, 256, 0, force_tiled<8, 128, 256, 3, 4, 0>},
-    {6, 256, 256, 0, force_tiled<6, 256, 256, 1, 4, 0>},
-    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 4, 0>},
-    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 2, 0>},
-    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 8, 0>},
-    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 8, 0>},
-    {6, 128, 256, 0, force_tiled<6, 128, 256, 3, 4, 0>},
-    {4, 128, 256, 0, force_tiled<4, 128, 256, 4, 4, 0>},
-    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 2, 1>},
-    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 4, 1>},
-    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 2, 1>},
-    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1>},
-    {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1>},
-    {4, 256, 256, 1, force_tiled<4, 256, 256, 2, 4, 1>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 4, 0, 0>},
+    {4, 128, 128, 0, force_tiled<4, 128, 128, 2, 4, 0, 0>},
+    {2, 128, 64, 0, force_tiled<2, 128, 64, 4, 4, 0, 0>},
+    {8, 128, 256, 0, force_tiled<8, 128, 256, 2, 4, 0, 0>},
+    {8, 128, 256, 0, force_tiled<8, 128, 256, 3, 4, 0, 0>},
+    {6, 256, 256, 0, force_tiled<6, 256, 256, 1, 4, 0, 0>},
+    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 4, 0, 0>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 2, 0, 0>},
+    {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 8, 0, 0>},
+    {4, 256, 256, 0, force_tiled<4, 256, 256, 2, 8, 0, 0>},
+    {6, 128, 256, 0, force_tiled<6, 128, 256, 3, 4, 0, 0>},
+    {4, 128, 256, 0, force_tiled<4, 128, 256, 4, 4, 0, 0>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 2, 1, 2>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 2, 1, 3>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 2, 1, 4>},
+    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 2, 1, 2>},
+    {8, 256, 256, 1, force_tiled<8, 256, 256, 1, 4, 1, 2>},
+    {4, 256, 256, 1, force_tiled<4, 256, 256, 2, 4, 1, 1>},
+    {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1, 2>},
+    {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1, 2>},
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
@@ -457,7 +459,7 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
 
 namespace nbody {
 namespace {
-// force_tiled<4, 128, 128, 2, 4, 0>: 512 targets per i-block, 128-source tiles.
+// force_tiled<4, 128, 128, 2, 4, 0, 0>: 512 targets per i-block, 128-source tiles.
 constexpr int kNoAllocCfg = 1;
 constexpr long long kNoAllocMaxGrid = 384;
 constexpr long long kNoAllocDupRows = 2LL * NBODY_NOALLOC_MAX_N;  // 128 divides 65536

@@ -8,7 +8,7 @@
 //   expand_sources      float4 (x,y,z,m) rows -> two rows (x,x,y,y),(z,z,m,m)
 //                       per body, zero-padded to whole tiles, so each source
 //                       component arrives as an already duplicated FP32 pair.
-//   force_tiled<KI,NT,TJ,MINB,UNR,FORM>
+//   force_tiled<KI,NT,TJ,MINB,UNR,FORM,NLOG>
 //                       KI target bodies per thread in registers (KI/2 packed
 //                       FP32 pairs), source tiles of TJ bodies staged in
 //                       shared memory by 1-D TMA bulk copies on a two-stage
@@ -149,13 +149,10 @@ __device__ __forceinline__ void interact2(float2 X, float2 Y, float2 Z, float2 M
   az = __ffma2_rn(rz, s, az);
 }
 
-// The same interaction with the mass factor and the inverse 3/2 power taken
-// through base-2 logarithms: s = m_j d^(-3/2) = 2^(L_j - 1.5 log2 d), where
-// L = (log2 m_j, log2 m_j) is stored with the source.  10 packed-pair FP32
-// instructions and 4 MUFU (2 LG2, 2 EX2) for two interactions: it moves two
-// FP32 operations per interaction onto the MUFU pipe, which has room for them.
-// Zero mass is L = -inf, which gives s = +0 exactly.
-__device__ __forceinline__ void interact2_log(float2 X, float2 Y, float2 Z, float2 L, float2 nx,
+// The interaction with a scalar source mass m (both targets see the same
+// source): the mass factor costs two scalar multiplies on the FMA pipe, the
+// same pipe time as one packed multiply, and needs no duplicated register.
+__device__ __forceinline__ void interact2_rsq(float2 X, float2 Y, float2 Z, float m, float2 nx,
                                               float2 ny, float2 nz, float2 e2, float2& ax,
                                               float2& ay, float2& az) {
   const float2 rx = __fadd2_rn(X, nx);
@@ -164,9 +161,31 @@ __device__ __forceinline__ void interact2_log(float2 X, float2 Y, float2 Z, floa
   float2 d = __ffma2_rn(rx, rx, e2);
   d = __ffma2_rn(ry, ry, d);
   d = __ffma2_rn(rz, rz, d);
-  const float2 lg = make_float2(lg2_approx(d.x), lg2_approx(d.y));
-  const float2 t = __ffma2_rn(lg, make_float2(-1.5f, -1.5f), L);
-  const float2 s = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+  const float2 q = make_float2(rsqrt_approx(d.x), rsqrt_approx(d.y));
+  const float2 q2 = __fmul2_rn(q, q);
+  const float2 s = __fmul2_rn(make_float2(m * q.x, m * q.y), q2);
+  ax = __ffma2_rn(rx, s, ax);
+  ay = __ffma2_rn(ry, s, ay);
+  az = __ffma2_rn(rz, s, az);
+}
+
+// The interaction with the mass factor and the inverse 3/2 power taken
+// through base-2 logarithms: s = m_j d^(-3/2) = 2^(L_j - 1.5 log2 d), with
+// L_j = log2 m_j stored with the source (-inf for m_j = 0, which gives s = +0
+// exactly).  Two FP32 operations per interaction fewer than interact2 on the
+// FMA pipe, in exchange for one more MUFU; mixing the two forms balances the
+// FMA and MUFU pipes.
+__device__ __forceinline__ void interact2_lg(float2 X, float2 Y, float2 Z, float L, float2 nx,
+                                             float2 ny, float2 nz, float2 e2, float2& ax,
+                                             float2& ay, float2& az) {
+  const float2 rx = __fadd2_rn(X, nx);
+  const float2 ry = __fadd2_rn(Y, ny);
+  const float2 rz = __fadd2_rn(Z, nz);
+  float2 d = __ffma2_rn(rx, rx, e2);
+  d = __ffma2_rn(ry, ry, d);
+  d = __ffma2_rn(rz, rz, d);
+  const float2 s = make_float2(ex2_approx(fmaf(lg2_approx(d.x), -1.5f, L)),
+                               ex2_approx(fmaf(lg2_approx(d.y), -1.5f, L)));
   ax = __ffma2_rn(rx, s, ax);
   ay = __ffma2_rn(ry, s, ay);
   az = __ffma2_rn(rz, s, az);
@@ -214,14 +233,14 @@ __device__ __forceinline__ void finish_body(const Epilogue& e, long long i, floa
 // source expansion
 // ---------------------------------------------------------------------------
 
-// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,w,w) for i < npad, where w encodes
-// the mass m (zero for the padding rows n <= i < npad, which add exactly
-// nothing):
-//   FORM 0: w = m.
-//   FORM 1: w = log2 m (-inf for m = 0), for the logarithmic inner loop;
-//           one CTA per source tile (blockDim.x == tile width), and a tile
-//           holding any negative or NaN mass keeps w = m and sets
-//           tile_exact[tile] = 1 so the force kernel takes the exact loop.
+// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,w0,w1) for i < npad, where (w0, w1)
+// encode the mass m (zero rows for the padding n <= i < npad, which add
+// exactly nothing):
+//   FORM 0: (m, m).
+//   FORM 1: (m, log2 m), log2 0 = -inf, for the mixed inner loop; one CTA
+//           per source tile (blockDim.x == tile width), and a tile holding
+//           any negative or NaN mass sets tile_exact[tile] = 1 so the force
+//           kernel runs the rsqrt form on all of it.
 // dup2, when given, receives the same padding rows (the other buffer of a
 // multi-step call, whose real rows the step epilogue writes).
 template <int FORM>
@@ -231,16 +250,16 @@ __global__ void expand_sources(const float4* __restrict__ pos, float4* __restric
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool live = i < n;
   const float4 x = live ? pos[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float w = x.w;
+  float w1 = x.w;
   if (FORM == 1) {
     const bool odd_mass = live && !(x.w >= 0.0f);  // negative or NaN
     const bool exact = __syncthreads_or(odd_mass) != 0;
     if (threadIdx.x == 0) tile_exact[blockIdx.x] = exact ? 1 : 0;
-    if (!exact) w = x.w > 0.0f ? log2f(x.w) : -INFINITY;
+    w1 = x.w > 0.0f ? log2f(x.w) : (x.w == 0.0f ? -INFINITY : x.w);
   }
   if (i >= npad) return;
   const float4 r0 = make_float4(x.x, x.x, x.y, x.y);
-  const float4 r1 = make_float4(x.z, x.z, w, w);
+  const float4 r1 = make_float4(x.z, x.z, x.w, w1);
   dup[2 * i] = r0;
   dup[2 * i + 1] = r1;
   if (!live && dup2 != nullptr) {
@@ -262,7 +281,7 @@ struct TiledArgs {
   long long units;   // i-blocks * ntiles
   long long grid;    // CTAs launched
   float4* partial;   // [grid][2][KI*NT] partial sums of split i-blocks
-  const int* tile_exact;  // FORM 1: per source tile, 1 = take the exact loop
+  const int* tile_exact;  // FORM 1: per source tile, 1 = rsqrt form for all pairs
   uint64_t timeout_ns;
   long long withhold;  // failure-detection check only: this unit's copy is never issued (-1: none)
 };
@@ -279,7 +298,7 @@ __host__ __device__ __forceinline__ long long unit_owner(long long units, long l
   return ((u + 1) * grid - 1) / units;
 }
 
-template <int KI, int NT, int TJ, int MINB, int UNR, int FORM>
+template <int KI, int NT, int TJ, int MINB, int UNR, int FORM, int NLOG>
 __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const Epilogue e) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KI / 2;
@@ -360,6 +379,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
       const float4* src = tile[s];
       if (FORM == 1 && a.tile_exact[t] == 0) {
+        // mixed form: the first NLOG target pairs take the logarithmic form
 #pragma unroll UNR
         for (int j = 0; j < TJ; ++j) {
           const float4 lo = src[2 * j];
@@ -367,10 +387,25 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
           const float2 X = make_float2(lo.x, lo.y);
           const float2 Y = make_float2(lo.z, lo.w);
           const float2 Z = make_float2(hi.x, hi.y);
-          const float2 L = make_float2(hi.z, hi.w);
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            if (p < NLOG)
+              interact2_lg(X, Y, Z, hi.w, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+            else
+              interact2_rsq(X, Y, Z, hi.z, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+          }
+        }
+      } else if (FORM == 1) {
+#pragma unroll UNR
+        for (int j = 0; j < TJ; ++j) {
+          const float4 lo = src[2 * j];
+          const float4 hi = src[2 * j + 1];
+          const float2 X = make_float2(lo.x, lo.y);
+          const float2 Y = make_float2(lo.z, lo.w);
+          const float2 Z = make_float2(hi.x, hi.y);
 #pragma unroll
           for (int p = 0; p < P; ++p)
-            interact2_log(X, Y, Z, L, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+            interact2_rsq(X, Y, Z, hi.z, nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
         }
       } else {
 #pragma unroll UNR

@@ -265,7 +265,7 @@ def test_bounded_wait_times_out_and_context_survives():
 # every kernel variant of the tuning table, and the logarithmic inner loop
 # ---------------------------------------------------------------------------
 
-N_TILED_VARIANTS = 18
+N_TILED_VARIANTS = 20
 
 
 @pytest.mark.parametrize("cfg", range(N_TILED_VARIANTS))
@@ -285,7 +285,7 @@ def special_masses(n, seed):
     return pm
 
 
-@pytest.mark.parametrize("cfg", [7, 12, 14])
+@pytest.mark.parametrize("cfg", [7, 12, 14, 17])
 def test_zero_masses(cfg, monkeypatch):
     monkeypatch.setenv("NBODY_TILED_CONFIG", str(cfg))
     pm = special_masses(20000, 5)
@@ -299,7 +299,7 @@ def test_zero_masses(cfg, monkeypatch):
     assert np.all(a[123, :3] == 0.0)
 
 
-@pytest.mark.parametrize("cfg", [7, 12])
+@pytest.mark.parametrize("cfg", [7, 12, 14])
 def test_negative_masses_take_the_exact_loop(cfg, monkeypatch):
     monkeypatch.setenv("NBODY_TILED_CONFIG", str(cfg))
     pm = W.random_bodies(20000, 6)
