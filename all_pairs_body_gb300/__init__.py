@@ -30,7 +30,8 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_leapfrog_step", "nbody_leapfrog_step_on_stream",
            "nbody_leapfrog_step_with", "nbody_sync", "nbody_plan", "nbody_strerror",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
-           "nbody_profile_read", "nbody_accel_noalloc")
+           "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
+           "nbody_leapfrog_kdk_with", "nbody_render_points")
 NOALLOC_MAX_N = 65536
 
 
@@ -61,6 +62,9 @@ def lib() -> ctypes.CDLL:
             "nbody_leapfrog_step": [p, p, p, i64, f32, f32, i32],
             "nbody_leapfrog_step_on_stream": [p, p, p, i64, f32, f32, i32, p],
             "nbody_leapfrog_step_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
+            "nbody_leapfrog_kdk_on_stream": [p, p, p, i64, f32, f32, i32, p],
+            "nbody_leapfrog_kdk_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
+            "nbody_render_points": [p, p, p, i64, f32, f32, f32, f32, f32, p],
             "nbody_sync": [p],
             "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
             "nbody_selftest_timeout": [i32, p],
@@ -147,6 +151,35 @@ def leapfrog_step(pos_mass, vel, accel_out, eps2: float, dt: float, steps: int =
         _rows(pos_mass, None, "pos_mass"), _rows(vel, n, "vel"), _rows(accel_out, n, "accel"),
         n, float(eps2), float(dt), int(steps), int(path), int(split), _stream(stream))
     _check(rc, "nbody_leapfrog_step")
+
+
+def leapfrog_kdk(pos_mass, vel, accel_out, eps2: float, dt: float, steps: int = 1,
+                 path: int = PATH_AUTO, split: int = 0, stream=None) -> None:
+    """``steps`` kick-drift-kick steps in place; ``accel_out`` receives the
+    accelerations at the final positions."""
+    n = int(pos_mass.shape[0])
+    rc = lib().nbody_leapfrog_kdk_with(
+        _rows(pos_mass, None, "pos_mass"), _rows(vel, n, "vel"), _rows(accel_out, n, "accel"),
+        n, float(eps2), float(dt), int(steps), int(path), int(split), _stream(stream))
+    _check(rc, "nbody_leapfrog_kdk")
+
+
+def render_points(pos_mass, max_xyz, min_w: float, max_w: float, ndc=None, rgba=None,
+                  stream=None):
+    """Normalised device coordinates and mass colours of all bodies (the
+    pages' point shaders as a kernel); returns (ndc, rgba), (n, 4) each."""
+    import torch
+    n = int(pos_mass.shape[0])
+    if ndc is None:
+        ndc = torch.empty_like(pos_mass)
+    if rgba is None:
+        rgba = torch.empty_like(pos_mass)
+    mx, my, mz = (float(v) for v in max_xyz)
+    rc = lib().nbody_render_points(_rows(pos_mass, None, "pos_mass"), _rows(ndc, n, "ndc"),
+                                   _rows(rgba, n, "rgba"), n, mx, my, mz, float(min_w),
+                                   float(max_w), _stream(stream))
+    _check(rc, "nbody_render_points")
+    return ndc, rgba
 
 
 def sync(stream=None) -> None:

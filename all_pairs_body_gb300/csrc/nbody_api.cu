@@ -450,6 +450,99 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
   return launch_status();
 }
 
+// Kick-drift-kick: steps + 1 force passes.  Pass 0 half-kicks and drifts,
+// passes 1..steps-1 kick by a full dt (the closing half kick of one step and
+// the opening half kick of the next, fused) and drift, the last pass only
+// half-kicks with the accelerations at the final positions.
+int leapfrog_kdk_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
+                      int steps, int path, int split, cudaStream_t st) {
+  int rc = check_scalars(n, eps2, path, split);
+  if (rc != NBODY_OK) return rc;
+  if (!std::isfinite(dt) || steps < 0) return NBODY_EINVAL;
+  if (n == 0 || steps == 0) return NBODY_OK;
+  if (pos_mass == nullptr || vel == nullptr || accel == nullptr) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !aligned16(vel) || !aligned16(accel)) return NBODY_EINVAL;
+  const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
+  if (overlaps(pos_mass, accel, bytes) || overlaps(vel, accel, bytes) ||
+      overlaps(pos_mass, vel, bytes))
+    return NBODY_EINVAL;
+  int dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(vel, dev)) != NBODY_OK) return rc;
+  if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
+  Plan p;
+  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
+  Scratch* s = nullptr;
+  if ((rc = get_scratch(dev, st, p, n, true, &s)) != NBODY_OK) return rc;
+
+  float4* user = reinterpret_cast<float4*>(pos_mass);
+  float4* alt = static_cast<float4*>(s->pos_alt.p);
+  float4* cur = user;
+  float4* nxt = alt;
+  if (steps & 1) {  // `steps` drifts then end in the caller's buffer
+    if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
+      cudaGetLastError();
+      return NBODY_ECUDA;
+    }
+    cur = alt;
+    nxt = user;
+  }
+  const bool tiled = p.path != NBODY_PATH_WARP;
+  float4* dup_cur = static_cast<float4*>(s->dup_a.p);
+  float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
+  int* flags = static_cast<int*>(s->tile_exact.p);
+  if (tiled) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
+  float4* acc = reinterpret_cast<float4*>(accel);
+  float4* v = reinterpret_cast<float4*>(vel);
+  float4* partial = static_cast<float4*>(s->partial.p);
+  for (int k = 0; k < steps; ++k) {
+    Epilogue epi{cur, acc, v, nxt, tiled ? dup_nxt : nullptr, tiled ? dup_cur : nullptr,
+                 k == 0 ? 0.5f * dt : dt, dt};
+    launch_force(p, cur, dup_cur, flags, n, eps2, partial, epi, st);
+    std::swap(cur, nxt);
+    std::swap(dup_cur, dup_nxt);
+  }
+  Epilogue last{cur, acc, v, nullptr, nullptr, nullptr, 0.5f * dt, dt};
+  launch_force(p, cur, dup_cur, flags, n, eps2, partial, last, st);
+  return launch_status();
+}
+
+int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float max_x,
+                float max_y, float max_z, float min_w, float max_w, cudaStream_t st) {
+  if (n < 0 || n > static_cast<int64_t>(INT32_MAX)) return NBODY_EINVAL;
+  for (float lim : {max_x, max_y, max_z})
+    if (!std::isfinite(lim) || !(lim > 0.0f)) return NBODY_EINVAL;
+  if (!std::isfinite(min_w) || !std::isfinite(max_w) || !(max_w > min_w)) return NBODY_EINVAL;
+  if (n == 0) return NBODY_OK;
+  if (pos_mass == nullptr || ndc == nullptr || rgba == nullptr) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !aligned16(ndc) || !aligned16(rgba)) return NBODY_EINVAL;
+  const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
+  if (overlaps(pos_mass, ndc, bytes) || overlaps(pos_mass, rgba, bytes) || overlaps(ndc, rgba, bytes))
+    return NBODY_EINVAL;
+  int rc = NBODY_OK, dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  for (const void* ptr : {static_cast<const void*>(pos_mass), static_cast<const void*>(ndc),
+                          static_cast<const void*>(rgba)})
+    if ((rc = check_device_pointer(ptr, dev)) != NBODY_OK) return rc;
+  DeviceInfo d;
+  if ((rc = device_info(dev, &d)) != NBODY_OK) return rc;
+  RenderArgs a;
+  a.pos = reinterpret_cast<const float4*>(pos_mass);
+  a.ndc = reinterpret_cast<float4*>(ndc);
+  a.rgba = reinterpret_cast<float4*>(rgba);
+  a.n = n;
+  a.lim = make_float3(max_x, max_y, max_z);
+  a.scale = make_float3(static_cast<float>(2.0 / (2.0 * max_x)), static_cast<float>(2.0 / (2.0 * max_y)),
+                        static_cast<float>(2.0 / (2.0 * max_z)));
+  a.min_w = min_w;
+  a.inv_range = static_cast<float>(1.0 / (static_cast<double>(max_w) - min_w));
+  const long long blocks = std::min(ceil_div(n, 256), static_cast<long long>(d.sms) * 8);
+  count_launches(1);
+  render_points<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace nbody
 
@@ -601,6 +694,24 @@ int nbody_leapfrog_step_with(float* pos_mass, float* vel, float* accel, int64_t 
                              float dt, int steps, int path, int split, void* cuda_stream) {
   return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split,
                               static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_leapfrog_kdk_on_stream(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
+                                 float dt, int steps, void* cuda_stream) {
+  return nbody::leapfrog_kdk_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                                  static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_leapfrog_kdk_with(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
+                            float dt, int steps, int path, int split, void* cuda_stream) {
+  return nbody::leapfrog_kdk_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split,
+                                  static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_render_points(const float* pos_mass, float* ndc, float* rgba, int64_t n, float max_x,
+                        float max_y, float max_z, float min_w, float max_w, void* cuda_stream) {
+  return nbody::render_impl(pos_mass, ndc, rgba, n, max_x, max_y, max_z, min_w, max_w,
+                            static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_sync(void* cuda_stream) {

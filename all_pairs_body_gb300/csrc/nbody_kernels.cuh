@@ -23,6 +23,9 @@
 //                       threads stride over one j slice; warp shuffles then
 //                       shared memory (fixed order) combine the threads.
 //   finish_slices       second pass for the warp kernel: sums S slices in order.
+//   render_points       the point shaders of "CUDA N-Body Simulation" §4.3 as a
+//                       kernel: normalised device coordinates and mass colour
+//                       of every body into a device buffer (no graphics API).
 //
 // The pages' tiled kernel ("CUDA N-Body Simulation" §3.1, "Cuda Nbody Notes"
 // calculate_forces, The CUDA Handbook ch. 14 shared-memory kernel) keeps one
@@ -198,28 +201,33 @@ __device__ __forceinline__ void interact2_lg(float2 X, float2 Y, float2 Z, float
 struct Epilogue {
   const float4* pos;  // start-of-step positions (x, y, z, m)
   float4* accel;      // out: (ax, ay, az, 0)
-  float4* vel;        // leapfrog only (nullptr: acceleration only)
-  float4* pos_next;   // leapfrog: end-of-step positions
-  float4* dup_next;   // leapfrog, optional: expanded end-of-step sources
+  float4* vel;        // step only (nullptr: acceleration only)
+  float4* pos_next;   // step with a drift: end-of-step positions (nullptr: kick only)
+  float4* dup_next;   // optional: expanded end-of-step sources
   const float4* dup;  // with dup_next: the current expanded sources (mass encoding)
-  float half_dt;
-  float dt;
+  float kick;         // velocity kick coefficient on a (dt/2 for a half kick)
+  float dt;           // drift coefficient on v
 };
 
-// v <- v + (dt/2) a ; x <- x + dt v   ("CUDA N-Body Simulation" §1.3)
+// v <- v + kick a ; then, with a drift, x <- x + dt v.
+// The pages' step is kick = dt/2 plus the drift ("CUDA N-Body Simulation"
+// §1.3); the kick-drift-kick form fuses the closing half kick of one step
+// with the opening half kick of the next (kick = dt) and ends with a
+// kick-only pass.
 __device__ __forceinline__ void finish_body(const Epilogue& e, long long i, float ax, float ay,
                                             float az) {
   e.accel[i] = make_float4(ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
     float4 v = e.vel[i];
+    v.x = fmaf(e.kick, ax, v.x);
+    v.y = fmaf(e.kick, ay, v.y);
+    v.z = fmaf(e.kick, az, v.z);
+    e.vel[i] = v;
+    if (e.pos_next == nullptr) return;
     float4 x = e.pos[i];
-    v.x = fmaf(e.half_dt, ax, v.x);
-    v.y = fmaf(e.half_dt, ay, v.y);
-    v.z = fmaf(e.half_dt, az, v.z);
     x.x = fmaf(e.dt, v.x, x.x);
     x.y = fmaf(e.dt, v.y, x.y);
     x.z = fmaf(e.dt, v.z, x.z);
-    e.vel[i] = v;
     e.pos_next[i] = x;
     if (e.dup_next != nullptr) {  // masses do not move: keep this body's mass encoding
       const float4 enc = e.dup[2 * i + 1];
@@ -595,6 +603,43 @@ __global__ void finish_slices(const float4* __restrict__ partial, int n, int sli
     sz += p.z;
   }
   finish_body(e, i, sx, sy, sz);
+}
+
+// ---------------------------------------------------------------------------
+// point shaders as a kernel
+// ---------------------------------------------------------------------------
+
+struct RenderArgs {
+  const float4* pos;  // n rows (x, y, z, m)
+  float4* ndc;        // out: (x_ndc, y_ndc, z_ndc, 1)
+  float4* rgba;       // out: (r, g, b, 1)
+  long long n;
+  float3 lim;        // (max_x, max_y, max_z)
+  float3 scale;      // 2 / (max_c - (-max_c)) per component
+  float min_w;
+  float inv_range;   // 1 / (max_w - min_w)
+};
+
+// Vertex shader: p_c = 2 (c - (-max_c)) / (max_c - (-max_c)) - 1 and
+// weight = (m - min_w) / (max_w - min_w); fragment shader: mix(green, red,
+// weight) = (weight, 1 - weight, 0) with alpha 1 ("CUDA N-Body Simulation"
+// §4.3).  The per-draw reciprocals are taken once on the host, as a shader
+// compiler folds uniforms; no clamping, as in the shaders.  Memory-bound:
+// 16 bytes in and 32 bytes out per body; grid-stride over the SMs.
+__global__ void render_points(const RenderArgs a) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n;
+       i += stride) {
+    const float4 b = a.pos[i];
+    float4 p;
+    p.x = fmaf(b.x + a.lim.x, a.scale.x, -1.0f);
+    p.y = fmaf(b.y + a.lim.y, a.scale.y, -1.0f);
+    p.z = fmaf(b.z + a.lim.z, a.scale.z, -1.0f);
+    p.w = 1.0f;
+    const float w = (b.w - a.min_w) * a.inv_range;
+    a.ndc[i] = p;
+    a.rgba[i] = make_float4(w, 1.0f - w, 0.0f, 1.0f);
+  }
 }
 
 }  // namespace nbody

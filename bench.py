@@ -57,8 +57,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", choices=("step", "accel"), default="step",
-                    help="step: one leapfrog kick/drift step; accel: acceleration only")
+    ap.add_argument("--mode", choices=("step", "accel", "kdk", "render"), default="step",
+                    help="step: one leapfrog kick/drift step (default); accel: acceleration "
+                         "only; kdk: one kick-drift-kick step (two force passes); render: the "
+                         "point-shader kernel (memory-bound, reported in GB/s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -245,12 +247,20 @@ def oracle_sample_rate(pos_mass, eps2: float, seconds: float, seed: int):
     return k * n / wall / 1e9, k, oracle.threads(), wall
 
 
+MODE_TEXT = {
+    "step": "one leapfrog kick/drift step (all-pairs acceleration + fused half-kick and drift, "
+            "dt={dt:g}); N^2 interactions per step",
+    "accel": "one all-pairs acceleration evaluation; N^2 interactions per step",
+    "kdk": "one kick-drift-kick step (two all-pairs passes: half kick + drift, then the closing "
+           "half kick, dt={dt:g}); 2 N^2 interactions per step",
+    "render": "one pass of the point-shader kernel (NDC + mass colour); 48 bytes per body",
+}
+
+
 def workload_config(w, mode: str, world: int) -> dict:
-    what = ("one leapfrog kick/drift step (all-pairs acceleration + fused half-kick and drift, "
-            f"dt={w.dt:g})" if mode == "step" else "one all-pairs acceleration evaluation")
+    what = MODE_TEXT[mode].format(dt=w.dt)
     return {
-        "workload": f"{w.name}: N={w.n} bodies, eps2={w.eps2:g}, seed {w.seed}; each step is {what}; "
-                    f"N^2 interactions per step",
+        "workload": f"{w.name}: N={w.n} bodies, eps2={w.eps2:g}, seed {w.seed}; each step is {what}",
         "n_bodies": w.n,
         "l2": "flushed between timed steps (256 MiB write); sources 16N bytes",
         "parallelism": "replicas" if world > 1 else "single GPU",
@@ -283,9 +293,18 @@ def run_ours(args):
     acc = torch.empty_like(pm)
     stream = torch.cuda.current_stream()
 
+    ndc = torch.empty_like(pm) if args.mode == "render" else None
+    rgba = torch.empty_like(pm) if args.mode == "render" else None
+    m_lo = float(w.pos_mass[:, 3].min())
+    m_hi = max(float(w.pos_mass[:, 3].max()), m_lo * (1 + 1e-6) + 1e-30)
+
     def step():
         if args.mode == "step":
             nb.leapfrog_step(pm, vel, acc, w.eps2, dt, 1)
+        elif args.mode == "kdk":
+            nb.leapfrog_kdk(pm, vel, acc, w.eps2, dt, 1)
+        elif args.mode == "render":
+            nb.render_points(pm, (1.0, 1.0, 1.0), m_lo, m_hi, ndc=ndc, rgba=rgba)
         else:
             nb.accel(pm, w.eps2, out=acc)
 
@@ -315,8 +334,19 @@ def run_ours(args):
     force_ms, force_launches, launches = nb.profile_read()
     nb.profile_enable(False)
     total_s = reduce_max(sum(step_ms) / 1e3, dist, device="cuda")
-    interactions = float(n) * float(n)
+    if args.mode == "render":
+        if rank == 0:
+            print(json.dumps(render_line(args, w, world, total_s, launches, clocks)), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    interactions = float(n) * float(n) * (2.0 if args.mode == "kdk" else 1.0)
     value = aggregate_value(interactions * args.steps, world, total_s)
+    if args.mode == "kdk":
+        force_launches = max(force_launches, 1)
+        interactions_per_launch = float(n) * float(n)
+    else:
+        interactions_per_launch = interactions
 
     # end to end through the same API with pinned host buffers
     e2e = None
@@ -339,6 +369,8 @@ def run_ours(args):
             d_v.copy_(h_v, non_blocking=True)
             if args.mode == "step":
                 nb.leapfrog_step(d_pm, d_v, d_a, w.eps2, dt, 1)
+            elif args.mode == "kdk":
+                nb.leapfrog_kdk(d_pm, d_v, d_a, w.eps2, dt, 1)
             else:
                 nb.accel(d_pm, w.eps2, out=d_a)
             o_pm.copy_(d_pm, non_blocking=True)
@@ -356,7 +388,8 @@ def run_ours(args):
     # roofline of the force kernel
     sms = plan["sms"]
     f_max, f_src = measured_sm_max_mhz(clocks)
-    achieved = interactions / (force_ms / 1e3 / force_launches) / 1e9 if force_launches else None
+    achieved = (interactions_per_launch / (force_ms / 1e3 / force_launches) / 1e9
+                if force_launches else None)
     peak = alu_peak_ginter(sms, f_max)
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
             "frac": (achieved / peak) if achieved else None,
@@ -390,6 +423,32 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def measured_hbm_gbs() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs"
+    except (OSError, KeyError, ValueError, TypeError):
+        return 6800.0, "fallback HBM copy bandwidth"
+
+
+def render_line(args, w, world, total_s, launches, clocks) -> dict:
+    """JSON line of the memory-bound point-shader kernel: 16 bytes read and
+    32 bytes written per body (the algorithmic traffic)."""
+    nbytes = 48.0 * w.n * args.steps
+    gbs = world * nbytes / total_s / 1e9
+    peak, src = measured_hbm_gbs()
+    return {
+        "metric": "point-shader kernel throughput (NDC + mass colour)", "value": gbs,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, "render", world),
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / world / peak, "traffic": None, "peak_basis": src},
+        "gpu_launches": launches, "clocks": clocks, "impl": "ours",
+    }
 
 
 # ---------------------------------------------------------------------------

@@ -138,6 +138,42 @@ int nbody_leapfrog_step_with(float *pos_mass, float *vel, float *accel,
                              int path, int split, void *cuda_stream);
 
 /*
+ * `steps` kick-drift-kick leapfrog steps: per step
+ *     v <- v + (dt/2) a(x(t));  x <- x + dt v;  v <- v + (dt/2) a(x(t + dt)),
+ * the closed, time-symmetric form of the staggered leapfrog that
+ * "CUDA N-Body Simulation" §1.3 names (the pages' own step, above, stops
+ * after the drift).  The closing half kick of each step is fused with the
+ * opening half kick of the next, so a call costs steps + 1 force passes.
+ *   pos_mass, vel  in/out as for nbody_leapfrog_step.
+ *   accel          out: the accelerations at the final positions.
+ * Arguments, errors and paths as for nbody_leapfrog_step_with.
+ */
+int nbody_leapfrog_kdk_on_stream(float *pos_mass, float *vel, float *accel,
+                                 int64_t n, float eps2, float dt, int steps,
+                                 void *cuda_stream);
+
+int nbody_leapfrog_kdk_with(float *pos_mass, float *vel, float *accel,
+                            int64_t n, float eps2, float dt, int steps,
+                            int path, int split, void *cuda_stream);
+
+/*
+ * The point shaders of "CUDA N-Body Simulation" §4.3 (vertex and fragment
+ * shader of the mass-coloured GL_POINTS view) as a kernel writing into
+ * device buffers, for use without any graphics API:
+ *   ndc[i]  = (p_x, p_y, p_z, 1),  p_c = 2 (c - (-max_c)) / (max_c - (-max_c)) - 1
+ *   rgba[i] = (w, 1 - w, 0, 1),    w = (m - min_w) / (max_w - min_w),
+ * i.e. GLSL mix(green, red, w); nothing is clamped, as in the shaders.
+ *   pos_mass   in   n rows (x, y, z, m).
+ *   ndc, rgba  out  n float4 rows each; must not overlap each other or pos_mass.
+ *   max_x, max_y, max_z  finite, > 0 (the view box half-widths).
+ *   min_w, max_w         finite, max_w > min_w (the mass range).
+ * Errors as for nbody_accel; n == 0 is a no-op.
+ */
+int nbody_render_points(const float *pos_mass, float *ndc, float *rgba,
+                        int64_t n, float max_x, float max_y, float max_z,
+                        float min_w, float max_w, void *cuda_stream);
+
+/*
  * Wait for the stream, then report and clear the device-side status of
  * this device: NBODY_OK, NBODY_ETIMEOUT, or NBODY_ECUDA if the stream
  * reported a CUDA error.

@@ -7,7 +7,8 @@ double loops, j ascending); this module only marshals NumPy arrays.
 
 Sources: "CUDA N-Body Simulation" (LienoPC/N-BodySimulation README) §1.2 for
 the softened sum with G = 1, §1.3 for the half-kick + drift step with
-accelerations from the start-of-step coordinates.
+accelerations from the start-of-step coordinates, and for the staggered
+leapfrog whose kick-drift-kick form ``leapfrog_kdk`` states.
 """
 from __future__ import annotations
 
@@ -41,6 +42,10 @@ class Oracle:
         lib.oracle_accel.restype = i32
         lib.oracle_leapfrog.argtypes = [p, p, p, i64, d, d, i32, i32]
         lib.oracle_leapfrog.restype = i32
+        lib.oracle_leapfrog_kdk.argtypes = [p, p, p, i64, d, d, i32, i32]
+        lib.oracle_leapfrog_kdk.restype = i32
+        lib.oracle_render_points.argtypes = [p, i64, d, d, d, d, d, p, p]
+        lib.oracle_render_points.restype = i32
         self.lib = lib
         self.path = path
 
@@ -91,6 +96,41 @@ class Oracle:
         return pm, v, acc
 
 
+    def leapfrog_kdk(self, pos_mass, vel, eps2: float, dt: float, steps: int,
+                     threads: int = 0):
+        """FP64 kick-drift-kick leapfrog (closing half-kick with a(x(t+dt))).
+
+        Same arguments and returns as ``leapfrog``; ``acc`` is A at the final
+        positions (zeros when ``steps`` is 0).
+        """
+        pm = _bodies64(pos_mass).copy()
+        v = np.ascontiguousarray(np.asarray(vel, dtype=np.float64)[:, :3]).copy()
+        n = pm.shape[0]
+        if v.shape[0] != n:
+            raise ValueError("vel must have one row per body")
+        acc = np.zeros((n, 3), dtype=np.float64)
+        rc = self.lib.oracle_leapfrog_kdk(_ptr(pm), _ptr(v), _ptr(acc), n, float(eps2),
+                                          float(dt), int(steps), int(threads))
+        if rc < 0:
+            raise ValueError("oracle_leapfrog_kdk: bad argument")
+        return pm, v, acc
+
+
+    def render_points(self, pos_mass, max_xyz, min_w: float, max_w: float):
+        """CPU restatement of the point shaders ("CUDA N-Body Simulation"
+        §4.3): returns (ndc (n,4), rgba (n,4)) in float64."""
+        pm = _bodies64(pos_mass)
+        n = pm.shape[0]
+        ndc = np.zeros((n, 4))
+        rgba = np.zeros((n, 4))
+        mx, my, mz = (float(v) for v in max_xyz)
+        rc = self.lib.oracle_render_points(_ptr(pm), n, mx, my, mz, float(min_w), float(max_w),
+                                           _ptr(ndc), _ptr(rgba))
+        if rc < 0:
+            raise ValueError("oracle_render_points: bad argument")
+        return ndc, rgba
+
+
 _default: Oracle | None = None
 
 
@@ -111,3 +151,11 @@ def accel(pos_mass, eps2: float, idx=None, threads: int = 0) -> np.ndarray:
 
 def leapfrog(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int = 0):
     return default().leapfrog(pos_mass, vel, eps2, dt, steps, threads)
+
+
+def leapfrog_kdk(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int = 0):
+    return default().leapfrog_kdk(pos_mass, vel, eps2, dt, steps, threads)
+
+
+def render_points(pos_mass, max_xyz, min_w: float, max_w: float):
+    return default().render_points(pos_mass, max_xyz, min_w, max_w)

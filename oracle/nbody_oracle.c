@@ -19,6 +19,9 @@
  *     §1.3 Numerical Time Integration: the half-step velocity kick with
  *          a(x(t)) followed by the full-step drift with the kicked velocity;
  *          accelerations come from the coordinates at the start of the step.
+ *          The same section names the scheme a staggered leapfrog; its
+ *          textbook closed form (kick-drift-kick) adds the second half-kick
+ *          with a(x(t + dt)) and is given as oracle_leapfrog_kdk.
  *   "Cuda Nbody Notes": the per-pair interaction (r, |r|^2 + eps^2, the
  *          inverse 3/2 power, the mass factor, the accumulation).
  */
@@ -128,4 +131,79 @@ int oracle_leapfrog(double *pos_mass, double *vel, double *acc, int64_t n,
         }
     }
     return nt;
+}
+
+/*
+ * `steps` kick-drift-kick leapfrog steps in place, the closed form of the
+ * staggered leapfrog named in "CUDA N-Body Simulation" §1.3:
+ *   a = A(x(t))                       (once, before the first step)
+ *   per step, for every body:
+ *       v_i <- v_i + (dt/2) a_i       half kick with a(x(t))
+ *       x_i <- x_i + dt v_i           drift
+ *   then a = A(x(t + dt)) for every body, and for every body:
+ *       v_i <- v_i + (dt/2) a_i       half kick with a(x(t + dt))
+ * steps + 1 evaluations of A.  On return acc holds A at the final positions
+ * (untouched when steps is 0).  Returns the threads used or -1.
+ */
+int oracle_leapfrog_kdk(double *pos_mass, double *vel, double *acc, int64_t n,
+                        double eps2, double dt, int steps, int threads)
+{
+    if (n < 0 || steps < 0)
+        return -1;
+    if (n > 0 && (pos_mass == NULL || vel == NULL || acc == NULL))
+        return -1;
+    const int nt = oracle_threads(threads);
+    if (steps == 0)
+        return nt;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
+    for (int64_t i = 0; i < n; ++i)
+        accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);
+    for (int s = 0; s < steps; ++s) {
+#pragma omp parallel for schedule(static) num_threads(nt)
+        for (int64_t i = 0; i < n; ++i) {
+            for (int c = 0; c < 3; ++c) {
+                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];
+                pos_mass[4 * i + c] = pos_mass[4 * i + c] + dt * vel[3 * i + c];
+            }
+        }
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)
+        for (int64_t i = 0; i < n; ++i)
+            accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);
+#pragma omp parallel for schedule(static) num_threads(nt)
+        for (int64_t i = 0; i < n; ++i)
+            for (int c = 0; c < 3; ++c)
+                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];
+    }
+    return nt;
+}
+
+/*
+ * CPU restatement of the point shaders of "CUDA N-Body Simulation" §4.3
+ * (GLSL Shader Pipeline and Mass-Normalized Color Mapping), per body:
+ *   vertex:   weight = (m - min_w) / (max_w - min_w)
+ *             p_c    = 2 (c - (-max_c)) / (max_c - (-max_c)) - 1,  c = x, y, z
+ *             ndc    = (p_x, p_y, p_z, 1)
+ *   fragment: colour = mix(green, red, weight), GLSL mix(a, b, t) = a (1-t) + b t,
+ *             green = (0, 1, 0), red = (1, 0, 0); rgba = (colour, 1)
+ * No clamping: the shaders apply none.  ndc and rgba are n rows of 4 doubles.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_render_points(const double *pos_mass, int64_t n, double max_x, double max_y,
+                         double max_z, double min_w, double max_w, double *ndc, double *rgba)
+{
+    if (n < 0 || (n > 0 && (pos_mass == NULL || ndc == NULL || rgba == NULL)))
+        return -1;
+    const double lim[3] = {max_x, max_y, max_z};
+    const double green[3] = {0.0, 1.0, 0.0};
+    const double red[3] = {1.0, 0.0, 0.0};
+    for (int64_t i = 0; i < n; ++i) {
+        const double weight = (pos_mass[4 * i + 3] - min_w) / (max_w - min_w);
+        for (int c = 0; c < 3; ++c) {
+            ndc[4 * i + c] = 2.0 * (pos_mass[4 * i + c] - (-lim[c])) / (lim[c] - (-lim[c])) - 1.0;
+            rgba[4 * i + c] = green[c] * (1.0 - weight) + red[c] * weight;
+        }
+        ndc[4 * i + 3] = 1.0;
+        rgba[4 * i + 3] = 1.0;
+    }
+    return 0;
 }

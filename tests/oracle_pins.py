@@ -294,6 +294,165 @@ def pin_leapfrog_composition(o):
     assert np.array_equal(pa, pc) and np.array_equal(va, vc) and np.array_equal(aa, ac)
 
 
+# ---------------------------------------------------------------------------
+# kick-drift-kick leapfrog pins
+# ---------------------------------------------------------------------------
+
+
+def pin_kdk_zero_steps(o):
+    pm = np.array([[0.0, 0.0, 0.0, 1.0], [1.0, 0.0, 0.0, 1.0]])
+    v = np.array([[0.1, 0.2, 0.3], [0.0, 0.0, 0.0]])
+    p2, v2, a2 = o.leapfrog_kdk(pm, v, 0.01, 0.1, 0)
+    assert np.array_equal(p2, pm) and np.array_equal(v2, v) and np.all(a2 == 0)
+
+
+def pin_kdk_single_body_drift(o):
+    pm = np.array([[0.5, -1.0, 2.0, 3.0]])
+    v0 = np.array([[0.25, 0.5, -0.75]])
+    p, v, a = o.leapfrog_kdk(pm, v0, 1e-2, 0.125, 8)
+    assert np.all(a == 0.0) and np.array_equal(v, v0)
+    assert np.array_equal(p[0, :3], pm[0, :3] + 8 * 0.125 * v0[0])
+
+
+def pin_kdk_two_body_by_hand(o):
+    """Three kick-drift-kick steps integrated here from the closed-form
+    two-body accelerations."""
+    x = [np.array([0.0, 0.0, 0.0]), np.array([1.0, 0.5, -0.25])]
+    v = [np.array([0.0, 0.1, 0.0]), np.array([-0.2, 0.0, 0.05])]
+    m = [2.0, 0.5]
+    eps2, dt, steps = 0.04, 0.05, 3
+    pm = np.array([[*x[0], m[0]], [*x[1], m[1]]])
+    vv = np.array([v[0], v[1]])
+    a = list(_two_body_expected(x[0], x[1], m[0], m[1], eps2))
+    for _ in range(steps):
+        for k in range(2):
+            v[k] = v[k] + 0.5 * dt * a[k]
+            x[k] = x[k] + dt * v[k]
+        a = list(_two_body_expected(x[0], x[1], m[0], m[1], eps2))
+        for k in range(2):
+            v[k] = v[k] + 0.5 * dt * a[k]
+    p2, v2, a2 = o.leapfrog_kdk(pm, vv, eps2, dt, steps)
+    _close(p2[:, :3], np.array(x), 1e-14, what="kdk two-body positions")
+    _close(v2, np.array(v), 1e-14, what="kdk two-body velocities")
+    _close(a2, np.array(a), 1e-14, what="kdk two-body final accelerations")
+
+
+def pin_kdk_time_reversible(o):
+    """Kick-drift-kick is time-symmetric: run forward, reverse the velocities,
+    run the same number of steps, reverse again: the start comes back."""
+    rng = np.random.default_rng(11)
+    n = 24
+    pm = np.zeros((n, 4))
+    pm[:, :3] = rng.normal(size=(n, 3))
+    pm[:, 3] = rng.uniform(0.5, 1.5, size=n) / n
+    v0 = rng.normal(scale=0.2, size=(n, 3))
+    p1, v1, _ = o.leapfrog_kdk(pm, v0, 0.02, 0.01, 40)
+    p2, v2, _ = o.leapfrog_kdk(p1, -v1, 0.02, 0.01, 40)
+    _close(p2[:, :3], pm[:, :3], 1e-11, what="reversed positions")
+    _close(-v2, v0, 1e-10, what="reversed velocities")
+
+
+def _circular_pair(eps2):
+    """Two masses 1/2 at separation 1 on a circular orbit of the softened
+    force: omega^2 = 2 m / (D^2 + eps2)^{3/2}, radius D/2."""
+    m, D = 0.5, 1.0
+    R = D / 2
+    w = math.sqrt(2 * m / (D * D + eps2) ** 1.5)
+    pm = np.array([[R, 0.0, 0.0, m], [-R, 0.0, 0.0, m]])
+    v = np.array([[0.0, w * R, 0.0], [0.0, -w * R, 0.0]])
+    return pm, v, w, R
+
+
+def pin_kdk_second_order(o):
+    """Global error on a circular orbit falls 4x per halving of dt."""
+    eps2, T = 0.01, 2.0
+    pm, v, w, R = _circular_pair(eps2)
+    exact = np.array([R * math.cos(w * T), R * math.sin(w * T), 0.0])
+    errs = []
+    for steps in (50, 100, 200):
+        p, _, _ = o.leapfrog_kdk(pm, v, eps2, T / steps, steps)
+        errs.append(float(np.linalg.norm(p[0, :3] - exact)))
+    r1, r2 = errs[0] / errs[1], errs[1] / errs[2]
+    assert 3.6 < r1 < 4.4 and 3.6 < r2 < 4.4, (errs, r1, r2)
+
+
+def pin_kdk_matches_half_kick_drift_then_kick(o):
+    """One KDK step = the half-kick + drift step, then a half kick with the
+    acceleration at the new positions."""
+    rng = np.random.default_rng(12)
+    pm = np.zeros((30, 4))
+    pm[:, :3] = rng.normal(size=(30, 3))
+    pm[:, 3] = rng.uniform(0.5, 1.5, size=30)
+    v0 = rng.normal(scale=0.1, size=(30, 3))
+    pk, vk, ak = o.leapfrog_kdk(pm, v0, 0.01, 0.02, 1)
+    ph, vh, _ = o.leapfrog(pm, v0, 0.01, 0.02, 1)
+    assert np.array_equal(pk, ph), "KDK drift differs from the half-kick + drift step"
+    a1 = o.accel(ph, 0.01)
+    assert np.array_equal(ak, a1)
+    _close(vk, vh + 0.5 * 0.02 * a1, 1e-15, what="closing half kick")
+
+
+def pin_kdk_momentum(o):
+    rng = np.random.default_rng(13)
+    n = 40
+    pm = np.zeros((n, 4))
+    pm[:, :3] = rng.normal(size=(n, 3))
+    pm[:, 3] = rng.uniform(0.5, 1.5, size=n)
+    v0 = rng.normal(scale=0.3, size=(n, 3))
+    _, v, _ = o.leapfrog_kdk(pm, v0, 0.05, 0.01, 6)
+    m = pm[:, 3:4]
+    P0 = np.sum(m * v0, axis=0)
+    assert np.max(np.abs(np.sum(m * v, axis=0) - P0)) <= 1e-13 * float(np.sum(m * np.abs(v)))
+
+
+KDK_PINS = [
+    pin_kdk_zero_steps,
+    pin_kdk_single_body_drift,
+    pin_kdk_two_body_by_hand,
+    pin_kdk_time_reversible,
+    pin_kdk_second_order,
+    pin_kdk_matches_half_kick_drift_then_kick,
+    pin_kdk_momentum,
+]
+
+# ---------------------------------------------------------------------------
+# point-shader pins ("CUDA N-Body Simulation" §4.3)
+# ---------------------------------------------------------------------------
+
+
+def pin_render_ndc_equals_x_over_limit(o):
+    """The section states the affine map as x_NDC = x / X; the shader writes
+    2 (x + X) / (2 X) - 1.  The two agree, and the box corners map to +-1."""
+    rng = np.random.default_rng(14)
+    pm = np.zeros((100, 4))
+    lim = (2.0, 0.5, 300.0)
+    for c in range(3):
+        pm[:, c] = rng.uniform(-1.5, 1.5, size=100) * lim[c]
+    pm[:, 3] = rng.uniform(1.0, 2.0, size=100)
+    ndc, _ = o.render_points(pm, lim, 1.0, 2.0)
+    _close(ndc[:, :3], pm[:, :3] / np.array(lim), 1e-15, what="ndc = x / X")
+    assert np.all(ndc[:, 3] == 1.0)
+    corners = np.array([[2.0, -0.5, 300.0, 1.0], [-2.0, 0.5, -300.0, 1.0], [0, 0, 0, 1.0]])
+    ndc, _ = o.render_points(corners, lim, 1.0, 2.0)
+    assert np.array_equal(ndc[:, :3], [[1, -1, 1], [-1, 1, -1], [0, 0, 0]])
+
+
+def pin_render_colour_ramp(o):
+    """Lightest mass is green, heaviest red, the midpoint half of each, and
+    the colour is affine in the mass (GLSL mix)."""
+    pm = np.zeros((5, 4))
+    pm[:, 3] = [1e5, 1e9, 0.5 * (1e5 + 1e9), 1e5 + 0.25 * (1e9 - 1e5), 2e9]
+    _, rgba = o.render_points(pm, (1.0, 1.0, 1.0), 1e5, 1e9)
+    _close(rgba[0], [0, 1, 0, 1], 1e-15, what="min mass")
+    _close(rgba[1], [1, 0, 0, 1], 1e-15, what="max mass")
+    _close(rgba[2], [0.5, 0.5, 0, 1], 1e-15, what="mid mass")
+    _close(rgba[3], [0.25, 0.75, 0, 1], 1e-15, what="quarter mass")
+    w = (2e9 - 1e5) / (1e9 - 1e5)  # no clamp: extrapolates beyond red
+    _close(rgba[4], [w, 1 - w, 0, 1], 1e-15, what="beyond max mass")
+
+
+RENDER_PINS = [pin_render_ndc_equals_x_over_limit, pin_render_colour_ramp]
+
 ACCEL_PINS = [
     pin_two_body_closed_form,
     pin_ring_axis_closed_form,
@@ -314,7 +473,7 @@ LEAPFROG_PINS = [
     pin_leapfrog_momentum_and_com,
     pin_leapfrog_composition,
 ]
-ALL_PINS = ACCEL_PINS + LEAPFROG_PINS
+ALL_PINS = ACCEL_PINS + LEAPFROG_PINS + KDK_PINS + RENDER_PINS
 
 
 def failing_pins(o) -> list[str]:

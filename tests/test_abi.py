@@ -137,3 +137,24 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nb, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         nb.lib()
+
+
+def render(L, pos, ndc, rgba, n, lim=(1.0, 1.0, 1.0), w=(0.0, 1.0)):
+    return L.nbody_render_points(ctypes.c_void_p(pos), ctypes.c_void_p(ndc), ctypes.c_void_p(rgba),
+                                 n, *lim, *w, S)
+
+
+@pytest.mark.parametrize("lim,w", [((0.0, 1.0, 1.0), (0.0, 1.0)), ((1.0, -1.0, 1.0), (0.0, 1.0)),
+                                   ((1.0, 1.0, math.nan), (0.0, 1.0)), ((1.0, 1.0, 1.0), (1.0, 1.0)),
+                                   ((1.0, 1.0, 1.0), (2.0, 1.0)), ((1.0, 1.0, 1.0), (0.0, math.inf))])
+def test_render_bad_parameters(L, lim, w):
+    assert render(L, A, B, C, 10, lim, w) == nb.EINVAL
+
+
+def test_render_bad_pointers(L):
+    assert render(L, 0, B, C, 10) == nb.EINVAL
+    assert render(L, A, B + 4, C, 10) == nb.EINVAL
+    assert render(L, A, A + 16, C, 10) == nb.EINVAL
+    assert render(L, A, B, B, 10) == nb.EINVAL
+    assert render(L, A, B, C, -1) == nb.EINVAL
+    assert render(L, 0, 0, 0, 0) == nb.OK

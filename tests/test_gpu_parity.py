@@ -311,3 +311,109 @@ def test_negative_masses_take_the_exact_loop(cfg, monkeypatch):
     p, vv, aa = gpu_leapfrog(pm, v, 1e-3, 1e-3, 2, path=2)
     rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 2)
     assert rel_err(aa, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL
+
+
+# ---------------------------------------------------------------------------
+# kick-drift-kick leapfrog
+# ---------------------------------------------------------------------------
+
+
+def gpu_kdk(pos_mass_np, vel_np, eps2, dt, steps, path=0, split=0):
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = torch.from_numpy(np.ascontiguousarray(pos_mass_np, dtype=np.float32)).cuda()
+    v = torch.from_numpy(np.ascontiguousarray(vel_np, dtype=np.float32)).cuda()
+    a = torch.full_like(pm, float("nan"))
+    nb.leapfrog_kdk(pm, v, a, eps2, dt, steps, path=path, split=split)
+    nb.sync()
+    return pm.cpu().numpy(), v.cpu().numpy(), a.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["uniform-cube-1024", "plummer-16384", "two-plummer-131072"])
+def test_kdk_trajectory(name):
+    w = W.by_name(name)
+    steps = max(w.steps, 1)
+    p, v, a = gpu_kdk(w.pos_mass, w.vel, w.eps2, w.dt, steps)
+    rp, rv, ra = oracle.leapfrog_kdk(w.pos_mass, w.vel, w.eps2, w.dt, steps)
+    assert rel_err(p, rp) <= POS_TOL
+    assert rel_err(v, rv) <= VEL_TOL
+    assert rel_err(a, ra) <= ACC_TOL
+    assert displacement_err(p, rp, w.pos_mass, steps) <= 1e-3
+    assert np.array_equal(p[:, 3], w.pos_mass[:, 3]) and np.array_equal(v[:, 3], w.vel[:, 3])
+
+
+@pytest.mark.parametrize("path,split", PATHS)
+def test_kdk_paths(path, split):
+    n = 5000
+    pm = W.random_bodies(n, 23)
+    v = W.random_velocities(n, 23)
+    p, vv, a = gpu_kdk(pm, v, 1e-3, 1e-3, 3, path, split)
+    rp, rv, ra = oracle.leapfrog_kdk(pm, v, 1e-3, 1e-3, 3)
+    assert rel_err(a, ra) <= ACC_TOL
+    assert rel_err(vv, rv) <= VEL_TOL
+    assert rel_err(p, rp) <= POS_TOL
+
+
+def test_kdk_first_drift_is_the_pages_step():
+    pm = W.random_bodies(3000, 24)
+    v = W.random_velocities(3000, 24)
+    pk, vk, ak = gpu_kdk(pm, v, 1e-3, 1e-3, 1)
+    ph, vh, _ = gpu_leapfrog(pm, v, 1e-3, 1e-3, 1)
+    assert np.array_equal(pk, ph)
+    # the closing half kick uses the acceleration at the new positions
+    assert rel_err(vk[:, :3] - vh[:, :3], 0.5e-3 * oracle.accel(ph, 1e-3)) <= 1e-3
+
+
+def test_kdk_time_reversible():
+    pm = W.random_bodies(4000, 25)
+    v = W.random_velocities(4000, 25, scale=0.3)
+    p1, v1, _ = gpu_kdk(pm, v, 1e-3, 1e-3, 20)
+    back = v1.copy()
+    back[:, :3] *= -1.0
+    p2, v2, _ = gpu_kdk(p1, back, 1e-3, 1e-3, 20)
+    moved = float(np.abs(p1[:, :3] - pm[:, :3]).max())
+    assert float(np.abs(p2[:, :3] - pm[:, :3]).max()) <= 1e-3 * moved
+    assert float(np.abs(-v2[:, :3] - v[:, :3]).max()) <= 1e-4 * float(np.abs(v[:, :3]).max())
+
+
+# ---------------------------------------------------------------------------
+# point shaders as a kernel
+# ---------------------------------------------------------------------------
+
+RENDER_TOL = 2e-6  # float32 arithmetic on values of order one
+
+
+def gpu_render(pm_np, lim, min_w, max_w):
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = torch.from_numpy(np.ascontiguousarray(pm_np, dtype=np.float32)).cuda()
+    ndc, rgba = nb.render_points(pm, lim, min_w, max_w)
+    nb.sync()
+    return ndc.cpu().numpy(), rgba.cpu().numpy()
+
+
+def render_err(got, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.max(np.abs(got.astype(np.float64) - ref) / np.maximum(1.0, np.abs(ref))))
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000, 65537, 1048576])
+def test_render_points(n):
+    w = W.ball_lognormal_1048576(n) if n > 1 else W.random_bodies(1, 3)
+    pm = w.pos_mass if hasattr(w, "pos_mass") else w
+    m = pm[:, 3].astype(np.float64)
+    lim = (1.25, 0.75, 1.5)  # some bodies fall outside the box: no clamping
+    min_w, max_w = float(m.min()), float(m.max()) if n > 1 else float(m.min()) + 1.0
+    ndc, rgba = gpu_render(pm, lim, min_w, max_w)
+    rn, rc = oracle.render_points(pm, lim, np.float32(min_w), np.float32(max_w))
+    assert render_err(ndc, rn) <= RENDER_TOL and render_err(rgba, rc) <= RENDER_TOL
+    assert np.all(ndc[:, 3] == 1.0) and np.all(rgba[:, 3] == 1.0) and np.all(rgba[:, 2] == 0.0)
+
+
+def test_render_after_steps():
+    """The intended use: colour and place the bodies after each step."""
+    w = W.plummer_16384()
+    p, _, _ = gpu_leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, 3)
+    ndc, rgba = gpu_render(p, (4.0, 4.0, 4.0), 0.0, 2.0 / w.n)
+    rn, rc = oracle.render_points(p, (4.0, 4.0, 4.0), 0.0, np.float32(2.0 / w.n))
+    assert render_err(ndc, rn) <= RENDER_TOL and render_err(rgba, rc) <= RENDER_TOL

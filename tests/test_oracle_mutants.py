@@ -36,7 +36,51 @@ DRIFT_KICK = (
     "                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];\n"
 )
 
+KDK_CLOSING = (
+    "#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)\n"
+    "        for (int64_t i = 0; i < n; ++i)\n"
+    "            accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);\n"
+    "#pragma omp parallel for schedule(static) num_threads(nt)\n"
+    "        for (int64_t i = 0; i < n; ++i)\n"
+    "            for (int c = 0; c < 3; ++c)\n"
+    "                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];\n"
+    "    }\n"
+)
+KDK_CLOSING_STALE = (
+    "#pragma omp parallel for schedule(static) num_threads(nt)\n"
+    "        for (int64_t i = 0; i < n; ++i)\n"
+    "            for (int c = 0; c < 3; ++c)\n"
+    "                vel[3 * i + c] = vel[3 * i + c] + 0.5 * dt * acc[3 * i + c];\n"
+    "#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)\n"
+    "        for (int64_t i = 0; i < n; ++i)\n"
+    "            accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);\n"
+    "    }\n"
+)
+KDK_CLOSING_DROPPED = (
+    "#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)\n"
+    "        for (int64_t i = 0; i < n; ++i)\n"
+    "            accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);\n"
+    "    }\n"
+)
+KDK_FIRST_ACCEL = (
+    "    if (steps == 0)\n"
+    "        return nt;\n"
+    "#pragma omp parallel for schedule(dynamic, 16) num_threads(nt)\n"
+    "    for (int64_t i = 0; i < n; ++i)\n"
+    "        accel_of_body(pos_mass, n, eps2, i, acc + 3 * i);\n"
+)
+
 MUTANTS = {
+    "render_colours_swapped": [("const double green[3] = {0.0, 1.0, 0.0};",
+                                "const double green[3] = {1.0, 0.0, 0.0};"),
+                               ("const double red[3] = {1.0, 0.0, 0.0};",
+                                "const double red[3] = {0.0, 1.0, 0.0};")],
+    "render_weight_not_normalised": [("/ (max_w - min_w);", "/ max_w;")],
+    "render_offset_dropped": [("/ (lim[c] - (-lim[c])) - 1.0;", "/ (lim[c] - (-lim[c]));")],
+    "render_half_range": [("/ (lim[c] - (-lim[c])) - 1.0;", "/ lim[c] - 1.0;")],
+    "kdk_closing_kick_dropped": [(KDK_CLOSING, KDK_CLOSING_DROPPED)],
+    "kdk_closing_kick_with_old_accel": [(KDK_CLOSING, KDK_CLOSING_STALE)],
+    "kdk_first_accel_skipped": [(KDK_FIRST_ACCEL, "    if (steps == 0)\n        return nt;\n")],
     "reversed_separation": [("pm[4 * j + 0] - xi", "xi - pm[4 * j + 0]"),
                             ("pm[4 * j + 1] - yi", "yi - pm[4 * j + 1]"),
                             ("pm[4 * j + 2] - zi", "zi - pm[4 * j + 2]")],
@@ -57,9 +101,9 @@ MUTANTS = {
     "drift_before_kick": [(KICK_DRIFT, DRIFT_KICK)],
     "in_place_update_race": [(STEP_LOOPS, FUSED_IN_PLACE)],
     # (stays in bounds: widening the drift loop to 4 columns would write past vel)
-    "mass_drifted": [("for (int c = 0; c < 3; ++c) {",
+    "mass_drifted": [("for (int c = 0; c < 3; ++c) {\n                vel[3 * i + c]",
                       "pos_mass[4 * i + 3] = pos_mass[4 * i + 3] + dt * vel[3 * i];\n"
-                      "            for (int c = 0; c < 3; ++c) {")],
+                      "            for (int c = 0; c < 3; ++c) {\n                vel[3 * i + c]")],
     "sample_index_ignored": [("const int64_t i = idx ? idx[k] : k;", "const int64_t i = k;")],
 }
 
