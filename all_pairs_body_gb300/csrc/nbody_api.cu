@@ -58,6 +58,7 @@ const TiledConfig kTiled[] = {
     {4, 256, 256, 1, force_tiled<4, 256, 256, 2, 4, 1, 1>},
     {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1, 2>},
     {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1, 2>},
+    {10, 256, 256, 0, force_tiled<10, 256, 256, 1, 2, 0, 0>},
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
@@ -170,7 +171,7 @@ int current_device(int* dev) {
 int auto_tiled_config(long long n) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n >= 131072) return 7;  // fastest at 2^20 in a sweep of the table
+  if (n >= 131072) return 20;  // fastest at 2^20 in a sweep of 52 shapes
   if (n >= 16384) return 1;
   return 2;
 }

@@ -214,8 +214,11 @@ struct Epilogue {
 // §1.3); the kick-drift-kick form fuses the closing half kick of one step
 // with the opening half kick of the next (kick = dt) and ends with a
 // kick-only pass.
-__device__ __forceinline__ void finish_body(const Epilogue& e, long long i, float ax, float ay,
-                                            float az) {
+// Kept out of line (and taken by value): it runs once per body and segment,
+// and inlining it into the force kernel perturbs the register allocation and
+// schedule of the inner loop (up to 2.5% in a measured sweep).
+__device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
+                                         float az) {
   e.accel[i] = make_float4(ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
     float4 v = e.vel[i];
