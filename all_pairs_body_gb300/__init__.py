@@ -31,7 +31,7 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_leapfrog_step_with", "nbody_sync", "nbody_plan", "nbody_strerror",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
            "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
-           "nbody_leapfrog_kdk_with", "nbody_render_points")
+           "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d")
 NOALLOC_MAX_N = 65536
 
 
@@ -65,6 +65,7 @@ def lib() -> ctypes.CDLL:
             "nbody_leapfrog_kdk_on_stream": [p, p, p, i64, f32, f32, i32, p],
             "nbody_leapfrog_kdk_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
             "nbody_render_points": [p, p, p, i64, f32, f32, f32, f32, f32, p],
+            "nbody_neighbors_2d": [p, p, i64, f32, i32, p, p, p],
             "nbody_sync": [p],
             "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
             "nbody_selftest_timeout": [i32, p],
@@ -180,6 +181,30 @@ def render_points(pos_mass, max_xyz, min_w: float, max_w: float, ndc=None, rgba=
                                    float(max_w), _stream(stream))
     _check(rc, "nbody_render_points")
     return ndc, rgba
+
+
+def neighbors_2d(x, y, cutoff: float, max_neighbors: int, nn=None, nl=None, stream=None):
+    """2-D cutoff neighbour list (all pairs, no atomics): returns (nn, nl),
+    nn (n,) int32 counts and nl (max_neighbors, n) int32 ascending lists
+    padded with -1."""
+    import torch
+    for name, t in (("x", x), ("y", y)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32
+                and t.is_contiguous() and t.dim() == 1):
+            raise ValueError(f"{name} must be a contiguous 1-D float32 CUDA tensor")
+    n = int(x.shape[0])
+    if int(y.shape[0]) != n:
+        raise ValueError("x and y must have the same length")
+    mn = int(max_neighbors)
+    if nn is None:
+        nn = torch.empty(n, dtype=torch.int32, device=x.device)
+    if nl is None:
+        nl = torch.empty((mn, n), dtype=torch.int32, device=x.device)
+    rc = lib().nbody_neighbors_2d(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()), n,
+                                  float(cutoff), mn, ctypes.c_void_p(nn.data_ptr()),
+                                  ctypes.c_void_p(nl.data_ptr() if mn > 0 else 0), _stream(stream))
+    _check(rc, "nbody_neighbors_2d")
+    return nn, nl
 
 
 def sync(stream=None) -> None:

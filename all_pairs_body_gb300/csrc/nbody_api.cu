@@ -544,6 +544,45 @@ int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float
   return launch_status();
 }
 
+constexpr int kNeighborKI = 4;
+constexpr int kNeighborNT = 128;
+
+int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int max_neighbors,
+                   int32_t* nn, int32_t* nl, cudaStream_t st) {
+  if (n < 0 || n > static_cast<int64_t>(INT32_MAX) || max_neighbors < 0) return NBODY_EINVAL;
+  if (!std::isfinite(cutoff) || !(cutoff > 0.0f)) return NBODY_EINVAL;
+  const float c2 = cutoff * cutoff;
+  if (!(c2 >= 1.17549435e-38f) || !std::isfinite(c2)) return NBODY_EINVAL;  // normal, finite
+  if (n == 0) return NBODY_OK;
+  if (x == nullptr || y == nullptr || nn == nullptr) return NBODY_EINVAL;
+  if (max_neighbors > 0 && nl == nullptr) return NBODY_EINVAL;
+  const size_t b4 = static_cast<size_t>(n) * 4;
+  const size_t bl = b4 * static_cast<size_t>(max_neighbors);
+  for (const void* ptr : {static_cast<const void*>(x), static_cast<const void*>(y),
+                          static_cast<const void*>(nn), static_cast<const void*>(nl)})
+    if (ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 3u) != 0) return NBODY_EINVAL;
+  if (overlaps(nn, x, b4) || overlaps(nn, y, b4)) return NBODY_EINVAL;
+  if (max_neighbors > 0) {
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(nl), l1 = l0 + bl;
+    for (const void* q : {static_cast<const void*>(x), static_cast<const void*>(y),
+                          static_cast<const void*>(nn)}) {
+      const uintptr_t q0 = reinterpret_cast<uintptr_t>(q), q1 = q0 + b4;
+      if (q0 < l1 && l0 < q1) return NBODY_EINVAL;
+    }
+  }
+  int rc = NBODY_OK, dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  for (const void* ptr : {static_cast<const void*>(x), static_cast<const void*>(y),
+                          static_cast<const void*>(nn)})
+    if ((rc = check_device_pointer(ptr, dev)) != NBODY_OK) return rc;
+  if (max_neighbors > 0 && (rc = check_device_pointer(nl, dev)) != NBODY_OK) return rc;
+  NeighborArgs a{x, y, static_cast<int>(n), c2, max_neighbors, nn, nl, ceil_div(n, kNeighborNT)};
+  const long long blocks = ceil_div(n, static_cast<long long>(kNeighborKI) * kNeighborNT);
+  count_launches(1);
+  neighbors_2d<kNeighborKI, kNeighborNT><<<static_cast<unsigned>(blocks), kNeighborNT, 0, st>>>(a);
+  return launch_status();
+}
+
 }  // namespace
 }  // namespace nbody
 
@@ -713,6 +752,12 @@ int nbody_render_points(const float* pos_mass, float* ndc, float* rgba, int64_t 
                         float max_y, float max_z, float min_w, float max_w, void* cuda_stream) {
   return nbody::render_impl(pos_mass, ndc, rgba, n, max_x, max_y, max_z, min_w, max_w,
                             static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_neighbors_2d(const float* x, const float* y, int64_t n, float cutoff, int max_neighbors,
+                       int32_t* nn, int32_t* nl, void* cuda_stream) {
+  return nbody::neighbors_impl(x, y, n, cutoff, max_neighbors, nn, nl,
+                               static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_sync(void* cuda_stream) {

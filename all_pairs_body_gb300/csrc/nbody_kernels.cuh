@@ -26,6 +26,9 @@
 //   render_points       the point shaders of "CUDA N-Body Simulation" §4.3 as a
 //                       kernel: normalised device coordinates and mass colour
 //                       of every body into a device buffer (no graphics API).
+//   neighbors_2d        the 2-D cutoff neighbour list of "CUDA编程（九）原子函数
+//                       的合理使用" §3 without atomics: all pairs, packed FP32,
+//                       per-target counts and ascending transposed lists.
 //
 // The pages' tiled kernel ("CUDA N-Body Simulation" §3.1, "Cuda Nbody Notes"
 // calculate_forces, The CUDA Handbook ch. 14 shared-memory kernel) keeps one
@@ -642,6 +645,105 @@ __global__ void render_points(const RenderArgs a) {
     const float w = (b.w - a.min_w) * a.inv_range;
     a.ndc[i] = p;
     a.rgba[i] = make_float4(w, 1.0f - w, 0.0f, 1.0f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2-D cutoff neighbour list
+// ---------------------------------------------------------------------------
+
+struct NeighborArgs {
+  const float* x;  // n source/target x
+  const float* y;  // n source/target y
+  int n;
+  float cutoff_square;  // cutoff * cutoff, rounded to float
+  int max_neighbors;    // MN: list slots per target
+  int* nn;              // out: neighbours per target
+  int* nl;              // out: nl[k * n + i], ascending, -1 past the count
+  long long ntiles;
+};
+
+// All pairs in the page's single precision, every operation rounded
+// separately (packed round-to-nearest intrinsics are never contracted):
+//   x12 = x_j - x_i, y12 = y_j - y_i, d2 = x12 * x12 + y12 * y12,
+//   neighbour when d2 < cutoff^2 and j != i.
+// KI targets per thread as KI/2 packed pairs; sources staged as (x,x,y,y) in
+// a two-buffer shared ring filled by plain loads (one source per thread per
+// tile, prefetched into registers during the previous tile).  One CTA covers
+// the whole j range of its targets, so every list is appended in ascending j.
+// Padding sources sit at +inf and padding targets are NaN: neither can pass
+// the test.  Hits are rare, so the append runs in a divergent branch.
+template <int KI, int NT>
+__global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
+  static_assert(KI % 2 == 0, "targets are processed in packed pairs");
+  constexpr int P = KI / 2;
+  constexpr int TJ = NT;
+  __shared__ __align__(16) float4 tile[2][TJ];
+
+  const int tid = threadIdx.x;
+  const long long base = static_cast<long long>(blockIdx.x) * KI * NT;
+  const float c2 = a.cutoff_square;
+  float2 nx[P], ny[P];
+  int cnt[KI];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    float v[2][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const long long i = base + (2 * p + h) * NT + tid;
+      v[h][0] = i < a.n ? -a.x[i] : __int_as_float(0x7fc00000);
+      v[h][1] = i < a.n ? -a.y[i] : __int_as_float(0x7fc00000);
+      cnt[2 * p + h] = 0;
+    }
+    nx[p] = make_float2(v[0][0], v[1][0]);
+    ny[p] = make_float2(v[0][1], v[1][1]);
+  }
+
+  long long jl = tid;
+  float px = jl < a.n ? a.x[jl] : __int_as_float(0x7f800000);
+  float py = jl < a.n ? a.y[jl] : __int_as_float(0x7f800000);
+  for (long long t = 0; t < a.ntiles; ++t) {
+    const int s = static_cast<int>(t & 1);
+    tile[s][tid] = make_float4(px, px, py, py);
+    __syncthreads();  // also: every thread is done with tile t-2 (same buffer)
+    if (t + 1 < a.ntiles) {
+      jl = (t + 1) * TJ + tid;
+      px = jl < a.n ? a.x[jl] : __int_as_float(0x7f800000);
+      py = jl < a.n ? a.y[jl] : __int_as_float(0x7f800000);
+    }
+    const long long j0 = t * TJ;
+#pragma unroll 4
+    for (int jj = 0; jj < TJ; ++jj) {
+      const float4 b = tile[s][jj];
+      const float2 X = make_float2(b.x, b.y);
+      const float2 Y = make_float2(b.z, b.w);
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const float2 dx = __fadd2_rn(X, nx[p]);
+        const float2 dy = __fadd2_rn(Y, ny[p]);
+        const float2 d2 = __fadd2_rn(__fmul2_rn(dx, dx), __fmul2_rn(dy, dy));
+        if (d2.x < c2 || d2.y < c2) {
+          const long long j = j0 + jj;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const long long i = base + (2 * p + h) * NT + tid;
+            if ((h ? d2.y : d2.x) < c2 && j != i) {
+              int& c = cnt[2 * p + h];
+              if (c < a.max_neighbors) a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
+              ++c;
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KI; ++k) {
+    const long long i = base + k * NT + tid;
+    if (i < a.n) {
+      a.nn[i] = cnt[k];
+      for (int q = cnt[k]; q < a.max_neighbors; ++q) a.nl[static_cast<long long>(q) * a.n + i] = -1;
+    }
   }
 }
 

@@ -57,10 +57,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--mode", choices=("step", "accel", "kdk", "render"), default="step",
+    ap.add_argument("--mode", choices=("step", "accel", "kdk", "render", "neighbors"),
+                    default="step",
                     help="step: one leapfrog kick/drift step (default); accel: acceleration "
                          "only; kdk: one kick-drift-kick step (two force passes); render: the "
-                         "point-shader kernel (memory-bound, reported in GB/s)")
+                         "point-shader kernel (memory-bound, reported in GB/s); neighbors: the "
+                         "2-D cutoff neighbour list (pair tests/s; default points2d-1048576)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -254,6 +256,7 @@ MODE_TEXT = {
     "kdk": "one kick-drift-kick step (two all-pairs passes: half kick + drift, then the closing "
            "half kick, dt={dt:g}); 2 N^2 interactions per step",
     "render": "one pass of the point-shader kernel (NDC + mass colour); 48 bytes per body",
+    "neighbors": "one all-pairs 2-D cutoff neighbour list",
 }
 
 
@@ -498,8 +501,86 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+NEIGHBOR_FP32_OPS = 5  # per pair test: 2 subtracts, 2 squares, 1 add
+
+
+def run_neighbors(args):
+    """Pair tests per second of the 2-D cutoff neighbour list on one GPU."""
+    import torch
+
+    import __graft_entry__
+    import workloads
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, True)
+    __graft_entry__.build()
+    import all_pairs_body_gb300 as nb
+
+    name = args.workload if args.workload.startswith("points2d-") else "points2d-1048576"
+    p = workloads.by_name(name)
+    x = torch.from_numpy(p.x).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    nn = torch.empty(p.n, dtype=torch.int32, device="cuda")
+    nl = torch.empty((p.max_neighbors, p.n), dtype=torch.int32, device="cuda")
+    for _ in range(max(args.warmup, 0)):
+        nb.neighbors_2d(x, y, p.cutoff, p.max_neighbors, nn=nn, nl=nl)
+    nb.sync()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(gpu_selector(local)).start()
+    nb.profile_enable(True)
+    nb.profile_read()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.zero_()
+        starts[k].record(stream)
+        nb.neighbors_2d(x, y, p.cutoff, p.max_neighbors, nn=nn, nl=nl)
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clocks = sampler.stop()
+    nb.sync()
+    _, _, launches = nb.profile_read()
+    nb.profile_enable(False)
+    total_s = reduce_max(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3, dist,
+                         device="cuda")
+    tests = float(p.n) * float(p.n)
+    value = aggregate_value(tests * args.steps, world, total_s)
+    sms = nb.plan(p.n)["sms"]
+    f_max, f_src = measured_sm_max_mhz(clocks)
+    peak = sms * f_max * 1e6 * FP32_LANES_PER_SM / NEIGHBOR_FP32_OPS / 1e9
+    line = {
+        "metric": "2-D cutoff neighbour list: pair tests/s (billions)", "value": value,
+        "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{p.name}: N={p.n} uniform 2-D points, 0.4 per unit area, "
+                               f"cutoff {p.cutoff}, {p.max_neighbors} list slots; each step "
+                               "tests all N^2 ordered pairs",
+                   "n_points": p.n, "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "alu", "achieved": value / world, "peak": peak, "unit": "Gpairs/s",
+                     "frac": value / world / peak, "traffic": None,
+                     "peak_basis": f"{sms} SMs x {f_max:g} MHz ({f_src}) x {FP32_LANES_PER_SM} "
+                                   f"FP32 lanes / {NEIGHBOR_FP32_OPS} FP32 ops per pair test"},
+        "mean_neighbors": float(nn.double().mean().item()), "gpu_launches": launches,
+        "clocks": clocks, "impl": "ours",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.impl == "ours" and args.mode == "neighbors":
+        run_neighbors(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -174,6 +174,29 @@ int nbody_render_points(const float *pos_mass, float *ndc, float *rgba,
                         float min_w, float max_w, void *cuda_stream);
 
 /*
+ * 2-D cutoff neighbour list over all pairs, without atomics: the neighbour-
+ * list example of "CUDA编程（九）原子函数的合理使用" §3 in its atomic-free form
+ * (every pair (i, j), j != i, tested by the thread of i, which alone writes
+ * the list of i).  In single precision, each operation rounded separately:
+ *     x12 = x[j] - x[i], y12 = y[j] - y[i], d2 = x12*x12 + y12*y12,
+ *     j is a neighbour of i when d2 < cutoff*cutoff (cutoff*cutoff rounded
+ *     to float).
+ *   x, y    in   n floats each (4-byte aligned device arrays).
+ *   nn      out  n int32: number of neighbours of each point (not capped).
+ *   nl      out  max_neighbors * n int32, transposed as on the page:
+ *                nl[k * n + i] = k-th neighbour of i in ascending index
+ *                order for k < min(nn[i], max_neighbors), -1 for the other
+ *                k < max_neighbors.  nn[i] > max_neighbors means the list of
+ *                i was truncated.  May be NULL when max_neighbors == 0.
+ *   cutoff  finite, > 0, with cutoff*cutoff a normal float.
+ * nn and nl must not overlap each other or x, y.  Errors as for
+ * nbody_accel; n == 0 is a no-op.  Deterministic: no atomics.
+ */
+int nbody_neighbors_2d(const float *x, const float *y, int64_t n, float cutoff,
+                       int max_neighbors, int32_t *nn, int32_t *nl,
+                       void *cuda_stream);
+
+/*
  * Wait for the stream, then report and clear the device-side status of
  * this device: NBODY_OK, NBODY_ETIMEOUT, or NBODY_ECUDA if the stream
  * reported a CUDA error.

@@ -46,6 +46,8 @@ class Oracle:
         lib.oracle_leapfrog_kdk.restype = i32
         lib.oracle_render_points.argtypes = [p, i64, d, d, d, d, d, p, p]
         lib.oracle_render_points.restype = i32
+        lib.oracle_neighbors_2d.argtypes = [p, p, i64, ctypes.c_float, i32, p, i64, p, p, i32]
+        lib.oracle_neighbors_2d.restype = i32
         self.lib = lib
         self.path = path
 
@@ -131,6 +133,28 @@ class Oracle:
         return ndc, rgba
 
 
+    def neighbors_2d(self, x, y, cutoff: float, max_neighbors: int, idx=None, threads: int = 0):
+        """All-pairs 2-D cutoff neighbour list in float32 ("CUDA编程（九）" §3):
+        returns (nn (m,) int32, nl (max_neighbors, m) int32, -1 = empty) for
+        the m targets ``idx`` (all n points when None)."""
+        xs = np.ascontiguousarray(x, dtype=np.float32)
+        ys = np.ascontiguousarray(y, dtype=np.float32)
+        n = xs.shape[0]
+        if ys.shape[0] != n:
+            raise ValueError("x and y must have the same length")
+        idx_arr = None if idx is None else np.ascontiguousarray(idx, dtype=np.int64)
+        m = n if idx_arr is None else idx_arr.shape[0]
+        nn = np.zeros(m, dtype=np.int32)
+        nl = np.zeros((max(int(max_neighbors), 0), m), dtype=np.int32)
+        rc = self.lib.oracle_neighbors_2d(_ptr(xs), _ptr(ys), n, float(cutoff),
+                                          int(max_neighbors),
+                                          None if idx_arr is None else _ptr(idx_arr), m,
+                                          _ptr(nn), _ptr(nl), int(threads))
+        if rc < 0:
+            raise ValueError("oracle_neighbors_2d: bad argument")
+        return nn, nl
+
+
 _default: Oracle | None = None
 
 
@@ -159,3 +183,7 @@ def leapfrog_kdk(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int
 
 def render_points(pos_mass, max_xyz, min_w: float, max_w: float):
     return default().render_points(pos_mass, max_xyz, min_w, max_w)
+
+
+def neighbors_2d(x, y, cutoff: float, max_neighbors: int, idx=None, threads: int = 0):
+    return default().neighbors_2d(x, y, cutoff, max_neighbors, idx, threads)

@@ -207,3 +207,53 @@ int oracle_render_points(const double *pos_mass, int64_t n, double max_x, double
     }
     return 0;
 }
+
+/*
+ * 2-D cutoff neighbour list, all pairs, without atomics ("CUDA编程（九）原子函数
+ * 的合理使用" §3, the neighbour-list example: the version that tests every pair
+ * (n1, n2), n2 != n1, and writes only the lists of n1).  In the page's single
+ * precision: x12 = x[n2] - x[n1], y12 = y[n2] - y[n1],
+ * d2 = x12 * x12 + y12 * y12, neighbour when d2 < cutoff * cutoff (all float,
+ * every operation rounded separately: this file is built with
+ * -ffp-contract=off).  nn[n1] = number of neighbours; nl[k * n + n1] = the
+ * k-th neighbour in ascending index order for k < min(nn[n1], mn), -1 for the
+ * remaining k < mn (the page's transposed layout).  With idx, only the
+ * targets idx[0..n_idx) are listed (row k of nl then has n_idx entries);
+ * idx NULL means all n targets in order.  Returns 0 or -1.
+ */
+int oracle_neighbors_2d(const float *x, const float *y, int64_t n, float cutoff, int mn,
+                        const int64_t *idx, int64_t n_idx, int32_t *nn, int32_t *nl,
+                        int threads)
+{
+    if (n < 0 || mn < 0 || n_idx < 0 || (idx == NULL && n_idx != n))
+        return -1;
+    if (n_idx > 0 && (x == NULL || y == NULL || nn == NULL || (mn > 0 && nl == NULL)))
+        return -1;
+    if (idx != NULL)
+        for (int64_t k = 0; k < n_idx; ++k)
+            if (idx[k] < 0 || idx[k] >= n)
+                return -1;
+    const float cutoff_square = cutoff * cutoff;
+    const int nt = oracle_threads(threads);
+#pragma omp parallel for schedule(dynamic, 64) num_threads(nt)
+    for (int64_t k = 0; k < n_idx; ++k) {
+        const int64_t n1 = idx ? idx[k] : k;
+        const float x1 = x[n1];
+        const float y1 = y[n1];
+        int32_t count = 0;
+        for (int64_t n2 = 0; n2 < n; ++n2) {
+            const float x12 = x[n2] - x1;
+            const float y12 = y[n2] - y1;
+            const float distance_square = x12 * x12 + y12 * y12;
+            if (distance_square < cutoff_square && n2 != n1) {
+                if (count < mn)
+                    nl[(int64_t)count * n_idx + k] = (int32_t)n2;
+                ++count;
+            }
+        }
+        nn[k] = count;
+        for (int32_t q = count; q < mn; ++q)
+            nl[(int64_t)q * n_idx + k] = -1;
+    }
+    return 0;
+}

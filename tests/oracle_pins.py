@@ -453,6 +453,117 @@ def pin_render_colour_ramp(o):
 
 RENDER_PINS = [pin_render_ndc_equals_x_over_limit, pin_render_colour_ramp]
 
+
+# ---------------------------------------------------------------------------
+# 2-D cutoff neighbour-list pins ("CUDA编程（九）原子函数的合理使用" §3)
+# ---------------------------------------------------------------------------
+
+
+def _lattice(k):
+    """k x k unit square lattice, row-major indices, integer coordinates."""
+    ix, iy = np.meshgrid(np.arange(k), np.arange(k), indexing="xy")
+    return ix.ravel().astype(np.float32), iy.ravel().astype(np.float32)
+
+
+def _lattice_neighbours(k, offsets):
+    out = []
+    for y in range(k):
+        for x in range(k):
+            nb = [(y + dy) * k + (x + dx) for dx, dy in offsets
+                  if 0 <= x + dx < k and 0 <= y + dy < k]
+            out.append(sorted(nb))
+    return out
+
+
+def pin_neighbors_square_lattice(o):
+    """Unit lattice: cutoff 1.2 keeps the 4 edge neighbours, cutoff 1.5 adds
+    the 4 diagonals (sqrt 2), cutoff exactly 2 adds nothing more because the
+    test is strict (d^2 = 4 is not < 4).  Lists come in ascending order."""
+    k = 7
+    x, y = _lattice(k)
+    four = [(1, 0), (-1, 0), (0, 1), (0, -1)]
+    eight = four + [(1, 1), (1, -1), (-1, 1), (-1, -1)]
+    for cutoff, offs in [(1.2, four), (1.5, eight), (2.0, eight)]:
+        nn, nl = o.neighbors_2d(x, y, cutoff, 12)
+        want = _lattice_neighbours(k, offs)
+        for i in range(k * k):
+            assert nn[i] == len(want[i]), (cutoff, i, nn[i], want[i])
+            assert list(nl[:nn[i], i]) == want[i], (cutoff, i)
+            assert np.all(nl[nn[i]:, i] == -1)
+
+
+def pin_neighbors_symmetric(o):
+    rng = np.random.default_rng(15)
+    x = (8 * rng.random(300)).astype(np.float32)
+    y = (8 * rng.random(300)).astype(np.float32)
+    nn, nl = o.neighbors_2d(x, y, 1.1, 64)
+    assert nn.max() < 64
+    pairs = {(i, int(j)) for i in range(300) for j in nl[:nn[i], i]}
+    assert all((j, i) in pairs for i, j in pairs), "neighbour relation not symmetric"
+    assert all(i != j for i, j in pairs), "a point is its own neighbour"
+
+
+def _half_loop_lists(x, y, cutoff, mn):
+    """The page's CPU algorithm, restated in pure Python with float32 scalars:
+    n2 > n1 only, and every hit is appended to both lists."""
+    n = len(x)
+    c2 = np.float32(cutoff) * np.float32(cutoff)
+    lists = [[] for _ in range(n)]
+    for n1 in range(n):
+        for n2 in range(n1 + 1, n):
+            x12 = np.float32(x[n2] - x[n1])
+            y12 = np.float32(y[n2] - y[n1])
+            d2 = np.float32(np.float32(x12 * x12) + np.float32(y12 * y12))
+            if d2 < c2:
+                lists[n1].append(n2)
+                lists[n2].append(n1)
+    nn = np.array([len(l) for l in lists], dtype=np.int32)
+    nl = np.full((mn, n), -1, dtype=np.int32)
+    for i, l in enumerate(lists):
+        for k, j in enumerate(l[:mn]):
+            nl[k, i] = j
+    return nn, nl
+
+
+def pin_neighbors_match_half_loop_algorithm(o):
+    rng = np.random.default_rng(16)
+    for n, cutoff, mn in [(2, 5.0, 3), (60, 1.9, 10), (150, 1.9, 4)]:
+        x = (6 * rng.random(n)).astype(np.float32)
+        y = (6 * rng.random(n)).astype(np.float32)
+        nn, nl = o.neighbors_2d(x, y, cutoff, mn)
+        wn, wl = _half_loop_lists(x, y, cutoff, mn)
+        assert np.array_equal(nn, wn) and np.array_equal(nl, wl), (n, cutoff, mn)
+
+
+def pin_neighbors_truncation_and_duplicates(o):
+    """20 points packed in a small circle: each has 19 neighbours (two of them
+    coincide and are each other's neighbour, never their own); the list keeps
+    the 10 lowest indices."""
+    th = np.linspace(0.0, 2 * np.pi, 19, endpoint=False)
+    x = np.concatenate([0.1 * np.cos(th), [0.1]]).astype(np.float32)
+    y = np.concatenate([0.1 * np.sin(th), [0.0]]).astype(np.float32)  # last = copy of point 0
+    nn, nl = o.neighbors_2d(x, y, 1.0, 10)
+    assert np.all(nn == 19)
+    for i in range(20):
+        assert list(nl[:, i]) == [j for j in range(20) if j != i][:10]
+    far = np.array([0.0, 100.0], dtype=np.float32)
+    nn, nl = o.neighbors_2d(far, far, 1.0, 3)
+    assert np.all(nn == 0) and np.all(nl == -1)
+
+
+def pin_neighbors_sampled_rows_match_full(o):
+    rng = np.random.default_rng(17)
+    x = (10 * rng.random(400)).astype(np.float32)
+    y = (10 * rng.random(400)).astype(np.float32)
+    nn, nl = o.neighbors_2d(x, y, 1.9, 6)
+    idx = np.array([399, 0, 17, 17, 200])
+    sn, sl = o.neighbors_2d(x, y, 1.9, 6, idx=idx)
+    assert np.array_equal(sn, nn[idx]) and np.array_equal(sl, nl[:, idx])
+
+
+NEIGHBOR_PINS = [pin_neighbors_sampled_rows_match_full, pin_neighbors_square_lattice, pin_neighbors_symmetric,
+                 pin_neighbors_match_half_loop_algorithm, pin_neighbors_truncation_and_duplicates]
+
 ACCEL_PINS = [
     pin_two_body_closed_form,
     pin_ring_axis_closed_form,
@@ -473,7 +584,7 @@ LEAPFROG_PINS = [
     pin_leapfrog_momentum_and_com,
     pin_leapfrog_composition,
 ]
-ALL_PINS = ACCEL_PINS + LEAPFROG_PINS + KDK_PINS + RENDER_PINS
+ALL_PINS = ACCEL_PINS + LEAPFROG_PINS + KDK_PINS + RENDER_PINS + NEIGHBOR_PINS
 
 
 def failing_pins(o) -> list[str]:

@@ -37,7 +37,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(nbody_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(nbody_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_bound_functions():
@@ -158,3 +158,22 @@ def test_render_bad_pointers(L):
     assert render(L, A, B, B, 10) == nb.EINVAL
     assert render(L, A, B, C, -1) == nb.EINVAL
     assert render(L, 0, 0, 0, 0) == nb.OK
+
+
+def neighbors(L, x, y, n, cutoff, mn, nn, nl):
+    return L.nbody_neighbors_2d(ctypes.c_void_p(x), ctypes.c_void_p(y), n, cutoff, mn,
+                                ctypes.c_void_p(nn), ctypes.c_void_p(nl), S)
+
+
+def test_neighbors_bad_arguments(L):
+    D = 0x40000
+    assert neighbors(L, A, B, 10, 0.0, 4, C, D) == nb.EINVAL
+    assert neighbors(L, A, B, 10, math.nan, 4, C, D) == nb.EINVAL
+    assert neighbors(L, A, B, 10, 1e-30, 4, C, D) == nb.EINVAL  # cutoff^2 not a normal float
+    assert neighbors(L, A, B, 10, 1.0, -1, C, D) == nb.EINVAL
+    assert neighbors(L, A, B, -1, 1.0, 4, C, D) == nb.EINVAL
+    assert neighbors(L, A, B, 10, 1.0, 4, C, 0) == nb.EINVAL
+    assert neighbors(L, A + 2, B, 10, 1.0, 4, C, D) == nb.EINVAL
+    assert neighbors(L, A, B, 10, 1.0, 4, A, D) == nb.EINVAL  # nn overlaps x
+    assert neighbors(L, A, B, 10, 1.0, 4, C, C + 8) == nb.EINVAL  # nl overlaps nn
+    assert neighbors(L, 0, 0, 0, 1.0, 4, 0, 0) == nb.OK

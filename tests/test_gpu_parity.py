@@ -417,3 +417,58 @@ def test_render_after_steps():
     ndc, rgba = gpu_render(p, (4.0, 4.0, 4.0), 0.0, 2.0 / w.n)
     rn, rc = oracle.render_points(p, (4.0, 4.0, 4.0), 0.0, np.float32(2.0 / w.n))
     assert render_err(ndc, rn) <= RENDER_TOL and render_err(rgba, rc) <= RENDER_TOL
+
+
+# ---------------------------------------------------------------------------
+# 2-D cutoff neighbour list: counts and lists bit-exact against the oracle
+# ---------------------------------------------------------------------------
+
+
+def gpu_neighbors(x, y, cutoff, mn):
+    import torch
+    import all_pairs_body_gb300 as nb
+    tx = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    ty = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).cuda()
+    nn = torch.full((len(x),), -7, dtype=torch.int32, device="cuda")
+    nl = torch.full((mn, len(x)), -7, dtype=torch.int32, device="cuda")
+    nb.neighbors_2d(tx, ty, cutoff, mn, nn=nn, nl=nl)
+    nb.sync()
+    return nn.cpu().numpy(), nl.cpu().numpy()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 127, 128, 129, 511, 512, 513, 1000, 20000, 65537])
+def test_neighbors_match_oracle(n):
+    p = W.points_2d(n)
+    nn, nl = gpu_neighbors(p.x, p.y, p.cutoff, p.max_neighbors)
+    rn, rl = oracle.neighbors_2d(p.x, p.y, p.cutoff, p.max_neighbors)
+    assert np.array_equal(nn, rn) and np.array_equal(nl, rl)
+
+
+def test_neighbors_lattice_boundary_cases():
+    k = 37
+    ix, iy = np.meshgrid(np.arange(k), np.arange(k), indexing="xy")
+    x, y = ix.ravel().astype(np.float32), iy.ravel().astype(np.float32)
+    for cutoff in (1.0, 1.2, np.sqrt(2.0), 1.5, 2.0, 2.5):  # exact-distance ties included
+        nn, nl = gpu_neighbors(x, y, cutoff, 24)
+        rn, rl = oracle.neighbors_2d(x, y, cutoff, 24)
+        assert np.array_equal(nn, rn) and np.array_equal(nl, rl), cutoff
+
+
+def test_neighbors_truncated_and_empty_lists():
+    p = W.points_2d(30000)
+    for mn in (0, 1, 3, 64):
+        nn, nl = gpu_neighbors(p.x, p.y, p.cutoff, mn)
+        rn, rl = oracle.neighbors_2d(p.x, p.y, p.cutoff, mn)
+        assert np.array_equal(nn, rn) and np.array_equal(nl, rl), mn
+    assert (rn > 3).any()
+
+
+def test_neighbors_large_sampled():
+    """2^20 points: 4096 seeded sampled targets against the oracle, plus the
+    symmetry of the relation (the sum of all counts is even)."""
+    p = W.points_2d(1048576)
+    nn, nl = gpu_neighbors(p.x, p.y, p.cutoff, p.max_neighbors)
+    assert int(nn.astype(np.int64).sum()) % 2 == 0
+    idx = W.sample_indices(p.n, 5)
+    rn, rl = oracle.neighbors_2d(p.x, p.y, p.cutoff, p.max_neighbors, idx=idx)
+    assert np.array_equal(nn[idx], rn) and np.array_equal(nl[:, idx], rl)

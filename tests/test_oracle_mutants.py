@@ -71,6 +71,18 @@ KDK_FIRST_ACCEL = (
 )
 
 MUTANTS = {
+    "neighbors_not_strict": [("if (distance_square < cutoff_square && n2 != n1)",
+                              "if (distance_square <= cutoff_square && n2 != n1)")],
+    "neighbors_self_included": [("if (distance_square < cutoff_square && n2 != n1)",
+                                 "if (distance_square < cutoff_square)")],
+    "neighbors_cutoff_not_squared": [("const float cutoff_square = cutoff * cutoff;",
+                                      "const float cutoff_square = cutoff;")],
+    "neighbors_row_major_list": [("nl[(int64_t)count * n_idx + k] = (int32_t)n2;",
+                                  "nl[k * mn + count] = (int32_t)n2;")],
+    "neighbors_empty_slots_not_cleared": [("            nl[(int64_t)q * n_idx + k] = -1;",
+                                           "            (void)q;")],
+    "neighbors_sample_index_ignored": [("const int64_t n1 = idx ? idx[k] : k;",
+                                        "const int64_t n1 = k;")],
     "render_colours_swapped": [("const double green[3] = {0.0, 1.0, 0.0};",
                                 "const double green[3] = {1.0, 0.0, 0.0};"),
                                ("const double red[3] = {1.0, 0.0, 0.0};",

@@ -28,6 +28,12 @@ Workloads (sizes and parameters as the benchmark definition states them):
 * ``cube-sweep-<N>``         N in {1000, 4097, 65537, 500000, 4194304}, uniform
                              in [0,1]^3, m=1/N, seed 4, eps2=1e-3, one
                              evaluation; 4096 sampled bodies above N=65537.
+* ``points2d-<N>``           2-D points for the cutoff neighbour list: uniform in
+                             a square of side sqrt(N / 0.4) (0.4 points per unit
+                             area, so ~4.5 neighbours within the cutoff 1.9 and
+                             a thin tail above 10), seed 5, float32.  Stands in
+                             for the coordinate file of the neighbour-list
+                             example, which is not available here.
 """
 from __future__ import annotations
 
@@ -220,6 +226,8 @@ def by_name(name: str) -> Workload:
         return ball_lognormal_1048576(int(name.rsplit("-", 1)[1]))
     if name.startswith("cube-sweep-"):
         return cube_sweep(int(name.rsplit("-", 1)[1]))
+    if name.startswith("points2d-"):
+        return points_2d(int(name.rsplit("-", 1)[1]))
     raise KeyError(name)
 
 
@@ -247,3 +255,29 @@ def random_velocities(n: int, seed: int, scale: float = 0.1) -> np.ndarray:
     v[:, :3] = scale * rng.standard_normal((n, 3))
     v[:, 3] = rng.random(n)  # arbitrary w: the library must leave it untouched
     return np.ascontiguousarray(v.astype(np.float32))
+
+
+NEIGHBOR_CUTOFF = 1.9
+NEIGHBOR_MAX = 10
+
+
+@dataclasses.dataclass
+class Points2D:
+    name: str
+    x: np.ndarray  # (n,) float32
+    y: np.ndarray  # (n,) float32
+    cutoff: float
+    max_neighbors: int
+
+    @property
+    def n(self) -> int:
+        return int(self.x.shape[0])
+
+
+def points_2d(n: int, seed: int = 5, density: float = 0.4) -> Points2D:
+    rng = np.random.default_rng(seed)
+    side = float(np.sqrt(n / density))
+    xy = side * rng.random((n, 2))
+    return Points2D(f"points2d-{n}", np.ascontiguousarray(xy[:, 0].astype(np.float32)),
+                    np.ascontiguousarray(xy[:, 1].astype(np.float32)), NEIGHBOR_CUTOFF,
+                    NEIGHBOR_MAX)
