@@ -544,8 +544,9 @@ int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float
   return launch_status();
 }
 
-constexpr int kNeighborKI = 4;
+constexpr int kNeighborKI = 8;
 constexpr int kNeighborNT = 128;
+constexpr int kNeighborU = 4;
 
 int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int max_neighbors,
                    int32_t* nn, int32_t* nl, cudaStream_t st) {
@@ -579,7 +580,8 @@ int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int 
   NeighborArgs a{x, y, static_cast<int>(n), c2, max_neighbors, nn, nl, ceil_div(n, kNeighborNT)};
   const long long blocks = ceil_div(n, static_cast<long long>(kNeighborKI) * kNeighborNT);
   count_launches(1);
-  neighbors_2d<kNeighborKI, kNeighborNT><<<static_cast<unsigned>(blocks), kNeighborNT, 0, st>>>(a);
+  neighbors_2d<kNeighborKI, kNeighborNT, kNeighborU>
+      <<<static_cast<unsigned>(blocks), kNeighborNT, 0, st>>>(a);
   return launch_status();
 }
 

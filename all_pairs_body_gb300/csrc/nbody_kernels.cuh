@@ -671,13 +671,18 @@ struct NeighborArgs {
 // a two-buffer shared ring filled by plain loads (one source per thread per
 // tile, prefetched into registers during the previous tile).  One CTA covers
 // the whole j range of its targets, so every list is appended in ascending j.
-// Padding sources sit at +inf and padding targets are NaN: neither can pass
-// the test.  Hits are rare, so the append runs in a divergent branch.
-template <int KI, int NT>
+// Hits are rare (a few per million pairs): U sources at a time are tested
+// into registers, their minimum taken on the ALU pipe (FMNMX), and a single
+// branch per group enters the exact per-pair check, which appends in
+// ascending j.  Padding sources sit at +inf and padding targets are NaN;
+// neither passes the per-pair test (the minimum ignores NaN, the test does
+// not).
+template <int KI, int NT, int U>
 __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KI / 2;
   constexpr int TJ = NT;
+  static_assert(TJ % U == 0, "whole groups per tile");
   __shared__ __align__(16) float4 tile[2][TJ];
 
   const int tid = threadIdx.x;
@@ -712,25 +717,38 @@ __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
       py = jl < a.n ? a.y[jl] : __int_as_float(0x7f800000);
     }
     const long long j0 = t * TJ;
-#pragma unroll 4
-    for (int jj = 0; jj < TJ; ++jj) {
-      const float4 b = tile[s][jj];
-      const float2 X = make_float2(b.x, b.y);
-      const float2 Y = make_float2(b.z, b.w);
+#pragma unroll 1
+    for (int jg = 0; jg < TJ; jg += U) {
+      float2 d2[U][P];
+      float lo = __int_as_float(0x7f800000);
 #pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const float2 dx = __fadd2_rn(X, nx[p]);
-        const float2 dy = __fadd2_rn(Y, ny[p]);
-        const float2 d2 = __fadd2_rn(__fmul2_rn(dx, dx), __fmul2_rn(dy, dy));
-        if (d2.x < c2 || d2.y < c2) {
-          const long long j = j0 + jj;
+      for (int u = 0; u < U; ++u) {
+        const float4 b = tile[s][jg + u];
+        const float2 X = make_float2(b.x, b.y);
+        const float2 Y = make_float2(b.z, b.w);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const long long i = base + (2 * p + h) * NT + tid;
-            if ((h ? d2.y : d2.x) < c2 && j != i) {
-              int& c = cnt[2 * p + h];
-              if (c < a.max_neighbors) a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
-              ++c;
+        for (int p = 0; p < P; ++p) {
+          const float2 dx = __fadd2_rn(X, nx[p]);
+          const float2 dy = __fadd2_rn(Y, ny[p]);
+          d2[u][p] = __fadd2_rn(__fmul2_rn(dx, dx), __fmul2_rn(dy, dy));
+          lo = fminf(lo, fminf(d2[u][p].x, d2[u][p].y));
+        }
+      }
+      if (lo < c2) {  // rare: some pair of the group is close
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const long long j = j0 + jg + u;
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const long long i = base + (2 * p + h) * NT + tid;
+              if ((h ? d2[u][p].y : d2[u][p].x) < c2 && j != i) {
+                int& c = cnt[2 * p + h];
+                if (c < a.max_neighbors)
+                  a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
+                ++c;
+              }
             }
           }
         }
