@@ -31,7 +31,9 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_leapfrog_step_with", "nbody_sync", "nbody_plan", "nbody_strerror",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
            "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
-           "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d")
+           "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d",
+           "nbody_accel_layout", "nbody_leapfrog_step_layout")
+ROWS4, ROWS3, BLOCKS3 = 0, 1, 2
 NOALLOC_MAX_N = 65536
 
 
@@ -66,6 +68,8 @@ def lib() -> ctypes.CDLL:
             "nbody_leapfrog_kdk_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
             "nbody_render_points": [p, p, p, i64, f32, f32, f32, f32, f32, p],
             "nbody_neighbors_2d": [p, p, i64, f32, i32, p, p, p],
+            "nbody_accel_layout": [p, p, i64, f32, i32, p],
+            "nbody_leapfrog_step_layout": [p, p, p, i64, f32, f32, i32, i32, p],
             "nbody_sync": [p],
             "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
             "nbody_selftest_timeout": [i32, p],
@@ -205,6 +209,38 @@ def neighbors_2d(x, y, cutoff: float, max_neighbors: int, nn=None, nl=None, stre
                                   ctypes.c_void_p(nl.data_ptr() if mn > 0 else 0), _stream(stream))
     _check(rc, "nbody_neighbors_2d")
     return nn, nl
+
+
+def _vec(t, n: int, layout: int, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    want = 4 * n if layout == ROWS4 else 3 * n
+    if t.numel() != want:
+        raise ValueError(f"{name} must hold {want} floats for layout {layout}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def accel_layout(pos_mass, out, eps2: float, layout: int, stream=None):
+    """Accelerations into ``out`` in ``layout`` (ROWS4: (n,4); ROWS3: (n,3);
+    BLOCKS3: (3,n))."""
+    n = int(pos_mass.shape[0])
+    rc = lib().nbody_accel_layout(_rows(pos_mass, None, "pos_mass"), _vec(out, n, layout, "out"), n,
+                                  float(eps2), int(layout), _stream(stream))
+    _check(rc, "nbody_accel_layout")
+    return out
+
+
+def leapfrog_step_layout(pos_mass, vel, accel_out, eps2: float, dt: float, steps: int,
+                         layout: int, stream=None) -> None:
+    """``steps`` half-kick + drift steps with ``vel`` and ``accel_out`` in ``layout``."""
+    n = int(pos_mass.shape[0])
+    rc = lib().nbody_leapfrog_step_layout(_rows(pos_mass, None, "pos_mass"),
+                                          _vec(vel, n, layout, "vel"),
+                                          _vec(accel_out, n, layout, "accel"), n, float(eps2),
+                                          float(dt), int(steps), int(layout), _stream(stream))
+    _check(rc, "nbody_leapfrog_step_layout")
 
 
 def sync(stream=None) -> None:

@@ -299,6 +299,11 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
+bool overlaps_sized(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bbytes && y < x + abytes;
+}
+
 int check_scalars(int64_t n, float eps2, int path, int split) {
   if (n < 0 || n > static_cast<int64_t>(INT32_MAX)) return NBODY_EINVAL;
   if (!std::isfinite(eps2) || !(eps2 > 0.0f)) return NBODY_EINVAL;
@@ -326,6 +331,33 @@ int launch_status() {
 // --------------------------------------------------------------------------
 // launch sequences
 // --------------------------------------------------------------------------
+
+Epilogue make_epilogue(const float4* pos, void* accel, void* vel, float4* pos_next,
+                       float4* dup_next, const float4* dup, float kick, float dt, int layout,
+                       long long n) {
+  Epilogue e;
+  e.pos = pos;
+  e.accel = static_cast<float*>(accel);
+  e.vel = static_cast<float*>(vel);
+  e.pos_next = pos_next;
+  e.dup_next = dup_next;
+  e.dup = dup;
+  e.kick = kick;
+  e.dt = dt;
+  e.layout = layout;
+  e.n = n;
+  return e;
+}
+
+// Bytes and alignment of one velocity/acceleration array in `layout`.
+size_t vec_bytes(int layout, long long n) {
+  return static_cast<size_t>(n) * (layout == kRows4 ? 16 : 12);
+}
+
+bool vec_aligned(const void* p, int layout) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return layout == kRows4 ? (a & 15u) == 0 : (a & 3u) == 0;
+}
 
 void launch_expand(const Plan& p, const float4* pos, float4* dup, float4* dup2, int* tile_exact,
                    long long n, cudaStream_t st) {
@@ -374,14 +406,16 @@ void launch_force(const Plan& p, const float4* pos, const float4* dup, const int
 }
 
 int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int path, int split,
-               cudaStream_t st) {
+               int layout, cudaStream_t st) {
   int rc = check_scalars(n, eps2, path, split);
   if (rc != NBODY_OK) return rc;
+  if (layout < kRows4 || layout > kBlocks3) return NBODY_EINVAL;
   if (n == 0) return NBODY_OK;
   if (pos_mass == nullptr || accel == nullptr) return NBODY_EINVAL;
-  if (!aligned16(pos_mass) || !aligned16(accel)) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !vec_aligned(accel, layout)) return NBODY_EINVAL;
   const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
-  if (overlaps(pos_mass, accel, bytes)) return NBODY_EINVAL;
+  const size_t vbytes = vec_bytes(layout, n);
+  if (overlaps_sized(pos_mass, bytes, accel, vbytes)) return NBODY_EINVAL;
   int dev = 0;
   if ((rc = current_device(&dev)) != NBODY_OK) return rc;
   if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
@@ -394,23 +428,37 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   float4* dup = static_cast<float4*>(s->dup_a.p);
   int* flags = static_cast<int*>(s->tile_exact.p);
-  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  const Epilogue epi =
+      make_epilogue(pos, accel, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, layout, n);
   if (p.path != NBODY_PATH_WARP) launch_expand(p, pos, dup, nullptr, flags, n, st);
   launch_force(p, pos, dup, flags, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
   return launch_status();
 }
 
-int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
-                  int steps, int path, int split, cudaStream_t st) {
+// `steps` steps of either scheme, velocities and accelerations in `layout`.
+//   kdk == false: the pages' step, one force pass per step: half kick with
+//                 a(x(t)), drift ("CUDA N-Body Simulation" §1.3).
+//   kdk == true:  kick-drift-kick, steps + 1 force passes: pass 0 half-kicks
+//                 and drifts, passes 1..steps-1 kick by a full dt (closing
+//                 half kick of one step fused with the opening half kick of
+//                 the next) and drift, the last pass half-kicks only.
+// Within a pass every acceleration uses the start-of-pass positions; the new
+// positions go to the other buffer of a ping-pong pair, and an odd number of
+// drifts starts from a copy so that the result lands in the caller's buffer.
+int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
+              int steps, int path, int split, int layout, bool kdk, cudaStream_t st) {
   int rc = check_scalars(n, eps2, path, split);
   if (rc != NBODY_OK) return rc;
   if (!std::isfinite(dt) || steps < 0) return NBODY_EINVAL;
+  if (layout < kRows4 || layout > kBlocks3) return NBODY_EINVAL;
   if (n == 0 || steps == 0) return NBODY_OK;
   if (pos_mass == nullptr || vel == nullptr || accel == nullptr) return NBODY_EINVAL;
-  if (!aligned16(pos_mass) || !aligned16(vel) || !aligned16(accel)) return NBODY_EINVAL;
+  if (!aligned16(pos_mass) || !vec_aligned(vel, layout) || !vec_aligned(accel, layout))
+    return NBODY_EINVAL;
   const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
-  if (overlaps(pos_mass, accel, bytes) || overlaps(vel, accel, bytes) ||
-      overlaps(pos_mass, vel, bytes))
+  const size_t vbytes = vec_bytes(layout, n);
+  if (overlaps_sized(pos_mass, bytes, accel, vbytes) || overlaps_sized(vel, vbytes, accel, vbytes) ||
+      overlaps_sized(pos_mass, bytes, vel, vbytes))
     return NBODY_EINVAL;
   int dev = 0;
   if ((rc = current_device(&dev)) != NBODY_OK) return rc;
@@ -426,62 +474,7 @@ int leapfrog_impl(float* pos_mass, float* vel, float* accel, int64_t n, float ep
   float4* alt = static_cast<float4*>(s->pos_alt.p);
   float4* cur = user;
   float4* nxt = alt;
-  if (steps & 1) {  // an odd count then ends in the caller's buffer
-    if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
-      cudaGetLastError();
-      return NBODY_ECUDA;
-    }
-    cur = alt;
-    nxt = user;
-  }
-  float4* dup_cur = static_cast<float4*>(s->dup_a.p);
-  float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
-  int* flags = static_cast<int*>(s->tile_exact.p);
-  if (p.path != NBODY_PATH_WARP) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
-  const float half_dt = 0.5f * dt;
-  for (int k = 0; k < steps; ++k) {
-    const bool last = (k + 1 == steps);
-    const bool chain = p.path != NBODY_PATH_WARP && !last;
-    Epilogue epi{cur, reinterpret_cast<float4*>(accel), reinterpret_cast<float4*>(vel), nxt,
-                 chain ? dup_nxt : nullptr, chain ? dup_cur : nullptr, half_dt, dt};
-    launch_force(p, cur, dup_cur, flags, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
-    std::swap(cur, nxt);
-    std::swap(dup_cur, dup_nxt);
-  }
-  return launch_status();
-}
-
-// Kick-drift-kick: steps + 1 force passes.  Pass 0 half-kicks and drifts,
-// passes 1..steps-1 kick by a full dt (the closing half kick of one step and
-// the opening half kick of the next, fused) and drift, the last pass only
-// half-kicks with the accelerations at the final positions.
-int leapfrog_kdk_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
-                      int steps, int path, int split, cudaStream_t st) {
-  int rc = check_scalars(n, eps2, path, split);
-  if (rc != NBODY_OK) return rc;
-  if (!std::isfinite(dt) || steps < 0) return NBODY_EINVAL;
-  if (n == 0 || steps == 0) return NBODY_OK;
-  if (pos_mass == nullptr || vel == nullptr || accel == nullptr) return NBODY_EINVAL;
-  if (!aligned16(pos_mass) || !aligned16(vel) || !aligned16(accel)) return NBODY_EINVAL;
-  const size_t bytes = static_cast<size_t>(n) * sizeof(float4);
-  if (overlaps(pos_mass, accel, bytes) || overlaps(vel, accel, bytes) ||
-      overlaps(pos_mass, vel, bytes))
-    return NBODY_EINVAL;
-  int dev = 0;
-  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
-  if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
-  if ((rc = check_device_pointer(vel, dev)) != NBODY_OK) return rc;
-  if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
-  Plan p;
-  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
-  Scratch* s = nullptr;
-  if ((rc = get_scratch(dev, st, p, n, true, &s)) != NBODY_OK) return rc;
-
-  float4* user = reinterpret_cast<float4*>(pos_mass);
-  float4* alt = static_cast<float4*>(s->pos_alt.p);
-  float4* cur = user;
-  float4* nxt = alt;
-  if (steps & 1) {  // `steps` drifts then end in the caller's buffer
+  if (steps & 1) {  // an odd number of drifts then ends in the caller's buffer
     if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
       cudaGetLastError();
       return NBODY_ECUDA;
@@ -493,19 +486,23 @@ int leapfrog_kdk_impl(float* pos_mass, float* vel, float* accel, int64_t n, floa
   float4* dup_cur = static_cast<float4*>(s->dup_a.p);
   float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
   int* flags = static_cast<int*>(s->tile_exact.p);
-  if (tiled) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
-  float4* acc = reinterpret_cast<float4*>(accel);
-  float4* v = reinterpret_cast<float4*>(vel);
   float4* partial = static_cast<float4*>(s->partial.p);
+  if (tiled) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
   for (int k = 0; k < steps; ++k) {
-    Epilogue epi{cur, acc, v, nxt, tiled ? dup_nxt : nullptr, tiled ? dup_cur : nullptr,
-                 k == 0 ? 0.5f * dt : dt, dt};
+    // the expanded next positions are needed by a following force pass only
+    const bool chain = tiled && (kdk || k + 1 < steps);
+    const float kick = (kdk && k > 0) ? dt : 0.5f * dt;
+    const Epilogue epi = make_epilogue(cur, accel, vel, nxt, chain ? dup_nxt : nullptr,
+                                       chain ? dup_cur : nullptr, kick, dt, layout, n);
     launch_force(p, cur, dup_cur, flags, n, eps2, partial, epi, st);
     std::swap(cur, nxt);
     std::swap(dup_cur, dup_nxt);
   }
-  Epilogue last{cur, acc, v, nullptr, nullptr, nullptr, 0.5f * dt, dt};
-  launch_force(p, cur, dup_cur, flags, n, eps2, partial, last, st);
+  if (kdk) {
+    const Epilogue last = make_epilogue(cur, accel, vel, nullptr, nullptr, nullptr, 0.5f * dt, dt,
+                                        layout, n);
+    launch_force(p, cur, dup_cur, flags, n, eps2, partial, last, st);
+  }
   return launch_status();
 }
 
@@ -676,7 +673,8 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   float4* dup = d.scratch;
   float4* partial = d.scratch + kNoAllocDupRows;
-  Epilogue epi{pos, reinterpret_cast<float4*>(accel), nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  const Epilogue epi =
+      make_epilogue(pos, accel, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, kRows4, n);
   // rewrites every expanded row the force kernel reads, zero padding included
   expand_sources<0><<<static_cast<unsigned>(ceil_div(npad, kFinishThreads)), kFinishThreads, 0, st>>>(
       pos, dup, nullptr, nullptr, static_cast<int>(n), npad);
@@ -700,18 +698,18 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
 extern "C" {
 
 int nbody_accel(const float* pos_mass, float* accel, int64_t n, float eps2) {
-  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0, nullptr);
+  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0, nbody::kRows4, nullptr);
 }
 
 int nbody_accel_on_stream(const float* pos_mass, float* accel, int64_t n, float eps2,
                           void* cuda_stream) {
-  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0,
+  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0, nbody::kRows4,
                            static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_accel_with(const float* pos_mass, float* accel, int64_t n, float eps2, int path,
                      int split, void* cuda_stream) {
-  return nbody::accel_impl(pos_mass, accel, n, eps2, path, split,
+  return nbody::accel_impl(pos_mass, accel, n, eps2, path, split, nbody::kRows4,
                            static_cast<cudaStream_t>(cuda_stream));
 }
 
@@ -722,32 +720,32 @@ int nbody_accel_noalloc(const float* pos_mass, float* accel, int64_t n, float ep
 
 int nbody_leapfrog_step(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
                         float dt, int steps) {
-  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
-                              nullptr);
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                          nbody::kRows4, false, nullptr);
 }
 
 int nbody_leapfrog_step_on_stream(float* pos_mass, float* vel, float* accel, int64_t n,
                                   float eps2, float dt, int steps, void* cuda_stream) {
-  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
-                              static_cast<cudaStream_t>(cuda_stream));
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                          nbody::kRows4, false, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_leapfrog_step_with(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
                              float dt, int steps, int path, int split, void* cuda_stream) {
-  return nbody::leapfrog_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split,
-                              static_cast<cudaStream_t>(cuda_stream));
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split, nbody::kRows4,
+                          false, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_leapfrog_kdk_on_stream(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
                                  float dt, int steps, void* cuda_stream) {
-  return nbody::leapfrog_kdk_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
-                                  static_cast<cudaStream_t>(cuda_stream));
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0,
+                          nbody::kRows4, true, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_leapfrog_kdk_with(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
                             float dt, int steps, int path, int split, void* cuda_stream) {
-  return nbody::leapfrog_kdk_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split,
-                                  static_cast<cudaStream_t>(cuda_stream));
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, path, split, nbody::kRows4,
+                          true, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_render_points(const float* pos_mass, float* ndc, float* rgba, int64_t n, float max_x,
@@ -760,6 +758,18 @@ int nbody_neighbors_2d(const float* x, const float* y, int64_t n, float cutoff, 
                        int32_t* nn, int32_t* nl, void* cuda_stream) {
   return nbody::neighbors_impl(x, y, n, cutoff, max_neighbors, nn, nl,
                                static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_accel_layout(const float* pos_mass, float* accel, int64_t n, float eps2, int layout,
+                       void* cuda_stream) {
+  return nbody::accel_impl(pos_mass, accel, n, eps2, NBODY_PATH_AUTO, 0, layout,
+                           static_cast<cudaStream_t>(cuda_stream));
+}
+
+int nbody_leapfrog_step_layout(float* pos_mass, float* vel, float* accel, int64_t n, float eps2,
+                               float dt, int steps, int layout, void* cuda_stream) {
+  return nbody::step_impl(pos_mass, vel, accel, n, eps2, dt, steps, NBODY_PATH_AUTO, 0, layout,
+                          false, static_cast<cudaStream_t>(cuda_stream));
 }
 
 int nbody_sync(void* cuda_stream) {
@@ -882,7 +892,7 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   cudaMemsetAsync(dup, 0, db, st);
   TiledArgs a{pos, dup, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr, nullptr,
               static_cast<uint64_t>(timeout_ms) * 1000000ull, 0};
-  Epilogue epi{pos, acc, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f};
+  const Epilogue epi = make_epilogue(pos, acc, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, kRows4, n);
   tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
   int rc = launch_status();
   const int srv = nbody_sync(cuda_stream);

@@ -201,16 +201,45 @@ __device__ __forceinline__ void interact2_lg(float2 X, float2 Y, float2 Z, float
 // finishing a body: write a_i, and for a leapfrog step kick and drift
 // ---------------------------------------------------------------------------
 
+// Layouts of the velocity and acceleration arrays (positions are always
+// float4 rows): rows of float4 (w of accel 0, w of vel kept), rows of three
+// floats, or three blocks x[0..n), y[0..n), z[0..n) ("CUDA N-Body
+// Simulation" §3.5 compares the float4 and float3 forms).
+enum VecLayout : int { kRows4 = 0, kRows3 = 1, kBlocks3 = 2 };
+
 struct Epilogue {
   const float4* pos;  // start-of-step positions (x, y, z, m)
-  float4* accel;      // out: (ax, ay, az, 0)
-  float4* vel;        // step only (nullptr: acceleration only)
+  float* accel;       // out: accelerations in `layout`
+  float* vel;         // step only (nullptr: acceleration only), in `layout`
   float4* pos_next;   // step with a drift: end-of-step positions (nullptr: kick only)
   float4* dup_next;   // optional: expanded end-of-step sources
   const float4* dup;  // with dup_next: the current expanded sources (mass encoding)
   float kick;         // velocity kick coefficient on a (dt/2 for a half kick)
   float dt;           // drift coefficient on v
+  int layout;         // VecLayout of accel and vel
+  long long n;        // bodies (block stride of kBlocks3)
 };
+
+__device__ __forceinline__ void store_vec3(float* base, int layout, long long n, long long i, float x,
+                                           float y, float z, float w) {
+  if (layout == kRows4) {
+    reinterpret_cast<float4*>(base)[i] = make_float4(x, y, z, w);
+  } else if (layout == kRows3) {
+    base[3 * i] = x;
+    base[3 * i + 1] = y;
+    base[3 * i + 2] = z;
+  } else {
+    base[i] = x;
+    base[n + i] = y;
+    base[2 * n + i] = z;
+  }
+}
+
+__device__ __forceinline__ float4 load_vec3(const float* base, int layout, long long n, long long i) {
+  if (layout == kRows4) return reinterpret_cast<const float4*>(base)[i];
+  if (layout == kRows3) return make_float4(base[3 * i], base[3 * i + 1], base[3 * i + 2], 0.f);
+  return make_float4(base[i], base[n + i], base[2 * n + i], 0.f);
+}
 
 // v <- v + kick a ; then, with a drift, x <- x + dt v.
 // The pages' step is kick = dt/2 plus the drift ("CUDA N-Body Simulation"
@@ -222,13 +251,13 @@ struct Epilogue {
 // schedule of the inner loop (up to 2.5% in a measured sweep).
 __device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
                                          float az) {
-  e.accel[i] = make_float4(ax, ay, az, 0.0f);
+  store_vec3(e.accel, e.layout, e.n, i, ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
-    float4 v = e.vel[i];
+    float4 v = load_vec3(e.vel, e.layout, e.n, i);
     v.x = fmaf(e.kick, ax, v.x);
     v.y = fmaf(e.kick, ay, v.y);
     v.z = fmaf(e.kick, az, v.z);
-    e.vel[i] = v;
+    store_vec3(e.vel, e.layout, e.n, i, v.x, v.y, v.z, v.w);
     if (e.pos_next == nullptr) return;
     float4 x = e.pos[i];
     x.x = fmaf(e.dt, v.x, x.x);

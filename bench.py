@@ -63,6 +63,9 @@ def parse_args(argv=None):
                          "only; kdk: one kick-drift-kick step (two force passes); render: the "
                          "point-shader kernel (memory-bound, reported in GB/s); neighbors: the "
                          "2-D cutoff neighbour list (pair tests/s; default points2d-1048576)")
+    ap.add_argument("--layout", choices=("rows4", "rows3", "blocks3"), default="rows4",
+                    help="velocity/acceleration layout for --mode step|accel (float4 rows, "
+                         "float3 rows, or x/y/z blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -291,9 +294,15 @@ def run_ours(args):
     w = workloads.by_name(args.workload)
     n = w.n
     dt = w.dt
+    layout = {"rows4": 0, "rows3": 1, "blocks3": 2}[args.layout]
+    if layout and args.mode not in ("step", "accel"):
+        raise SystemExit("--layout applies to --mode step and accel")
     pm = torch.from_numpy(w.pos_mass).cuda()
     vel = torch.from_numpy(w.vel).cuda()
     acc = torch.empty_like(pm)
+    if layout:
+        vel = vel[:, :3].contiguous() if layout == 1 else vel[:, :3].t().contiguous()
+        acc = torch.empty_like(vel)
     stream = torch.cuda.current_stream()
 
     ndc = torch.empty_like(pm) if args.mode == "render" else None
@@ -302,7 +311,11 @@ def run_ours(args):
     m_hi = max(float(w.pos_mass[:, 3].max()), m_lo * (1 + 1e-6) + 1e-30)
 
     def step():
-        if args.mode == "step":
+        if layout and args.mode == "step":
+            nb.leapfrog_step_layout(pm, vel, acc, w.eps2, dt, 1, layout)
+        elif layout:
+            nb.accel_layout(pm, acc, w.eps2, layout)
+        elif args.mode == "step":
             nb.leapfrog_step(pm, vel, acc, w.eps2, dt, 1)
         elif args.mode == "kdk":
             nb.leapfrog_kdk(pm, vel, acc, w.eps2, dt, 1)
@@ -353,7 +366,7 @@ def run_ours(args):
 
     # end to end through the same API with pinned host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not layout:
         h_pm = torch.from_numpy(w.pos_mass).pin_memory()
         h_v = torch.from_numpy(w.vel).pin_memory()
         o_pm = torch.empty_like(h_pm).pin_memory()
@@ -420,7 +433,7 @@ def run_ours(args):
         "data": "synthetic", "config": workload_config(w, args.mode, world),
         "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-        "plan": plan, "impl": "ours",
+        "plan": plan, "layout": args.layout, "impl": "ours",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -197,6 +197,33 @@ int nbody_neighbors_2d(const float *x, const float *y, int64_t n, float cutoff,
                        void *cuda_stream);
 
 /*
+ * Layouts of the velocity and acceleration arrays for the *_layout entry
+ * points ("CUDA N-Body Simulation" §3.5 compares float4 and float3 forms).
+ * Positions stay float4 rows (x, y, z, m) in every layout.
+ */
+typedef enum nbody_layout {
+    NBODY_ROWS4 = 0,   /* n rows of float4; accel.w = 0, vel.w kept; 16-byte aligned */
+    NBODY_ROWS3 = 1,   /* n rows of 3 floats (12 bytes); 4-byte aligned */
+    NBODY_BLOCKS3 = 2  /* x[0..n), then y[0..n), then z[0..n); 4-byte aligned */
+} nbody_layout;
+
+/*
+ * nbody_accel_on_stream writing accel in `layout` (12n bytes for the
+ * three-float layouts).  Same accelerations, bit for bit, as NBODY_ROWS4.
+ */
+int nbody_accel_layout(const float *pos_mass, float *accel, int64_t n,
+                       float eps2, int layout, void *cuda_stream);
+
+/*
+ * nbody_leapfrog_step_on_stream with vel and accel in `layout`.  Same
+ * results, bit for bit, as NBODY_ROWS4 (apart from the w column, which the
+ * three-float layouts do not have).
+ */
+int nbody_leapfrog_step_layout(float *pos_mass, float *vel, float *accel,
+                               int64_t n, float eps2, float dt, int steps,
+                               int layout, void *cuda_stream);
+
+/*
  * Wait for the stream, then report and clear the device-side status of
  * this device: NBODY_OK, NBODY_ETIMEOUT, or NBODY_ECUDA if the stream
  * reported a CUDA error.

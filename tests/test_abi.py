@@ -177,3 +177,17 @@ def test_neighbors_bad_arguments(L):
     assert neighbors(L, A, B, 10, 1.0, 4, A, D) == nb.EINVAL  # nn overlaps x
     assert neighbors(L, A, B, 10, 1.0, 4, C, C + 8) == nb.EINVAL  # nl overlaps nn
     assert neighbors(L, 0, 0, 0, 1.0, 4, 0, 0) == nb.OK
+
+
+def test_layout_entry_points_validate(L):
+    f = ctypes.c_float
+    assert L.nbody_accel_layout(ctypes.c_void_p(A), ctypes.c_void_p(B), 10, f(0.1), 3, S) == nb.EINVAL
+    assert L.nbody_accel_layout(ctypes.c_void_p(A), ctypes.c_void_p(B + 4), 10, f(0.1), 0, S) == nb.EINVAL
+    assert L.nbody_accel_layout(ctypes.c_void_p(A), ctypes.c_void_p(B + 2), 10, f(0.1), 1, S) == nb.EINVAL
+    # a three-float array of 10 rows is 120 bytes: it overlaps positions 16 bytes on
+    assert L.nbody_accel_layout(ctypes.c_void_p(A), ctypes.c_void_p(A + 16 * 9), 10, f(0.1), 1,
+                                S) == nb.EINVAL
+    assert L.nbody_leapfrog_step_layout(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(B + 100),
+                                        10, f(0.1), f(0.1), 1, 2, S) == nb.EINVAL  # vel/accel overlap
+    assert L.nbody_leapfrog_step_layout(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(C),
+                                        10, f(0.1), f(0.1), 1, -1, S) == nb.EINVAL

@@ -472,3 +472,39 @@ def test_neighbors_large_sampled():
     idx = W.sample_indices(p.n, 5)
     rn, rl = oracle.neighbors_2d(p.x, p.y, p.cutoff, p.max_neighbors, idx=idx)
     assert np.array_equal(nn[idx], rn) and np.array_equal(nl[:, idx], rl)
+
+
+# ---------------------------------------------------------------------------
+# velocity / acceleration layouts: same bits as the float4 rows
+# ---------------------------------------------------------------------------
+
+
+def _to_layout(v4, layout):
+    v = np.ascontiguousarray(v4[:, :3])
+    return v if layout == 1 else np.ascontiguousarray(v.T)
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+@pytest.mark.parametrize("n", [3000, 40000, 200000])  # warp, medium tiled, large tiled kernels
+def test_layouts_match_rows4(layout, n):
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = W.random_bodies(n, 40 + layout)
+    v = W.random_velocities(n, 40 + layout)
+    ref_a = gpu_accel(pm, 1e-3)
+    rp, rv, ra = gpu_leapfrog(pm, v, 1e-3, 1e-3, 3)
+    shape = (n, 4) if layout == 0 else ((n, 3) if layout == 1 else (3, n))
+    out = torch.empty(shape, device="cuda")
+    nb.accel_layout(torch.from_numpy(pm).cuda(), out, 1e-3, layout)
+    nb.sync()
+    want = ref_a if layout == 0 else _to_layout(ref_a, layout)
+    assert np.array_equal(out.cpu().numpy(), want)
+    tv = torch.from_numpy(v if layout == 0 else _to_layout(v, layout)).cuda()
+    ta = torch.empty_like(tv)
+    tp = torch.from_numpy(pm).cuda()
+    nb.leapfrog_step_layout(tp, tv, ta, 1e-3, 1e-3, 3, layout)
+    nb.sync()
+    assert np.array_equal(tp.cpu().numpy(), rp)
+    wantv = rv if layout == 0 else _to_layout(rv, layout)
+    wanta = ra if layout == 0 else _to_layout(ra, layout)
+    assert np.array_equal(tv.cpu().numpy(), wantv) and np.array_equal(ta.cpu().numpy(), wanta)
