@@ -25,7 +25,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per tile copy: only a f
 constexpr int kFinishThreads = 256;
 constexpr int kWarpKW = 8;
 constexpr int kWarpNW = 4;
-constexpr long long kWarpMaxN = 8192;  // AUTO uses the warp kernel up to this n
+// AUTO uses the warp kernel (one j slice: no second pass) up to this n, the
+// large tiled shape above it; both thresholds from a latency sweep over n.
+constexpr long long kWarpMaxN = 24576;
 
 using TiledKernel = void (*)(const TiledArgs, const Epilogue);
 
@@ -171,9 +173,8 @@ int current_device(int* dev) {
 int auto_tiled_config(long long n) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n >= 131072) return 20;  // fastest at 2^20 in a sweep of 52 shapes
-  if (n >= 16384) return 1;
-  return 2;
+  if (n > kWarpMaxN) return 20;  // fastest from 32768 up (and at 2^20 in a sweep of 52 shapes)
+  return 2;                      // forced TILED/SPLIT at small n: the smallest blocks
 }
 
 bool streamk_needs_second_pass(long long units, long long grid, long long ntiles) {
@@ -207,11 +208,10 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
   p->threads = kWarpNW * 32;
   p->block = kWarpKW;
   p->nblocks = ceil_div(n, kWarpKW);
-  long long s = split;
-  if (s <= 0) {
-    s = std::min(ceil_div(4LL * d.sms, p->nblocks), ceil_div(n, 256));
-    s = std::max(1LL, s);
-  }
+  // one slice by default: the single launch beats any split at every n the
+  // warp kernel is chosen for (measured); split > 0 forces S slices
+  long long s = split > 0 ? split : 1;
+  (void)d;
   s = std::min(s, std::min(n, 65535LL));
   p->slice_len = ceil_div(n, s);
   p->slices = static_cast<int>(ceil_div(n, p->slice_len));

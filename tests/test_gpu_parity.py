@@ -239,7 +239,7 @@ def test_allocation_failure_is_enomem(monkeypatch):
     import torch
     import all_pairs_body_gb300 as nb
     nb.release()
-    pm = torch.from_numpy(W.cube_sweep(20000).pos_mass).cuda()
+    pm = torch.from_numpy(W.cube_sweep(40000).pos_mass).cuda()  # tiled plan: needs scratch
     monkeypatch.setenv("NBODY_FAULT_ALLOC", "1")
     with pytest.raises(nb.NBodyError) as ei:
         nb.accel(pm, 1e-3)
