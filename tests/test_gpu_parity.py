@@ -508,3 +508,4 @@ def test_layouts_match_rows4(layout, n):
     wantv = rv if layout == 0 else _to_layout(rv, layout)
     wanta = ra if layout == 0 else _to_layout(ra, layout)
     assert np.array_equal(tv.cpu().numpy(), wantv) and np.array_equal(ta.cpu().numpy(), wanta)
+
