@@ -240,7 +240,8 @@ def oracle_sample_rate(pos_mass, eps2: float, seconds: float, seed: int):
     import oracle
     n = pos_mass.shape[0]
     rng = np.random.default_rng(seed)
-    probe = np.sort(rng.choice(n, size=min(64, n), replace=False))
+    # enough targets to keep every OpenMP thread busy while calibrating
+    probe = np.sort(rng.choice(n, size=min(16 * oracle.threads(), n), replace=False))
     t0 = time.perf_counter()
     oracle.accel(pos_mass, eps2, idx=probe)
     per_target = (time.perf_counter() - t0) / len(probe)
@@ -486,7 +487,7 @@ def run_reference(args):
     # size one step so warm-up + timed steps end within a few minutes
     per_step_s = min(8.0, 150.0 / max(1, args.steps + args.warmup))
     rng = np.random.default_rng(777)
-    probe = np.sort(rng.choice(n, size=min(32, n), replace=False))
+    probe = np.sort(rng.choice(n, size=min(16 * oracle.threads(), n), replace=False))
     t0 = time.perf_counter()
     oracle.accel(w.pos_mass, w.eps2, idx=probe)
     per_target = (time.perf_counter() - t0) / len(probe)

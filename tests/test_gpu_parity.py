@@ -509,3 +509,56 @@ def test_layouts_match_rows4(layout, n):
     wanta = ra if layout == 0 else _to_layout(ra, layout)
     assert np.array_equal(tv.cpu().numpy(), wantv) and np.array_equal(ta.cpu().numpy(), wanta)
 
+
+
+# ---------------------------------------------------------------------------
+# plain entry points (legacy default stream) and concurrent streams
+# ---------------------------------------------------------------------------
+
+
+def test_plain_entry_points_on_the_legacy_stream():
+    import ctypes
+    import torch
+    import all_pairs_body_gb300 as nb
+    L = nb.lib()
+    P = ctypes.c_void_p
+    w = W.cube_sweep(4097)
+    pm = torch.from_numpy(w.pos_mass).cuda()
+    out = torch.full_like(pm, float("nan"))
+    torch.cuda.synchronize()
+    assert L.nbody_accel(P(pm.data_ptr()), P(out.data_ptr()), w.n, ctypes.c_float(w.eps2)) == nb.OK
+    assert L.nbody_sync(P(0)) == nb.OK
+    assert rel_err(out.cpu().numpy(), oracle.accel(w.pos_mass, w.eps2)) <= ACC_TOL
+    v = torch.from_numpy(W.random_velocities(w.n, 9)).cuda()
+    a = torch.full_like(pm, float("nan"))
+    assert L.nbody_leapfrog_step(P(pm.data_ptr()), P(v.data_ptr()), P(a.data_ptr()), w.n,
+                                 ctypes.c_float(w.eps2), ctypes.c_float(1e-3), 2) == nb.OK
+    assert L.nbody_sync(P(0)) == nb.OK
+    rp, rv, ra = oracle.leapfrog(w.pos_mass, W.random_velocities(w.n, 9), w.eps2, 1e-3, 2)
+    assert rel_err(a.cpu().numpy(), ra) <= ACC_TOL and rel_err(pm.cpu().numpy(), rp) <= POS_TOL
+
+
+def test_concurrent_streams_use_separate_scratch():
+    """Two tiled multi-step calls in flight at once on two streams (each with
+    its own cached scratch) give the same bits as the same calls run alone."""
+    import torch
+    import all_pairs_body_gb300 as nb
+    inputs = [(W.random_bodies(40000, s), W.random_velocities(40000, s)) for s in (51, 52)]
+    alone = [gpu_leapfrog(pm, v, 1e-3, 1e-3, 3) for pm, v in inputs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    bufs = []
+    for (pm, v), st in zip(inputs, streams):
+        with torch.cuda.stream(st):
+            tp = torch.from_numpy(pm).to("cuda", non_blocking=False)
+            tv = torch.from_numpy(v).to("cuda", non_blocking=False)
+            ta = torch.empty_like(tp)
+            bufs.append((tp, tv, ta))
+    torch.cuda.synchronize()
+    for (tp, tv, ta), st in zip(bufs, streams):
+        with torch.cuda.stream(st):
+            nb.leapfrog_step(tp, tv, ta, 1e-3, 1e-3, 3)
+    for st in streams:
+        nb.sync(st)
+    for (tp, tv, ta), (rp, rv, ra) in zip(bufs, alone):
+        assert np.array_equal(tp.cpu().numpy(), rp) and np.array_equal(tv.cpu().numpy(), rv)
+        assert np.array_equal(ta.cpu().numpy(), ra)
