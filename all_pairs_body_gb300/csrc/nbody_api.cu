@@ -23,7 +23,7 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per tile copy: only a fault gets near it
 constexpr int kFinishThreads = 256;
-constexpr int kWarpKW = 8;
+constexpr int kWarpKW = 4;  // targets per CTA of the small-n kernel (sweep: 4 beats 6-16)
 constexpr int kWarpNW = 4;
 // AUTO uses the warp kernel (one j slice: no second pass) up to this n, the
 // large tiled shape above it; both thresholds from a latency sweep over n.
