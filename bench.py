@@ -63,6 +63,11 @@ def parse_args(argv=None):
                          "only; kdk: one kick-drift-kick step (two force passes); render: the "
                          "point-shader kernel (memory-bound, reported in GB/s); neighbors: the "
                          "2-D cutoff neighbour list (pair tests/s; default points2d-1048576)")
+    ap.add_argument("--path", choices=("auto", "tiled", "split", "warp"), default="auto",
+                    help="force-pass path for --mode step|accel|kdk (the library's choice by "
+                         "default); NBODY_TILED_CONFIG selects a row of the tiled-kernel table")
+    ap.add_argument("--split", type=int, default=0,
+                    help="j slices per target block for --path split|warp (0: library's choice)")
     ap.add_argument("--layout", choices=("rows4", "rows3", "blocks3"), default="rows4",
                     help="velocity/acceleration layout for --mode step|accel (float4 rows, "
                          "float3 rows, or x/y/z blocks)")
@@ -311,25 +316,34 @@ def run_ours(args):
     m_lo = float(w.pos_mass[:, 3].min())
     m_hi = max(float(w.pos_mass[:, 3].max()), m_lo * (1 + 1e-6) + 1e-30)
 
-    def step():
-        if layout and args.mode == "step":
-            nb.leapfrog_step_layout(pm, vel, acc, w.eps2, dt, 1, layout)
+    path = {"auto": nb.PATH_AUTO, "tiled": nb.PATH_TILED, "split": nb.PATH_SPLIT,
+            "warp": nb.PATH_WARP}[args.path]
+    if (path or args.split) and (layout or args.mode == "render"):
+        raise SystemExit("--path/--split apply to --mode step|accel|kdk with rows4")
+
+    def run_once(p_, v_, a_):
+        """One timed unit of work on the given device tensors."""
+        if args.mode == "render":
+            nb.render_points(p_, (1.0, 1.0, 1.0), m_lo, m_hi, ndc=ndc, rgba=rgba)
+        elif layout and args.mode == "step":
+            nb.leapfrog_step_layout(p_, v_, a_, w.eps2, dt, 1, layout)
         elif layout:
-            nb.accel_layout(pm, acc, w.eps2, layout)
+            nb.accel_layout(p_, a_, w.eps2, layout)
         elif args.mode == "step":
-            nb.leapfrog_step(pm, vel, acc, w.eps2, dt, 1)
+            nb.leapfrog_step(p_, v_, a_, w.eps2, dt, 1, path=path, split=args.split)
         elif args.mode == "kdk":
-            nb.leapfrog_kdk(pm, vel, acc, w.eps2, dt, 1)
-        elif args.mode == "render":
-            nb.render_points(pm, (1.0, 1.0, 1.0), m_lo, m_hi, ndc=ndc, rgba=rgba)
+            nb.leapfrog_kdk(p_, v_, a_, w.eps2, dt, 1, path=path, split=args.split)
         else:
-            nb.accel(pm, w.eps2, out=acc)
+            nb.accel(p_, w.eps2, out=a_, path=path, split=args.split)
+
+    def step():
+        run_once(pm, vel, acc)
 
     for _ in range(max(args.warmup, 0)):
         step()
     nb.sync()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    plan = nb.plan(n)
+    plan = nb.plan(n, path, args.split)
 
     sampler = ClockSampler(gpu_selector(local)).start()
     nb.profile_enable(True)
@@ -384,12 +398,7 @@ def run_ours(args):
         for _ in range(args.steps):
             d_pm.copy_(h_pm, non_blocking=True)
             d_v.copy_(h_v, non_blocking=True)
-            if args.mode == "step":
-                nb.leapfrog_step(d_pm, d_v, d_a, w.eps2, dt, 1)
-            elif args.mode == "kdk":
-                nb.leapfrog_kdk(d_pm, d_v, d_a, w.eps2, dt, 1)
-            else:
-                nb.accel(d_pm, w.eps2, out=d_a)
+            run_once(d_pm, d_v, d_a)
             o_pm.copy_(d_pm, non_blocking=True)
             o_v.copy_(d_v, non_blocking=True)
             o_a.copy_(d_a, non_blocking=True)
@@ -434,7 +443,7 @@ def run_ours(args):
         "data": "synthetic", "config": workload_config(w, args.mode, world),
         "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
-        "plan": plan, "layout": args.layout, "impl": "ours",
+        "plan": plan, "layout": args.layout, "path": args.path, "impl": "ours",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
