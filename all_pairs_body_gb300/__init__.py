@@ -136,7 +136,7 @@ def accel_noalloc(pos_mass, out, eps2: float, stream=None):
     """Accelerations into ``out`` without any allocation by the library.
 
     For callers that must not allocate device memory when they ask for
-    accelerations; the work memory is one fixed 8 MiB array per GPU that the
+    accelerations; the work memory is one fixed 6 MiB array per GPU that the
     library holds until exit.  n <= NOALLOC_MAX_N.  Calls must not overlap on
     the GPU (they share the array).  ``out`` must be allocated by the caller.
     """

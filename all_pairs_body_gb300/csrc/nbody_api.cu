@@ -61,6 +61,7 @@ const TiledConfig kTiled[] = {
     {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1, 2>},
     {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1, 2>},
     {10, 256, 256, 0, force_tiled<10, 256, 256, 1, 2, 0, 0>},
+    {10, 256, 512, 0, force_tiled<10, 256, 512, 1, 2, 0, 0>},
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
@@ -80,7 +81,6 @@ struct Plan {
   bool second_pass = false;
   int slices = 1;  // warp path
   long long slice_len = 0;
-  long long npad = 0;  // ntiles * tj
   int sms = 0;
 };
 
@@ -90,7 +90,7 @@ struct Buf {
 };
 
 struct Scratch {
-  Buf dup_a, dup_b, pos_alt, partial, tile_exact;
+  Buf pos_alt, partial;
 };
 
 std::mutex g_mu;
@@ -173,7 +173,7 @@ int current_device(int* dev) {
 int auto_tiled_config(long long n) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n > kWarpMaxN) return 20;  // fastest from 32768 up (and at 2^20 in a sweep of 52 shapes)
+  if (n > kWarpMaxN) return 21;  // fastest from 32768 up (shape searches at 2^20)
   return 2;                      // forced TILED/SPLIT at small n: the smallest blocks
 }
 
@@ -190,7 +190,6 @@ void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) 
   p->block = static_cast<long long>(tc.ki) * tc.nt;
   p->tj = tc.tj;
   p->ntiles = ceil_div(n, tc.tj);
-  p->npad = p->ntiles * tc.tj;
   p->nblocks = ceil_div(n, p->block);
   p->units = p->nblocks * p->ntiles;
   if (path == NBODY_PATH_TILED) {
@@ -235,10 +234,7 @@ int make_plan(long long n, int path, int split, int dev, Plan* p) {
   return NBODY_OK;
 }
 
-int launches_accel(const Plan& p) {
-  if (p.path == NBODY_PATH_WARP) return 1 + (p.second_pass ? 1 : 0);
-  return 2 + (p.second_pass ? 1 : 0);
-}
+int launches_accel(const Plan& p) { return 1 + (p.second_pass ? 1 : 0); }
 
 int launches_step1(const Plan& p) { return launches_accel(p); }
 
@@ -273,13 +269,8 @@ int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapf
   Scratch& s = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
   int rc = NBODY_OK;
   if (p.path != NBODY_PATH_WARP) {
-    const size_t dup_bytes = static_cast<size_t>(p.npad) * 2 * sizeof(float4);
-    if (rc == NBODY_OK) rc = ensure(s.dup_a, dup_bytes, st);
-    if (rc == NBODY_OK && leapfrog) rc = ensure(s.dup_b, dup_bytes, st);
-    if (rc == NBODY_OK && p.second_pass)
+    if (p.second_pass)
       rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
-    if (rc == NBODY_OK && kTiled[p.cfg].form == 1)
-      rc = ensure(s.tile_exact, static_cast<size_t>(p.ntiles) * sizeof(int), st);
   } else if (p.second_pass) {
     rc = ensure(s.partial, static_cast<size_t>(p.slices) * n * sizeof(float4), st);
   }
@@ -332,16 +323,13 @@ int launch_status() {
 // launch sequences
 // --------------------------------------------------------------------------
 
-Epilogue make_epilogue(const float4* pos, void* accel, void* vel, float4* pos_next,
-                       float4* dup_next, const float4* dup, float kick, float dt, int layout,
-                       long long n) {
+Epilogue make_epilogue(const float4* pos, void* accel, void* vel, float4* pos_next, float kick,
+                       float dt, int layout, long long n) {
   Epilogue e;
   e.pos = pos;
   e.accel = static_cast<float*>(accel);
   e.vel = static_cast<float*>(vel);
   e.pos_next = pos_next;
-  e.dup_next = dup_next;
-  e.dup = dup;
   e.kick = kick;
   e.dt = dt;
   e.layout = layout;
@@ -359,23 +347,10 @@ bool vec_aligned(const void* p, int layout) {
   return layout == kRows4 ? (a & 15u) == 0 : (a & 3u) == 0;
 }
 
-void launch_expand(const Plan& p, const float4* pos, float4* dup, float4* dup2, int* tile_exact,
-                   long long n, cudaStream_t st) {
-  count_launches(1);
-  if (kTiled[p.cfg].form == 1) {  // one CTA per source tile
-    expand_sources<1><<<static_cast<unsigned>(p.ntiles), p.tj, 0, st>>>(
-        pos, dup, dup2, tile_exact, static_cast<int>(n), p.npad);
-  } else {
-    const long long blocks = ceil_div(p.npad, kFinishThreads);
-    expand_sources<0><<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(
-        pos, dup, dup2, nullptr, static_cast<int>(n), p.npad);
-  }
-}
-
-// One force pass (plus its second pass): sources and targets `pos`
-// (expanded copy `dup` for the tiled kernel), finished through `epi`.
-void launch_force(const Plan& p, const float4* pos, const float4* dup, const int* tile_exact,
-                  long long n, float eps2, float4* partial, const Epilogue& epi, cudaStream_t st) {
+// One force pass (plus its second pass): sources and targets `pos`, finished
+// through `epi`.
+void launch_force(const Plan& p, const float4* pos, long long n, float eps2, float4* partial,
+                  const Epilogue& epi, cudaStream_t st) {
   if (p.path == NBODY_PATH_WARP) {
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
@@ -391,8 +366,7 @@ void launch_force(const Plan& p, const float4* pos, const float4* dup, const int
     }
     return;
   }
-  TiledArgs a{pos,   dup,     static_cast<int>(n), eps2,         p.ntiles, p.units,
-              p.grid, partial, tile_exact,          kWaitLimitNs, -1};
+  TiledArgs a{pos, static_cast<int>(n), eps2, p.ntiles, p.units, p.grid, partial, kWaitLimitNs, -1};
   cudaEvent_t e0 = prof_event(st);
   kTiled[p.cfg].kernel<<<static_cast<unsigned>(p.grid), p.threads, 0, st>>>(a, epi);
   cudaEvent_t e1 = prof_event(st);
@@ -426,12 +400,8 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
   if ((rc = get_scratch(dev, st, p, n, false, &s)) != NBODY_OK) return rc;
 
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
-  float4* dup = static_cast<float4*>(s->dup_a.p);
-  int* flags = static_cast<int*>(s->tile_exact.p);
-  const Epilogue epi =
-      make_epilogue(pos, accel, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, layout, n);
-  if (p.path != NBODY_PATH_WARP) launch_expand(p, pos, dup, nullptr, flags, n, st);
-  launch_force(p, pos, dup, flags, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+  const Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, layout, n);
+  launch_force(p, pos, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
   return launch_status();
 }
 
@@ -482,26 +452,16 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
     cur = alt;
     nxt = user;
   }
-  const bool tiled = p.path != NBODY_PATH_WARP;
-  float4* dup_cur = static_cast<float4*>(s->dup_a.p);
-  float4* dup_nxt = static_cast<float4*>(s->dup_b.p);
-  int* flags = static_cast<int*>(s->tile_exact.p);
   float4* partial = static_cast<float4*>(s->partial.p);
-  if (tiled) launch_expand(p, cur, dup_cur, dup_nxt, flags, n, st);
   for (int k = 0; k < steps; ++k) {
-    // the expanded next positions are needed by a following force pass only
-    const bool chain = tiled && (kdk || k + 1 < steps);
     const float kick = (kdk && k > 0) ? dt : 0.5f * dt;
-    const Epilogue epi = make_epilogue(cur, accel, vel, nxt, chain ? dup_nxt : nullptr,
-                                       chain ? dup_cur : nullptr, kick, dt, layout, n);
-    launch_force(p, cur, dup_cur, flags, n, eps2, partial, epi, st);
+    const Epilogue epi = make_epilogue(cur, accel, vel, nxt, kick, dt, layout, n);
+    launch_force(p, cur, n, eps2, partial, epi, st);
     std::swap(cur, nxt);
-    std::swap(dup_cur, dup_nxt);
   }
   if (kdk) {
-    const Epilogue last = make_epilogue(cur, accel, vel, nullptr, nullptr, nullptr, 0.5f * dt, dt,
-                                        layout, n);
-    launch_force(p, cur, dup_cur, flags, n, eps2, partial, last, st);
+    const Epilogue last = make_epilogue(cur, accel, vel, nullptr, 0.5f * dt, dt, layout, n);
+    launch_force(p, cur, n, eps2, partial, last, st);
   }
   return launch_status();
 }
@@ -594,9 +554,7 @@ namespace {
 // force_tiled<4, 128, 128, 2, 4, 0, 0>: 512 targets per i-block, 128-source tiles.
 constexpr int kNoAllocCfg = 1;
 constexpr long long kNoAllocMaxGrid = 384;
-constexpr long long kNoAllocDupRows = 2LL * NBODY_NOALLOC_MAX_N;  // 128 divides 65536
-constexpr long long kNoAllocPartialRows = kNoAllocMaxGrid * 2 * 512;
-constexpr long long kNoAllocRows = kNoAllocDupRows + kNoAllocPartialRows;  // 8 MiB of float4
+constexpr long long kNoAllocRows = kNoAllocMaxGrid * 2 * 512;  // partial sums: 6 MiB of float4
 constexpr int kNoAllocMaxDevices = 64;
 
 struct NoAllocDevice {
@@ -609,7 +567,7 @@ NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];  // fixed table: no allocation
 }  // namespace
 }  // namespace nbody
 
-// Working memory of nbody_accel_noalloc: expanded sources, then partial sums.
+// Working memory of nbody_accel_noalloc: the partial sums of split i-blocks.
 static __device__ __align__(256) float4 g_noalloc_scratch[nbody::kNoAllocRows];
 
 namespace nbody {
@@ -663,7 +621,6 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   const TiledConfig& tc = kTiled[kNoAllocCfg];
   const long long block = static_cast<long long>(tc.ki) * tc.nt;
   const long long ntiles = ceil_div(n, tc.tj);
-  const long long npad = ntiles * tc.tj;
   const long long units = ceil_div(n, block) * ntiles;
   // whole CTAs per SM so that every SM gets the same share, within the array
   const long long per_sm = std::max(1LL, std::min<long long>(d.occupancy, kNoAllocMaxGrid / d.sms));
@@ -671,14 +628,9 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   const bool second = streamk_needs_second_pass(units, grid, ntiles);
 
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
-  float4* dup = d.scratch;
-  float4* partial = d.scratch + kNoAllocDupRows;
-  const Epilogue epi =
-      make_epilogue(pos, accel, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, kRows4, n);
-  // rewrites every expanded row the force kernel reads, zero padding included
-  expand_sources<0><<<static_cast<unsigned>(ceil_div(npad, kFinishThreads)), kFinishThreads, 0, st>>>(
-      pos, dup, nullptr, nullptr, static_cast<int>(n), npad);
-  TiledArgs a{pos, dup, static_cast<int>(n), eps2, ntiles, units, grid, partial, nullptr, kWaitLimitNs, -1};
+  float4* partial = d.scratch;  // every slot a call reads, the same call writes first
+  const Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, kRows4, n);
+  TiledArgs a{pos, static_cast<int>(n), eps2, ntiles, units, grid, partial, kWaitLimitNs, -1};
   tc.kernel<<<static_cast<unsigned>(grid), tc.nt, 0, st>>>(a, epi);
   if (second) {
     StreamkFinishArgs f{partial, static_cast<int>(n), block, ntiles, units, grid};
@@ -858,8 +810,7 @@ void nbody_release(void) {
       continue;
     }
     cudaDeviceSynchronize();
-    for (nbody::Buf* b : {&kv.second.dup_a, &kv.second.dup_b, &kv.second.pos_alt, &kv.second.partial,
-                          &kv.second.tile_exact}) {
+    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial}) {
       if (b->p != nullptr) cudaFree(b->p);
       b->p = nullptr;
       b->bytes = 0;
@@ -878,27 +829,23 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   const TiledConfig& tc = kTiled[kCfg];
   const long long n = static_cast<long long>(tc.ki) * tc.nt;  // one i-block
   const long long ntiles = ceil_div(n, tc.tj);
-  float4 *pos = nullptr, *dup = nullptr, *acc = nullptr;
-  const size_t pb = n * sizeof(float4), db = 2 * ntiles * tc.tj * sizeof(float4);
-  if (cudaMalloc(&pos, pb) != cudaSuccess || cudaMalloc(&dup, db) != cudaSuccess ||
-      cudaMalloc(&acc, pb) != cudaSuccess) {
+  float4 *pos = nullptr, *acc = nullptr;
+  const size_t pb = n * sizeof(float4);
+  if (cudaMalloc(&pos, pb) != cudaSuccess || cudaMalloc(&acc, pb) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(pos);
-    cudaFree(dup);
     cudaFree(acc);
     return NBODY_ENOMEM;
   }
   cudaMemsetAsync(pos, 0, pb, st);
-  cudaMemsetAsync(dup, 0, db, st);
-  TiledArgs a{pos, dup, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr, nullptr,
+  TiledArgs a{pos, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr,
               static_cast<uint64_t>(timeout_ms) * 1000000ull, 0};
-  const Epilogue epi = make_epilogue(pos, acc, nullptr, nullptr, nullptr, nullptr, 0.f, 0.f, kRows4, n);
+  const Epilogue epi = make_epilogue(pos, acc, nullptr, nullptr, 0.f, 0.f, kRows4, n);
   tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
   int rc = launch_status();
   const int srv = nbody_sync(cuda_stream);
   if (rc == NBODY_OK) rc = srv;
   cudaFree(pos);
-  cudaFree(dup);
   cudaFree(acc);
   return rc;
 }

@@ -5,15 +5,15 @@
 // half-kick + drift of §1.3 into the pass that completes each a_i.
 //
 // Kernels
-//   expand_sources      float4 (x,y,z,m) rows -> two rows (x,x,y,y),(z,z,m,m)
-//                       per body, zero-padded to whole tiles, so each source
-//                       component arrives as an already duplicated FP32 pair.
 //   force_tiled<KI,NT,TJ,MINB,UNR,FORM,NLOG>
 //                       KI target bodies per thread in registers (KI/2 packed
-//                       FP32 pairs), source tiles of TJ bodies staged in
-//                       shared memory by 1-D TMA bulk copies on a two-stage
-//                       mbarrier pipeline, packed FFMA2/FADD2/FMUL2 + MUFU.RSQ
-//                       inner loop.  Work = (i-block, j-tile) units divided
+//                       FP32 pairs); source tiles of TJ bodies brought into a
+//                       two-stage shared-memory ring by 1-D TMA bulk copies of
+//                       the caller's float4 rows (mbarrier completion), then
+//                       expanded by the CTA into two rows (x,x,y,y),(z,z,w0,w1)
+//                       per body so each source component is an already
+//                       duplicated FP32 pair; packed FFMA2/FADD2/FMUL2 +
+//                       MUFU.RSQ inner loop.  Work = (i-block, j-tile) units divided
 //                       evenly over the grid; a CTA that covers an i-block's
 //                       whole j range finishes it (accel or kick/drift), else
 //                       it writes a partial sum for the second pass.
@@ -212,8 +212,6 @@ struct Epilogue {
   float* accel;       // out: accelerations in `layout`
   float* vel;         // step only (nullptr: acceleration only), in `layout`
   float4* pos_next;   // step with a drift: end-of-step positions (nullptr: kick only)
-  float4* dup_next;   // optional: expanded end-of-step sources
-  const float4* dup;  // with dup_next: the current expanded sources (mass encoding)
   float kick;         // velocity kick coefficient on a (dt/2 for a half kick)
   float dt;           // drift coefficient on v
   int layout;         // VecLayout of accel and vel
@@ -264,51 +262,33 @@ __device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax
     x.y = fmaf(e.dt, v.y, x.y);
     x.z = fmaf(e.dt, v.z, x.z);
     e.pos_next[i] = x;
-    if (e.dup_next != nullptr) {  // masses do not move: keep this body's mass encoding
-      const float4 enc = e.dup[2 * i + 1];
-      e.dup_next[2 * i] = make_float4(x.x, x.x, x.y, x.y);
-      e.dup_next[2 * i + 1] = make_float4(x.z, x.z, enc.z, enc.w);
-    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// source expansion
+// source tile expansion
 // ---------------------------------------------------------------------------
 
-// dup[2i] = (x,x,y,y), dup[2i+1] = (z,z,w0,w1) for i < npad, where (w0, w1)
-// encode the mass m (zero rows for the padding n <= i < npad, which add
-// exactly nothing):
-//   FORM 0: (m, m).
-//   FORM 1: (m, log2 m), log2 0 = -inf, for the mixed inner loop; one CTA
-//           per source tile (blockDim.x == tile width), and a tile holding
-//           any negative or NaN mass sets tile_exact[tile] = 1 so the force
-//           kernel runs the rsqrt form on all of it.
-// dup2, when given, receives the same padding rows (the other buffer of a
-// multi-step call, whose real rows the step epilogue writes).
-template <int FORM>
-__global__ void expand_sources(const float4* __restrict__ pos, float4* __restrict__ dup,
-                               float4* __restrict__ dup2, int* __restrict__ tile_exact, int n,
-                               long long npad) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const bool live = i < n;
-  const float4 x = live ? pos[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float w1 = x.w;
-  if (FORM == 1) {
-    const bool odd_mass = live && !(x.w >= 0.0f);  // negative or NaN
-    const bool exact = __syncthreads_or(odd_mass) != 0;
-    if (threadIdx.x == 0) tile_exact[blockIdx.x] = exact ? 1 : 0;
-    w1 = x.w > 0.0f ? log2f(x.w) : (x.w == 0.0f ? -INFINITY : x.w);
+// tile[2b] = (x,x,y,y), tile[2b+1] = (z,z,m,w1) for the staged rows b < tj of
+// one tile, zero rows past `live` (zero mass adds exactly nothing); w1 = m
+// for form 0, log2 m (-inf for m = 0) for form 1.  Returns whether any live
+// mass is negative or NaN.  Out of line: it runs once per tile and, inlined,
+// perturbs the register allocation of the inner loop.
+__device__ __noinline__ bool expand_tile(const float4* raw, float4* tile, int tj, int nt, int tid,
+                                         long long live, int form) {
+  bool odd = false;
+  for (int b = tid; b < tj; b += nt) {
+    const bool ok = b < live;
+    const float4 x = ok ? raw[b] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float w1 = x.w;
+    if (form == 1) {
+      odd |= ok && !(x.w >= 0.0f);
+      w1 = x.w > 0.0f ? log2f(x.w) : (x.w == 0.0f ? -INFINITY : x.w);
+    }
+    tile[2 * b] = make_float4(x.x, x.x, x.y, x.y);
+    tile[2 * b + 1] = make_float4(x.z, x.z, x.w, w1);
   }
-  if (i >= npad) return;
-  const float4 r0 = make_float4(x.x, x.x, x.y, x.y);
-  const float4 r1 = make_float4(x.z, x.z, x.w, w1);
-  dup[2 * i] = r0;
-  dup[2 * i + 1] = r1;
-  if (!live && dup2 != nullptr) {
-    dup2[2 * i] = r0;
-    dup2[2 * i + 1] = r1;
-  }
+  return odd;
 }
 
 // ---------------------------------------------------------------------------
@@ -316,15 +296,13 @@ __global__ void expand_sources(const float4* __restrict__ pos, float4* __restric
 // ---------------------------------------------------------------------------
 
 struct TiledArgs {
-  const float4* pos;  // n target rows (x, y, z, m)
-  const float4* dup;  // 2 * ntiles * TJ expanded source rows
+  const float4* pos;  // n rows (x, y, z, m): the targets and the sources
   int n;
   float eps2;
   long long ntiles;  // source tiles over n
   long long units;   // i-blocks * ntiles
   long long grid;    // CTAs launched
   float4* partial;   // [grid][2][KI*NT] partial sums of split i-blocks
-  const int* tile_exact;  // FORM 1: per source tile, 1 = rsqrt form for all pairs
   uint64_t timeout_ns;
   long long withhold;  // failure-detection check only: this unit's copy is never issued (-1: none)
 };
@@ -346,9 +324,9 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KI / 2;
   constexpr long long B = static_cast<long long>(KI) * NT;
-  constexpr uint32_t kTileBytes = TJ * 32u;
 
-  __shared__ __align__(128) float4 tile[2][2 * TJ];
+  __shared__ __align__(128) float4 raw[2][TJ];  // TMA targets: the caller's rows
+  __shared__ __align__(128) float4 tile[2 * TJ];  // expanded: (x,x,y,y),(z,z,w0,w1)
   __shared__ __align__(8) unsigned long long bar[2];
 
   const int tid = threadIdx.x;
@@ -357,10 +335,10 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
   const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
   // shared-memory addresses of stage s: base + s * stride
   const uint32_t bar0 = smem_u32(&bar[0]);
-  const uint32_t tile0 = smem_u32(&tile[0][0]);
-  constexpr uint32_t kTileStride = sizeof(tile[0]);
+  const uint32_t raw0 = smem_u32(&raw[0][0]);
+  constexpr uint32_t kRawStride = sizeof(raw[0]);
   auto bar_of = [&](long long k) { return bar0 + static_cast<uint32_t>(k & 1) * 8u; };
-  auto tile_of = [&](long long k) { return tile0 + static_cast<uint32_t>(k & 1) * kTileStride; };
+  auto raw_of = [&](long long k) { return raw0 + static_cast<uint32_t>(k & 1) * kRawStride; };
 
   if (tid == 0) {
     mbar_init(bar0, 1);
@@ -370,11 +348,14 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
   __syncthreads();
   if (count <= 0) return;
 
-  // Copy the source tile of local unit k into stage k & 1.
+  // Copy the source rows of local unit k's tile into stage k & 1 (only the
+  // rows that exist: the last tile may be short; 16 bytes per row keeps
+  // every address and size a multiple of 16).
   auto issue = [&](long long k) {
-    const long long t = (u_lo + k) % a.ntiles;
-    mbar_arrive_expect_tx(bar_of(k), kTileBytes);
-    bulk_copy_g2s(tile_of(k), a.dup + 2 * t * TJ, kTileBytes, bar_of(k));
+    const long long j0 = ((u_lo + k) % a.ntiles) * TJ;
+    const uint32_t bytes = static_cast<uint32_t>(min(static_cast<long long>(TJ), a.n - j0)) * 16u;
+    mbar_arrive_expect_tx(bar_of(k), bytes);
+    bulk_copy_g2s(raw_of(k), a.pos + j0, bytes, bar_of(k));
   };
   if (tid == 0 && a.withhold != 0) issue(0);
 
@@ -408,20 +389,33 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
       const bool ok = mbar_wait_bounded(bar_of(k), parity, a.timeout_ns);
       // Every thread reaches this barrier in bounded time; it makes the
       // timeout decision uniform and guarantees that all threads are done
-      // with stage s^1 (read in the previous iteration) before it is refilled.
+      // with the expanded tile (read in the previous iteration) and with
+      // stage s^1 of the ring (expanded in the previous iteration) before
+      // either is rewritten.
       if (!__syncthreads_and(ok)) {
         timed_out = true;
         break;
       }
       if (tid == 0 && k + 1 < count && k + 1 != a.withhold) issue(k + 1);
 
+      // Expand the tile: rows past n become zero-mass rows, which add exactly
+      // nothing.  FORM 1 stores log2 m beside m and runs the whole tile in
+      // the rsqrt form when any of its masses is negative or NaN.
+      const bool odd_mass =
+          expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, FORM);
+      bool exact = false;
+      if (FORM == 1)
+        exact = __syncthreads_or(odd_mass) != 0;
+      else
+        __syncthreads();
+
       // Per-tile sums, folded into the running sums after the tile: the
       // rounding error grows like sqrt(TJ) + sqrt(n / TJ), not sqrt(n).
       float2 tx[P], ty[P], tz[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
-      const float4* src = tile[s];
-      if (FORM == 1 && a.tile_exact[t] == 0) {
+      const float4* src = tile;
+      if (FORM == 1 && !exact) {
         // mixed form: the first NLOG target pairs take the logarithmic form
 #pragma unroll UNR
         for (int j = 0; j < TJ; ++j) {

@@ -28,10 +28,9 @@
  * Pointers are DEVICE pointers on the calling thread's current CUDA device
  * (cudaMalloc / cudaMallocAsync / managed memory); host pointers are
  * rejected with NBODY_EINVAL.  The caller owns every array it passes.  The
- * library owns only its cached scratch (an expanded copy of the sources,
- * the ping-pong positions of a multi-step call and the split-j partial
- * sums), allocated on first use per (device, stream) and freed by
- * nbody_release().
+ * library owns only its cached scratch (the ping-pong positions of a
+ * multi-step call and the split-j partial sums), allocated on first use per
+ * (device, stream) and freed by nbody_release().
  *
  * Execution is asynchronous: a call validates its arguments, enqueues its
  * kernels on the stream and returns.  NBODY_OK means "enqueued"; a device
@@ -246,9 +245,9 @@ int nbody_sync(void *cuda_stream);
  * allocations, and real-time or certified loops that ban allocation after
  * start-up because cudaMalloc may block or synchronise.  This call computes
  * the same accelerations as nbody_accel_on_stream, with the same argument
- * rules, but keeps its working memory (the expanded source tiles and the
- * split-j partial sums) in one fixed array that the library holds on every
- * GPU that loads it, until the process exits: 8 MiB of device memory.  It
+ * rules, but keeps its working memory (the split-j partial sums) in one
+ * fixed array that the library holds on every GPU that loads it, until the
+ * process exits: 6 MiB of device memory.  It
  * calls no allocation routine of CUDA, PyTorch or the C/C++ runtime.
  *
  *   n must be <= NBODY_NOALLOC_MAX_N; larger n returns NBODY_EINVAL and
@@ -257,8 +256,8 @@ int nbody_sync(void *cuda_stream);
  * The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress) with the device current; make that first call
  * before any stream capture.  All calls on a device share the one array,
- * which keeps whatever the last call left in it; every call rewrites the
- * parts it reads, including the zero padding of the last source tile.
+ * which keeps whatever the last call left in it; every call writes each
+ * slot it reads before reading it, so nothing needs clearing.
  * Two calls whose kernels overlap on the same GPU (for example on two
  * streams without ordering between them) race on the array and give wrong
  * results; order them (same stream, or an event).

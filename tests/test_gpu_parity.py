@@ -265,7 +265,7 @@ def test_bounded_wait_times_out_and_context_survives():
 # every kernel variant of the tuning table, and the logarithmic inner loop
 # ---------------------------------------------------------------------------
 
-N_TILED_VARIANTS = 21
+N_TILED_VARIANTS = 22
 
 
 @pytest.mark.parametrize("cfg", range(N_TILED_VARIANTS))
