@@ -170,11 +170,47 @@ int current_device(int* dev) {
 // launch plans
 // --------------------------------------------------------------------------
 
-int auto_tiled_config(long long n) {
+// The large-n shapes the stream-K plan chooses between, with their speed per
+// interaction relative to the first, measured at n = 2^20 (force kernel 379.2
+// against 389.8 ms).  The 512-source tiles are faster per interaction; the
+// 256-source tiles cut the work into twice as many units, which wins when a
+// CTA's share of units is small and its rounding up costs more.
+struct LargeShape {
+  int cfg;
+  double speed;
+};
+constexpr LargeShape kLargeShapes[] = {{21, 1.0}, {20, 0.973}};
+
+long long streamk_grid(long long units, const DeviceInfo& d, int cfg) {
+  const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.occupancy[cfg]);
+  return std::min(units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+}
+
+// Time model of a stream-K launch: the slowest CTA runs ceil(units / grid)
+// units of tj sources each, at the shape's speed.  It matched the measured
+// order of the two shapes at every n from 24577 to 131072.
+int choose_large_shape(long long n, const DeviceInfo& d) {
+  int best = -1;
+  double best_cost = 0.0;
+  for (const LargeShape& s : kLargeShapes) {
+    const TiledConfig& tc = kTiled[s.cfg];
+    const long long units =
+        ceil_div(n, static_cast<long long>(tc.ki) * tc.nt) * ceil_div(n, tc.tj);
+    const long long grid = streamk_grid(units, d, s.cfg);
+    const double cost = static_cast<double>(ceil_div(units, grid)) * tc.tj / s.speed;
+    if (best < 0 || cost < best_cost) {  // ties keep the earlier (faster) shape
+      best = s.cfg;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+int auto_tiled_config(long long n, bool streamk, const DeviceInfo& d) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n > kWarpMaxN) return 21;  // fastest from 32768 up (shape searches at 2^20)
-  return 2;                      // forced TILED/SPLIT at small n: the smallest blocks
+  if (n <= kWarpMaxN) return 2;  // forced TILED/SPLIT at small n: the smallest blocks
+  return streamk ? choose_large_shape(n, d) : kLargeShapes[0].cfg;
 }
 
 bool streamk_needs_second_pass(long long units, long long grid, long long ntiles) {
@@ -184,7 +220,8 @@ bool streamk_needs_second_pass(long long units, long long grid, long long ntiles
 }
 
 void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) {
-  p->cfg = auto_tiled_config(n);
+  const bool streamk = !(path == NBODY_PATH_TILED || (path == NBODY_PATH_SPLIT && split > 0));
+  p->cfg = auto_tiled_config(n, streamk, d);
   const TiledConfig& tc = kTiled[p->cfg];
   p->threads = tc.nt;
   p->block = static_cast<long long>(tc.ki) * tc.nt;
@@ -197,8 +234,7 @@ void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) 
   } else if (path == NBODY_PATH_SPLIT && split > 0) {
     p->grid = std::min(p->units, p->nblocks * static_cast<long long>(split));
   } else {  // one full wave of CTAs, work divided evenly (stream-K)
-    const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.occupancy[p->cfg]);
-    p->grid = std::min(p->units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+    p->grid = streamk_grid(p->units, d, p->cfg);
   }
   p->second_pass = streamk_needs_second_pass(p->units, p->grid, p->ntiles);
 }

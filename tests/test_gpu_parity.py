@@ -211,6 +211,28 @@ def test_plan_is_consistent():
     assert p["second_pass"] == 0 and p["grid"] * p["bodies_per_cta"] >= 1048576
 
 
+def test_plan_shape_follows_streamk_model():
+    """Above the warp kernel the plan takes the 512- or the 256-source shape,
+    whichever gives the slowest CTA less work: ceil(units / grid) tiles of tj
+    sources at the shape's relative speed (1 and 0.973)."""
+    import all_pairs_body_gb300 as nb
+    shapes = ((512, 1.0), (256, 0.973))
+    for n in list(range(24577, 140000, 4099)) + [262144, 500000, 1048576, 4194304]:
+        p = nb.plan(n)
+        assert p["bodies_per_cta"] == 2560
+        cost = []
+        for tj, speed in shapes:
+            units = -(-n // 2560) * -(-n // tj)
+            grid = min(units, p["sms"])
+            cost.append(-(-units // grid) * tj / speed)
+        want = shapes[0][0] if cost[0] <= cost[1] else shapes[1][0]
+        assert p["tile"] == want, (n, cost, p)
+        assert p["grid"] == min(p["units"], p["sms"])
+    if nb.plan(32768)["sms"] == 152:  # the measured cases on a 152-SM GPU
+        assert [nb.plan(n)["tile"] for n in (32768, 49152, 65537, 81920, 1048576)] == \
+            [256, 512, 256, 512, 512]
+
+
 # ---------------------------------------------------------------------------
 # errors seen from the GPU side
 # ---------------------------------------------------------------------------
