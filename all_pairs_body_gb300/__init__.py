@@ -21,7 +21,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libnbody_gb300.so")
 
-PATH_AUTO, PATH_TILED, PATH_SPLIT, PATH_WARP = 0, 1, 2, 3
+PATH_AUTO, PATH_TILED, PATH_SPLIT, PATH_WARP, PATH_PAIRS = 0, 1, 2, 3, 4
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
 PLAN_FIELDS = ("path", "grid", "threads", "bodies_per_cta", "tile", "tiles", "units",
                "second_pass", "launches_accel", "launches_step", "sms")

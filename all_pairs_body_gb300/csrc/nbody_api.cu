@@ -65,9 +65,34 @@ const TiledConfig kTiled[] = {
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
 
+using PairKernel = void (*)(const PairArgs);
+
+struct PairConfig {
+  int ki, nt, tj;
+  PairKernel kernel;
+  size_t smem() const { return pair_reduce_smem(nt, tj); }  // dynamic shared memory
+};
+
+// Shapes of the pair-symmetric kernel (targets per thread, threads, tile);
+// the first is the default.
+const PairConfig kPairs[] = {
+    {10, 256, 512, force_pairs<10, 256, 512>},
+    {8, 256, 256, force_pairs<8, 256, 256>},
+    {10, 256, 256, force_pairs<10, 256, 256>},
+    {8, 256, 512, force_pairs<8, 256, 512>},
+    {8, 256, 128, force_pairs<8, 256, 128>},
+};
+constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
+
+// The automatic plan takes the pair path while its reaction partials stay
+// within this many bytes (units * tile * 16: about N^2 / 320 at the default
+// shape, 3.4 GB at N = 2^20); NBODY_PAIRS_MAX_BYTES overrides it.
+constexpr long long kPairsMaxBytes = 16LL << 30;
+
 struct DeviceInfo {
   int sms = 0;
   int occupancy[kNumTiled] = {};
+  int pair_occupancy[kNumPairs] = {};
 };
 
 struct Plan {
@@ -91,6 +116,7 @@ struct Buf {
 
 struct Scratch {
   Buf pos_alt, partial;
+  Buf act, react;  // pair path: whole-block action sums, per-unit reaction sums
 };
 
 std::mutex g_mu;
@@ -151,6 +177,18 @@ int device_info(int dev, DeviceInfo* out) {
         return NBODY_ECUDA;
       }
       d.occupancy[c] = occ > 0 ? occ : 1;
+    }
+    for (int c = 0; c < kNumPairs; ++c) {
+      int occ = 0;
+      const int smem = static_cast<int>(kPairs[c].smem());
+      if (cudaFuncSetAttribute(kPairs[c].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kPairs[c].kernel, kPairs[c].nt,
+                                                        smem) != cudaSuccess) {
+        cudaGetLastError();
+        return NBODY_ECUDA;
+      }
+      d.pair_occupancy[c] = occ > 0 ? occ : 1;
     }
     it = g_devices.emplace(dev, d).first;
   }
@@ -254,6 +292,42 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
   p->second_pass = p->slices > 1;
 }
 
+int pair_config() {
+  const long long forced = env_int("NBODY_PAIRS_CONFIG", -1);
+  return forced >= 0 && forced < kNumPairs ? static_cast<int>(forced) : 0;
+}
+
+void plan_pairs(long long n, const DeviceInfo& d, Plan* p) {
+  p->cfg = pair_config();
+  const PairConfig& pc = kPairs[p->cfg];
+  p->threads = pc.nt;
+  p->block = static_cast<long long>(pc.ki) * pc.nt;
+  p->tj = pc.tj;
+  p->ntiles = ceil_div(n, pc.tj);
+  p->nblocks = ceil_div(n, p->block);
+  p->units = pair_units_before(p->nblocks, p->ntiles, p->block / pc.tj);
+  const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.pair_occupancy[p->cfg]);
+  p->grid = std::min(p->units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+  p->second_pass = true;  // reactions always come from other CTAs
+}
+
+// Reaction-partial bytes of the pair path's plan over n bodies.
+long long pair_react_bytes(long long n) {
+  const PairConfig& pc = kPairs[pair_config()];
+  const long long block = static_cast<long long>(pc.ki) * pc.nt;
+  const long long ntiles = ceil_div(n, pc.tj);
+  return pair_units_before(ceil_div(n, block), ntiles, block / pc.tj) * pc.tj *
+         static_cast<long long>(sizeof(float4));
+}
+
+// AUTO: the warp kernel up to kWarpMaxN; above it the pair path while its
+// reaction partials fit kPairsMaxBytes, else the one-sided stream-K kernel.
+int auto_path(long long n) {
+  if (n <= kWarpMaxN) return NBODY_PATH_WARP;
+  const long long cap = env_int("NBODY_PAIRS_MAX_BYTES", kPairsMaxBytes);
+  return pair_react_bytes(n) <= cap ? NBODY_PATH_PAIRS : NBODY_PATH_SPLIT;
+}
+
 int make_plan(long long n, int path, int split, int dev, Plan* p) {
   DeviceInfo d;
   const int st = device_info(dev, &d);
@@ -261,10 +335,12 @@ int make_plan(long long n, int path, int split, int dev, Plan* p) {
   *p = Plan();
   p->sms = d.sms;
   int resolved = path;
-  if (resolved == NBODY_PATH_AUTO) resolved = n <= kWarpMaxN ? NBODY_PATH_WARP : NBODY_PATH_SPLIT;
+  if (resolved == NBODY_PATH_AUTO) resolved = auto_path(n);
   p->path = resolved;
   if (resolved == NBODY_PATH_WARP)
     plan_warp(n, split, d, p);
+  else if (resolved == NBODY_PATH_PAIRS)
+    plan_pairs(n, d, p);
   else
     plan_tiled(n, resolved, path == NBODY_PATH_AUTO ? 0 : split, d, p);
   return NBODY_OK;
@@ -304,7 +380,12 @@ int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapf
   std::lock_guard<std::mutex> lk(g_mu);
   Scratch& s = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
   int rc = NBODY_OK;
-  if (p.path != NBODY_PATH_WARP) {
+  if (p.path == NBODY_PATH_PAIRS) {
+    rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
+    if (rc == NBODY_OK) rc = ensure(s.act, static_cast<size_t>(n) * sizeof(float4), st);
+    if (rc == NBODY_OK)
+      rc = ensure(s.react, static_cast<size_t>(p.units) * p.tj * sizeof(float4), st);
+  } else if (p.path != NBODY_PATH_WARP) {
     if (p.second_pass)
       rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
   } else if (p.second_pass) {
@@ -334,7 +415,7 @@ bool overlaps_sized(const void* a, size_t abytes, const void* b, size_t bbytes) 
 int check_scalars(int64_t n, float eps2, int path, int split) {
   if (n < 0 || n > static_cast<int64_t>(INT32_MAX)) return NBODY_EINVAL;
   if (!std::isfinite(eps2) || !(eps2 > 0.0f)) return NBODY_EINVAL;
-  if (path < NBODY_PATH_AUTO || path > NBODY_PATH_WARP) return NBODY_EINVAL;
+  if (path < NBODY_PATH_AUTO || path > NBODY_PATH_PAIRS) return NBODY_EINVAL;
   if (split < 0) return NBODY_EINVAL;
   return NBODY_OK;
 }
@@ -385,8 +466,43 @@ bool vec_aligned(const void* p, int layout) {
 
 // One force pass (plus its second pass): sources and targets `pos`, finished
 // through `epi`.
-void launch_force(const Plan& p, const float4* pos, long long n, float eps2, float4* partial,
+// Plan a force pass and get its scratch.  When the automatic plan chose the
+// pair path and its reaction partials cannot be allocated, the one-sided
+// stream-K plan (far less scratch) is taken instead.
+int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st, bool leapfrog,
+                      Plan* p, Scratch** s) {
+  int rc = make_plan(n, path, split, dev, p);
+  if (rc != NBODY_OK) return rc;
+  rc = get_scratch(dev, st, *p, n, leapfrog, s);
+  if (rc == NBODY_ENOMEM && path == NBODY_PATH_AUTO && p->path == NBODY_PATH_PAIRS) {
+    if ((rc = make_plan(n, NBODY_PATH_SPLIT, 0, dev, p)) != NBODY_OK) return rc;
+    rc = get_scratch(dev, st, *p, n, leapfrog, s);
+  }
+  return rc;
+}
+
+void launch_force(const Plan& p, const float4* pos, long long n, float eps2, const Scratch& s,
                   const Epilogue& epi, cudaStream_t st) {
+  float4* partial = static_cast<float4*>(s.partial.p);
+  if (p.path == NBODY_PATH_PAIRS) {
+    const PairConfig& pc = kPairs[p.cfg];
+    PairArgs a{pos,     static_cast<int>(n),
+               eps2,    p.ntiles,
+               p.nblocks, p.units,
+               p.grid,  static_cast<float4*>(s.act.p),
+               partial, static_cast<float4*>(s.react.p),
+               kWaitLimitNs, -1};
+    cudaEvent_t e0 = prof_event(st);
+    pc.kernel<<<static_cast<unsigned>(p.grid), p.threads, pc.smem(), st>>>(a);
+    cudaEvent_t e1 = prof_event(st);
+    if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+    count_launches(2);
+    PairFinishArgs f{a.act, partial, a.react, static_cast<int>(n), p.block, p.tj,
+                     p.ntiles, p.units, p.grid};
+    const long long blocks = ceil_div(n, kFinishThreads);
+    finish_pairs<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(f, epi);
+    return;
+  }
   if (p.path == NBODY_PATH_WARP) {
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
@@ -431,13 +547,12 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
   if ((rc = check_device_pointer(pos_mass, dev)) != NBODY_OK) return rc;
   if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
   Plan p;
-  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
   Scratch* s = nullptr;
-  if ((rc = get_scratch(dev, st, p, n, false, &s)) != NBODY_OK) return rc;
+  if ((rc = plan_with_scratch(n, path, split, dev, st, false, &p, &s)) != NBODY_OK) return rc;
 
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   const Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, layout, n);
-  launch_force(p, pos, n, eps2, static_cast<float4*>(s->partial.p), epi, st);
+  launch_force(p, pos, n, eps2, *s, epi, st);
   return launch_status();
 }
 
@@ -472,9 +587,8 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
   if ((rc = check_device_pointer(vel, dev)) != NBODY_OK) return rc;
   if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
   Plan p;
-  if ((rc = make_plan(n, path, split, dev, &p)) != NBODY_OK) return rc;
   Scratch* s = nullptr;
-  if ((rc = get_scratch(dev, st, p, n, true, &s)) != NBODY_OK) return rc;
+  if ((rc = plan_with_scratch(n, path, split, dev, st, true, &p, &s)) != NBODY_OK) return rc;
 
   float4* user = reinterpret_cast<float4*>(pos_mass);
   float4* alt = static_cast<float4*>(s->pos_alt.p);
@@ -488,16 +602,15 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
     cur = alt;
     nxt = user;
   }
-  float4* partial = static_cast<float4*>(s->partial.p);
   for (int k = 0; k < steps; ++k) {
     const float kick = (kdk && k > 0) ? dt : 0.5f * dt;
     const Epilogue epi = make_epilogue(cur, accel, vel, nxt, kick, dt, layout, n);
-    launch_force(p, cur, n, eps2, partial, epi, st);
+    launch_force(p, cur, n, eps2, *s, epi, st);
     std::swap(cur, nxt);
   }
   if (kdk) {
     const Epilogue last = make_epilogue(cur, accel, vel, nullptr, 0.5f * dt, dt, layout, n);
-    launch_force(p, cur, n, eps2, partial, last, st);
+    launch_force(p, cur, n, eps2, *s, last, st);
   }
   return launch_status();
 }
@@ -846,7 +959,7 @@ void nbody_release(void) {
       continue;
     }
     cudaDeviceSynchronize();
-    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial}) {
+    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial, &kv.second.act, &kv.second.react}) {
       if (b->p != nullptr) cudaFree(b->p);
       b->p = nullptr;
       b->bytes = 0;
@@ -861,29 +974,59 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   using namespace nbody;
   if (timeout_ms <= 0) return NBODY_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int rc = NBODY_OK, dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  DeviceInfo d;
+  if ((rc = device_info(dev, &d)) != NBODY_OK) return rc;  // sets the kernels' attributes
+  const uint64_t limit = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+
+  // One CTA of each tile-copying kernel whose first copy is never issued:
+  // the smallest one-sided tiled kernel over one i-block, and the default
+  // pair kernel over two i-blocks (zero bodies; only the wait matters).
   constexpr int kCfg = 2;  // smallest tiled kernel (4 KB tiles)
   const TiledConfig& tc = kTiled[kCfg];
-  const long long n = static_cast<long long>(tc.ki) * tc.nt;  // one i-block
-  const long long ntiles = ceil_div(n, tc.tj);
-  float4 *pos = nullptr, *acc = nullptr;
-  const size_t pb = n * sizeof(float4);
-  if (cudaMalloc(&pos, pb) != cudaSuccess || cudaMalloc(&acc, pb) != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(pos);
-    cudaFree(acc);
-    return NBODY_ENOMEM;
-  }
-  cudaMemsetAsync(pos, 0, pb, st);
-  TiledArgs a{pos, static_cast<int>(n), 1.0f, ntiles, ntiles, 1, nullptr,
-              static_cast<uint64_t>(timeout_ms) * 1000000ull, 0};
-  const Epilogue epi = make_epilogue(pos, acc, nullptr, nullptr, 0.f, 0.f, kRows4, n);
+  const PairConfig& pc = kPairs[0];
+  const long long n1 = static_cast<long long>(tc.ki) * tc.nt;
+  const long long pb = static_cast<long long>(pc.ki) * pc.nt;
+  const long long n2 = 2 * pb;
+  const long long nt2 = ceil_div(n2, pc.tj);
+  const long long units2 = pair_units_before(2, nt2, pb / pc.tj);
+  const size_t sizes[] = {static_cast<size_t>(n2) * sizeof(float4),  // positions (both)
+                          static_cast<size_t>(n2) * sizeof(float4),  // accel / action
+                          static_cast<size_t>(2 * pb) * sizeof(float4),
+                          static_cast<size_t>(units2 * pc.tj) * sizeof(float4)};
+  float4* buf[4] = {nullptr, nullptr, nullptr, nullptr};
+  auto free_all = [&]() {
+    for (float4*& b : buf) {
+      cudaFree(b);
+      b = nullptr;
+    }
+  };
+  for (int k = 0; k < 4; ++k)
+    if (cudaMalloc(&buf[k], sizes[k]) != cudaSuccess) {
+      cudaGetLastError();
+      free_all();
+      return NBODY_ENOMEM;
+    }
+  cudaMemsetAsync(buf[0], 0, sizes[0], st);
+
+  TiledArgs a{buf[0], static_cast<int>(n1), 1.0f, ceil_div(n1, tc.tj), ceil_div(n1, tc.tj), 1,
+              nullptr, limit, 0};
+  const Epilogue epi = make_epilogue(buf[0], buf[1], nullptr, nullptr, 0.f, 0.f, kRows4, n1);
   tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
-  int rc = launch_status();
-  const int srv = nbody_sync(cuda_stream);
-  if (rc == NBODY_OK) rc = srv;
-  cudaFree(pos);
-  cudaFree(acc);
-  return rc;
+  int rc1 = launch_status();
+  const int s1 = nbody_sync(cuda_stream);
+  if (rc1 == NBODY_OK) rc1 = s1;
+
+  PairArgs pa{buf[0], static_cast<int>(n2), 1.0f, nt2, 2, units2, 1, buf[1], buf[2], buf[3],
+              limit, 0};
+  pc.kernel<<<1, pc.nt, pc.smem(), st>>>(pa);
+  int rc2 = launch_status();
+  const int s2 = nbody_sync(cuda_stream);
+  if (rc2 == NBODY_OK) rc2 = s2;
+  free_all();
+  if (rc1 != NBODY_ETIMEOUT) return rc1;
+  return rc2;
 }
 
 }  // extern "C"

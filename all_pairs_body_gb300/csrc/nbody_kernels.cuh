@@ -19,6 +19,14 @@
 //                       it writes a partial sum for the second pass.
 //   finish_streamk      second pass for the tiled kernel: sums the partials
 //                       of split i-blocks in CTA (= j) order and finishes.
+//   force_pairs<KI,NT,TJ>
+//                       the tiled kernel with each pair of bodies in
+//                       different i-blocks evaluated once (Newton's third
+//                       law): action on the targets in registers, reaction on
+//                       the sources reduced over the CTA (warp butterfly,
+//                       then warps in order) into one partial per unit.
+//   finish_pairs        its second pass: action + reactions in block order,
+//                       then the finish (accel or kick/drift) of every body.
 //   force_warp<KW,NW>   small-n kernel: a CTA owns KW targets; its NW*32
 //                       threads stride over one j slice; warp shuffles then
 //                       shared memory (fixed order) combine the threads.
@@ -525,6 +533,365 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
     sx += p.x;
     sy += p.y;
     sz += p.z;
+  }
+  finish_body(e, i, sx, sy, sz);
+}
+
+// ---------------------------------------------------------------------------
+// pair-symmetric tiled force kernel
+// ---------------------------------------------------------------------------
+//
+// Every unordered pair of bodies in different i-blocks is evaluated once: the
+// term m_i (x_i - x_j) d^(-3/2) that body i adds to a_j is the negative of what
+// the same pair gives a_i with m_j replaced by m_i, bit for bit (the same r,
+// d and d^(-3/2) in FP32), so one evaluation serves both bodies (Newton's
+// third law).  Pairs inside one i-block are evaluated from both sides, as in
+// force_tiled.  Per pair: 3 FADD + 3 FFMA (d) + 1 MUFU.RSQ + 2 FMUL (d^-3/2)
+// + 2 FMUL (the two mass factors) + 6 FFMA (action and reaction) = 16 FP32
+// lane-ops for two interactions, against 24 for the one-sided form.
+//
+// Work: block I (B = KI * NT targets) meets the source tiles t of its own
+// block and of every later block, tiles [TB*I, ntiles) with TB = B / TJ, in
+// that order; the (I, t) units are numbered block by block and divided
+// evenly over one wave of CTAs as in force_tiled.  For a tile past block I
+// the reaction on its TJ sources is reduced over the CTA's B targets (a warp
+// butterfly that scatters 8 sources over the lanes, then the NW warps in
+// order through shared memory) and stored as that unit's partial; the
+// second pass adds, for each body, its action and the reactions from the
+// blocks before its own in block order.
+
+// Units of blocks 0 .. I-1: block I' has ntiles - TB * I' units.
+__host__ __device__ __forceinline__ long long pair_units_before(long long I, long long ntiles,
+                                                                long long tb) {
+  return I * ntiles - tb * (I * (I - 1) / 2);
+}
+
+struct PairArgs {
+  const float4* pos;  // n rows (x, y, z, m)
+  int n;
+  float eps2;
+  long long ntiles;   // source tiles of TJ bodies over n
+  long long nblocks;  // i-blocks of B bodies over n
+  long long units;    // pair_units_before(nblocks)
+  long long grid;     // CTAs launched
+  float4* act;        // [n] action sums of i-blocks one CTA covered whole
+  float4* partial;    // [grid][2][B] action sums of split i-blocks
+  float4* react;      // [units][TJ] reaction sums of the units past the diagonal
+  uint64_t timeout_ns;
+  long long withhold;  // failure-detection check only (see TiledArgs)
+};
+
+// One source (duplicated pairs X, Y, Z, M) against two targets (negated
+// coordinates nx, ny, nz and negated masses nm): the action on the targets
+// goes to (ax, ay, az), the reaction on the source to (bx, by, bz) per target
+// half.
+__device__ __forceinline__ void interact2_pair(float2 X, float2 Y, float2 Z, float2 M, float2 nx,
+                                               float2 ny, float2 nz, float2 nm, float2 e2,
+                                               float2& ax, float2& ay, float2& az, float2& bx,
+                                               float2& by, float2& bz) {
+  const float2 rx = __fadd2_rn(X, nx);
+  const float2 ry = __fadd2_rn(Y, ny);
+  const float2 rz = __fadd2_rn(Z, nz);
+  float2 d = __ffma2_rn(rx, rx, e2);
+  d = __ffma2_rn(ry, ry, d);
+  d = __ffma2_rn(rz, rz, d);
+  const float2 q = make_float2(rsqrt_approx(d.x), rsqrt_approx(d.y));
+  const float2 q3 = __fmul2_rn(__fmul2_rn(q, q), q);
+  const float2 si = __fmul2_rn(M, q3);
+  const float2 sj = __fmul2_rn(nm, q3);
+  ax = __ffma2_rn(rx, si, ax);
+  ay = __ffma2_rn(ry, si, ay);
+  az = __ffma2_rn(rz, si, az);
+  bx = __ffma2_rn(rx, sj, bx);
+  by = __ffma2_rn(ry, sj, by);
+  bz = __ffma2_rn(rz, sj, bz);
+}
+
+// Sum v[0..7] (one value per source of a batch of 8) over the 32 lanes of the
+// warp and leave source l >> 2's total in lane l: each butterfly level halves
+// the values a lane keeps (8, 4, 2, 1), the last two levels sum the one left.
+// 27 shuffles and 27 adds for 8 sources x 3 components.
+__device__ __forceinline__ float3 reduce_scatter8(const float (&vx)[8], const float (&vy)[8],
+                                                  const float (&vz)[8], int lane) {
+  const bool h = (lane >> 4) & 1, g = (lane >> 3) & 1, f = (lane >> 2) & 1;
+  constexpr unsigned kAll = 0xffffffffu;
+  float wx[4], wy[4], wz[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    wx[q] = (h ? vx[q + 4] : vx[q]) + __shfl_xor_sync(kAll, h ? vx[q] : vx[q + 4], 16);
+    wy[q] = (h ? vy[q + 4] : vy[q]) + __shfl_xor_sync(kAll, h ? vy[q] : vy[q + 4], 16);
+    wz[q] = (h ? vz[q + 4] : vz[q]) + __shfl_xor_sync(kAll, h ? vz[q] : vz[q + 4], 16);
+  }
+  float ux[2], uy[2], uz[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    ux[q] = (g ? wx[q + 2] : wx[q]) + __shfl_xor_sync(kAll, g ? wx[q] : wx[q + 2], 8);
+    uy[q] = (g ? wy[q + 2] : wy[q]) + __shfl_xor_sync(kAll, g ? wy[q] : wy[q + 2], 8);
+    uz[q] = (g ? wz[q + 2] : wz[q]) + __shfl_xor_sync(kAll, g ? wz[q] : wz[q + 2], 8);
+  }
+  float x = (f ? ux[1] : ux[0]) + __shfl_xor_sync(kAll, f ? ux[0] : ux[1], 4);
+  float y = (f ? uy[1] : uy[0]) + __shfl_xor_sync(kAll, f ? uy[0] : uy[1], 4);
+  float z = (f ? uz[1] : uz[0]) + __shfl_xor_sync(kAll, f ? uz[0] : uz[1], 4);
+  x += __shfl_xor_sync(kAll, x, 2);
+  y += __shfl_xor_sync(kAll, y, 2);
+  z += __shfl_xor_sync(kAll, z, 2);
+  x += __shfl_xor_sync(kAll, x, 1);
+  y += __shfl_xor_sync(kAll, y, 1);
+  z += __shfl_xor_sync(kAll, z, 1);
+  return make_float3(x, y, z);
+}
+
+// Dynamic shared memory of force_pairs: the per-warp reaction sums of a tile.
+__host__ __device__ constexpr size_t pair_reduce_smem(int nt, int tj) {
+  return static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float);
+}
+
+template <int KI, int NT, int TJ>
+__global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
+  static_assert(KI % 2 == 0, "targets are processed in packed pairs");
+  static_assert((KI * NT) % TJ == 0 && TJ % 8 == 0, "tiles tile an i-block; batches tile a tile");
+  constexpr int P = KI / 2;
+  constexpr int NW = NT / 32;
+  constexpr long long B = static_cast<long long>(KI) * NT;
+  constexpr long long TB = B / TJ;
+
+  __shared__ __align__(128) float4 raw[2][TJ];    // TMA targets: the caller's rows
+  __shared__ __align__(128) float4 tile[2 * TJ];  // expanded: (x,x,y,y),(z,z,m,m)
+  __shared__ __align__(8) unsigned long long bar[2];
+  extern __shared__ __align__(16) float react_smem[];  // [NW][3][TJ]
+  auto red = reinterpret_cast<float(*)[3][TJ]>(react_smem);
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const long long c = blockIdx.x;
+  const long long u_lo = unit_begin(a.units, a.grid, c);
+  const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
+  const uint32_t bar0 = smem_u32(&bar[0]);
+  const uint32_t raw0 = smem_u32(&raw[0][0]);
+  constexpr uint32_t kRawStride = sizeof(raw[0]);
+  auto bar_of = [&](long long k) { return bar0 + static_cast<uint32_t>(k & 1) * 8u; };
+  auto raw_of = [&](long long k) { return raw0 + static_cast<uint32_t>(k & 1) * kRawStride; };
+
+  // block and tile of the CTA's first unit (largest I with units_before(I) <= u_lo)
+  long long I0 = 0;
+  {
+    long long lo = 0, hi = a.nblocks - 1;
+    while (lo < hi) {
+      const long long mid = (lo + hi + 1) / 2;
+      if (pair_units_before(mid, a.ntiles, TB) <= u_lo)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    I0 = lo;
+  }
+  const long long t0 = TB * I0 + (u_lo - pair_units_before(I0, a.ntiles, TB));
+
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8u, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (count <= 0) return;
+
+  // Thread 0 issues the copies in unit order with its own (block, tile) cursor.
+  long long iss_I = I0, iss_t = t0;
+  auto issue_next = [&](long long k) {
+    if (k != a.withhold) {
+      const long long j0 = iss_t * TJ;
+      const uint32_t bytes =
+          static_cast<uint32_t>(min(static_cast<long long>(TJ), a.n - j0)) * 16u;
+      mbar_arrive_expect_tx(bar_of(k), bytes);
+      bulk_copy_g2s(raw_of(k), a.pos + j0, bytes, bar_of(k));
+    }
+    if (++iss_t == a.ntiles) {
+      ++iss_I;
+      iss_t = TB * iss_I;
+    }
+  };
+  if (tid == 0) issue_next(0);
+
+  const float2 e2 = make_float2(a.eps2, a.eps2);
+  float2 nx[P], ny[P], nz[P], nm[P], ax[P], ay[P], az[P];
+  long long k = 0, I = I0, t = t0;
+  bool timed_out = false;
+
+  while (k < count) {
+    const long long blk = I;
+    const long long tb = t;
+    const long long te = min(a.ntiles, tb + (count - k));
+    const bool first_segment = (k == 0);
+
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const long long i0 = blk * B + (2 * p) * NT + tid;
+      const long long i1 = i0 + NT;
+      const float4 q0 = a.pos[min(i0, static_cast<long long>(a.n - 1))];
+      const float4 q1 = a.pos[min(i1, static_cast<long long>(a.n - 1))];
+      nx[p] = make_float2(-q0.x, -q1.x);
+      ny[p] = make_float2(-q0.y, -q1.y);
+      nz[p] = make_float2(-q0.z, -q1.z);
+      // targets past n exert no reaction
+      nm[p] = make_float2(i0 < a.n ? -q0.w : 0.f, i1 < a.n ? -q1.w : 0.f);
+      ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+    }
+
+    for (; t < te; ++t, ++k) {
+      const int s = static_cast<int>(k & 1);
+      const bool ok = mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
+      // As in force_tiled, and: every thread is done with the previous tile's
+      // reaction sums in shared memory before they are rewritten.
+      if (!__syncthreads_and(ok)) {
+        timed_out = true;
+        break;
+      }
+      if (tid == 0 && k + 1 < count) issue_next(k + 1);
+      (void)expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
+      __syncthreads();
+
+      float2 tx[P], ty[P], tz[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
+      const float4* src = tile;
+      if (t < TB * (blk + 1)) {
+        // a tile of the block itself: both sides of each pair, as in force_tiled
+#pragma unroll 2
+        for (int j = 0; j < TJ; ++j) {
+          const float4 lo = src[2 * j];
+          const float4 hi = src[2 * j + 1];
+#pragma unroll
+          for (int p = 0; p < P; ++p)
+            interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w), make_float2(hi.x, hi.y),
+                      make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+        }
+      } else {
+#pragma unroll 1
+        for (int b0 = 0; b0 < TJ; b0 += 8) {
+          float vx[8], vy[8], vz[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 lo = src[2 * (b0 + q)];
+            const float4 hi = src[2 * (b0 + q) + 1];
+            float2 bx = make_float2(0.f, 0.f), by = bx, bz = bx;
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+              interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                             make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                             nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+            vx[q] = bx.x + bx.y;
+            vy[q] = by.x + by.y;
+            vz[q] = bz.x + bz.y;
+          }
+          const float3 r = reduce_scatter8(vx, vy, vz, lane);
+          if ((lane & 3) == 0) {
+            red[warp][0][b0 + (lane >> 2)] = r.x;
+            red[warp][1][b0 + (lane >> 2)] = r.y;
+            red[warp][2][b0 + (lane >> 2)] = r.z;
+          }
+        }
+        __syncthreads();
+        // the unit's reaction partial: the NW warps' sums in warp order
+        const long long u = u_lo + k;
+        for (int j = tid; j < TJ; j += NT) {
+          float sx = 0.f, sy = 0.f, sz = 0.f;
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            sx += red[w][0][j];
+            sy += red[w][1][j];
+            sz += red[w][2][j];
+          }
+          a.react[u * TJ + j] = make_float4(sx, sy, sz, 0.f);
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        ax[p] = __fadd2_rn(ax[p], tx[p]);
+        ay[p] = __fadd2_rn(ay[p], ty[p]);
+        az[p] = __fadd2_rn(az[p], tz[p]);
+      }
+    }
+    if (timed_out) break;
+
+    const bool whole = (tb == TB * blk && te == a.ntiles);
+    const long long slot = (c * 2 + (first_segment ? 0 : 1)) * B;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const long long local = (2 * p + h) * NT + tid;
+        const long long i = blk * B + local;
+        if (i < a.n) {
+          const float4 v = make_float4(h ? ax[p].y : ax[p].x, h ? ay[p].y : ay[p].x,
+                                       h ? az[p].y : az[p].x, 0.f);
+          if (whole)
+            a.act[i] = v;
+          else
+            a.partial[slot + local] = v;
+        }
+      }
+    }
+    if (t == a.ntiles) {  // the segment reached the last tile: next block
+      ++I;
+      t = TB * I;
+    }
+  }
+
+  if (timed_out && tid == 0) {
+    atomicExch(&g_status, static_cast<int>(NBODY_ETIMEOUT));
+    if (k != a.withhold)
+      (void)mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
+  }
+}
+
+// Second pass of force_pairs: one thread per body.  a_i = its action (whole
+// or the stream-K partials of its block, in CTA order) + the reactions of
+// its tile from blocks 0 .. I-1 in block order; then finish_body.
+struct PairFinishArgs {
+  const float4* act;
+  const float4* partial;
+  const float4* react;
+  int n;
+  long long block;  // B
+  long long tj;
+  long long ntiles;
+  long long units;
+  long long grid;
+};
+
+__global__ void finish_pairs(const PairFinishArgs a, const Epilogue e) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  const long long tb = a.block / a.tj;
+  const long long I = i / a.block;
+  const long long u0 = pair_units_before(I, a.ntiles, tb);
+  const long long u1 = pair_units_before(I + 1, a.ntiles, tb) - 1;
+  const long long c0 = unit_owner(a.units, a.grid, u0);
+  const long long c1 = unit_owner(a.units, a.grid, u1);
+  float sx = 0.f, sy = 0.f, sz = 0.f;
+  if (c0 == c1) {
+    const float4 v = a.act[i];
+    sx = v.x;
+    sy = v.y;
+    sz = v.z;
+  } else {
+    const long long local = i - I * a.block;
+    for (long long cc = c0; cc <= c1; ++cc) {
+      const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
+      const float4 p = a.partial[(cc * 2 + side) * a.block + local];
+      sx += p.x;
+      sy += p.y;
+      sz += p.z;
+    }
+  }
+  const long long t = i / a.tj;
+  const long long j = i - t * a.tj;
+  for (long long J = 0; J < I; ++J) {
+    const float4 r = a.react[(pair_units_before(J, a.ntiles, tb) + t - tb * J) * a.tj + j];
+    sx += r.x;
+    sy += r.y;
+    sz += r.z;
   }
   finish_body(e, i, sx, sy, sz);
 }

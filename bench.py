@@ -14,7 +14,9 @@ N^2 body-body interactions per step.
                positions and velocities in, runs the step and copies
                positions, velocities and accelerations back
     roofline = the force kernel alone against the FP32 issue roofline
-               SMs x f_SM x 128 lanes / 12 FP32 lane-ops per interaction
+               SMs x f_SM x 128 lanes / FP32 lane-ops per interaction: 12 for
+               the one-sided kernels, 8 for the pair-symmetric kernel (16 per
+               pair, which serves two interactions)
     cpu_baseline = the FP64 CPU oracle on a bounded sample of the same bodies
 
 ``--impl reference`` times the FP64 CPU oracle on the host cores instead.
@@ -40,9 +42,15 @@ UNIT = "Ginteractions/s"
 DEFAULT_WORKLOAD = "ball-lognormal-1048576"
 FLOP_PER_INTERACTION = 20  # bodybodyinteraction FLOP comments, "Cuda Nbody Notes"
 FP32_OPS_PER_INTERACTION = 12  # 3 FADD + 3 FFMA (|r|^2+eps2) + 3 FMUL (m q^3) + 3 FFMA (a += s r)
+# pair-symmetric kernel, per pair (two interactions): 3 FADD + 3 FFMA + 2 FMUL (q^3)
+# + 2 FMUL (both mass factors) + 6 FFMA (action and reaction) = 16
+FP32_OPS_PER_INTERACTION_PAIRS = 8
 FP32_LANES_PER_SM = 128  # per clock: 4 SM sub-partitions x 32 FP32 lanes
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "force_tiled_ball-lognormal-1048576.md")
+PROFILE_SUMMARIES = {  # force kernel -> committed ncu summary of one launch
+    "force_tiled": os.path.join(ROOT, "profiles", "force_tiled_ball-lognormal-1048576.md"),
+    "force_pairs": os.path.join(ROOT, "profiles", "force_pairs_ball-lognormal-1048576.md"),
+}
 KERNEL_SOURCE = os.path.join(ROOT, "all_pairs_body_gb300", "csrc", "nbody_kernels.cuh")
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -63,7 +71,7 @@ def parse_args(argv=None):
                          "only; kdk: one kick-drift-kick step (two force passes); render: the "
                          "point-shader kernel (memory-bound, reported in GB/s); neighbors: the "
                          "2-D cutoff neighbour list (pair tests/s; default points2d-1048576)")
-    ap.add_argument("--path", choices=("auto", "tiled", "split", "warp"), default="auto",
+    ap.add_argument("--path", choices=("auto", "tiled", "split", "warp", "pairs"), default="auto",
                     help="force-pass path for --mode step|accel|kdk (the library's choice by "
                          "default); NBODY_TILED_CONFIG selects a row of the tiled-kernel table")
     ap.add_argument("--split", type=int, default=0,
@@ -200,9 +208,10 @@ def measured_sm_max_mhz(clocks: dict | None) -> tuple[float, str]:
     return 2070.0, "fallback maximum SM clock"
 
 
-def alu_peak_ginter(sms: int, mhz: float) -> float:
-    """FP32 issue roofline in billions of interactions/s."""
-    return sms * mhz * 1e6 * FP32_LANES_PER_SM / FP32_OPS_PER_INTERACTION / 1e9
+def alu_peak_ginter(sms: int, mhz: float, ops: int = FP32_OPS_PER_INTERACTION) -> float:
+    """FP32 issue roofline in billions of interactions/s at `ops` FP32
+    lane-ops per interaction."""
+    return sms * mhz * 1e6 * FP32_LANES_PER_SM / ops / 1e9
 
 
 def kernel_source_digest() -> str:
@@ -210,12 +219,13 @@ def kernel_source_digest() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(n: int) -> float | None:
+def profiled_traffic(n: int, kernel: str = "force_tiled") -> float | None:
     """DRAM bytes per force-kernel launch from the committed ncu summary,
-    scaled to n bodies, or None if the kernel changed since the capture."""
+    scaled to n bodies (by n, or n^2 where the summary says the traffic grows
+    so), or None if there is no summary or the kernel changed since."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        text = open(PROFILE_SUMMARIES[kernel]).read()
+    except (OSError, KeyError):
         return None
     fields = {}
     for line in text.splitlines():
@@ -229,7 +239,8 @@ def profiled_traffic(n: int) -> float | None:
         n_captured = float(fields["n_captured"])
     except (KeyError, ValueError):
         return None
-    return bytes_captured * n / n_captured  # traffic grows with n (sources stay in L2)
+    power = 2 if fields.get("traffic_scales_as") == "n^2" else 1
+    return bytes_captured * (n / n_captured) ** power
 
 
 # ---------------------------------------------------------------------------
@@ -317,7 +328,7 @@ def run_ours(args):
     m_hi = max(float(w.pos_mass[:, 3].max()), m_lo * (1 + 1e-6) + 1e-30)
 
     path = {"auto": nb.PATH_AUTO, "tiled": nb.PATH_TILED, "split": nb.PATH_SPLIT,
-            "warp": nb.PATH_WARP}[args.path]
+            "warp": nb.PATH_WARP, "pairs": nb.PATH_PAIRS}[args.path]
     if (path or args.split) and (layout or args.mode == "render"):
         raise SystemExit("--path/--split apply to --mode step|accel|kdk with rows4")
 
@@ -416,16 +427,22 @@ def run_ours(args):
     f_max, f_src = measured_sm_max_mhz(clocks)
     achieved = (interactions_per_launch / (force_ms / 1e3 / force_launches) / 1e9
                 if force_launches else None)
-    peak = alu_peak_ginter(sms, f_max)
+    kernel = {nb.PATH_WARP: "force_warp", nb.PATH_PAIRS: "force_pairs"}.get(plan["path"],
+                                                                         "force_tiled")
+    ops = FP32_OPS_PER_INTERACTION_PAIRS if kernel == "force_pairs" else FP32_OPS_PER_INTERACTION
+    peak = alu_peak_ginter(sms, f_max, ops)
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": UNIT,
             "frac": (achieved / peak) if achieved else None,
-            "traffic": profiled_traffic(n),
+            "traffic": profiled_traffic(n, kernel),
             "peak_basis": f"{sms} SMs x {f_max:g} MHz ({f_src}) x {FP32_LANES_PER_SM} FP32 lanes"
-                          f" / {FP32_OPS_PER_INTERACTION} FP32 ops per interaction",
-            "kernel": "force_tiled" if plan["path"] != nb.PATH_WARP else "force_warp",
+                          f" / {ops} FP32 ops per interaction",
+            "kernel": kernel,
             "force_ms_per_launch": force_ms / force_launches if force_launches else None}
+    if kernel == "force_pairs" and achieved:
+        # the same launch against the one-sided form's 12 ops per interaction
+        roof["frac_of_one_sided_roofline"] = achieved / alu_peak_ginter(sms, f_max)
     if clocks and achieved:
-        pc = alu_peak_ginter(sms, clocks["sm_mhz"])
+        pc = alu_peak_ginter(sms, clocks["sm_mhz"], ops)
         roof["peak_at_measured_clock"] = pc
         roof["frac_at_measured_clock"] = achieved / pc
 

@@ -29,8 +29,9 @@
  * (cudaMalloc / cudaMallocAsync / managed memory); host pointers are
  * rejected with NBODY_EINVAL.  The caller owns every array it passes.  The
  * library owns only its cached scratch (the ping-pong positions of a
- * multi-step call and the split-j partial sums), allocated on first use per
- * (device, stream) and freed by nbody_release().
+ * multi-step call, the split-j partial sums and the pair path's action and
+ * reaction sums), allocated on first use per (device, stream) and freed by
+ * nbody_release().
  *
  * Execution is asynchronous: a call validates its arguments, enqueues its
  * kernels on the stream and returns.  NBODY_OK means "enqueued"; a device
@@ -73,9 +74,11 @@ typedef enum nbody_status {
 
 /* Force-pass path for the *_with entry points. */
 typedef enum nbody_path {
-    /* Library's choice: the tiled kernel with its work (i-block, j-tile
-       pairs) divided evenly over one wave of CTAs (stream-K), or the
-       warp-split kernel for small n. */
+    /* Library's choice: the warp-split kernel for small n, the
+       pair-symmetric kernel above it (NBODY_PATH_PAIRS), the one-sided
+       tiled kernel with its (i-block, j-tile) units divided evenly over one
+       wave of CTAs (stream-K) where the pair path's scratch would be too
+       large. */
     NBODY_PATH_AUTO = 0,
     /* One CTA per i-block over the whole j range; no second pass.  The
        pages' tiled design ("CUDA N-Body Simulation" §3.1). */
@@ -87,7 +90,19 @@ typedef enum nbody_path {
     /* Small-n kernel: the 32 lanes of a warp share target bodies and
        stride over sources; lanes combine by warp shuffles, warps through
        shared memory in fixed order, CTAs through the second pass. */
-    NBODY_PATH_WARP = 3
+    NBODY_PATH_WARP = 3,
+    /* Pair-symmetric tiled kernel: every pair of bodies in different
+       i-blocks is evaluated once and serves both bodies (Newton's third
+       law: the term body i adds to a_j is the negative of the one body j
+       adds to a_i with m_j replaced by m_i, bit for bit in FP32), about 2/3
+       of the FP32 work of the one-sided paths.  The reactions on a tile's
+       sources are summed over the CTA's targets in fixed order and stored
+       per (i-block, tile) unit; the second pass adds them to the action in
+       block order.  Scratch: about n^2 / 320 bytes of reaction sums (3.4 GB
+       at n = 2^20).  AUTO takes this path above the warp kernel's range
+       while that scratch is at most 16 GiB (or NBODY_PAIRS_MAX_BYTES), and
+       falls back to NBODY_PATH_SPLIT's plan if it cannot be allocated. */
+    NBODY_PATH_PAIRS = 4
 } nbody_path;
 
 /*
@@ -300,11 +315,12 @@ const char *nbody_strerror(int status);
 void nbody_release(void);
 
 /*
- * Failure-detection check: runs the force kernel on a tiny private problem
- * with one tile copy deliberately never issued and a wait limit of
- * `timeout_ms`, then waits for the stream.  A correct build returns
- * NBODY_ETIMEOUT (the kernel gave up and returned; the context stays
- * usable).  Allocates and frees its own small buffers.
+ * Failure-detection check: runs the one-sided tiled kernel and the pair
+ * kernel, each on a tiny private problem with its first tile copy
+ * deliberately never issued and a wait limit of `timeout_ms`, waiting for
+ * the stream after each.  A correct build returns NBODY_ETIMEOUT (both
+ * kernels gave up and returned; the context stays usable); otherwise the
+ * first other status.  Allocates and frees its own small buffers.
  */
 int nbody_selftest_timeout(int timeout_ms, void *cuda_stream);
 

@@ -71,7 +71,7 @@ def test_accel_bad_scalars(L, n, eps2):
     assert accel(L, A, B, n, eps2) == nb.EINVAL
 
 
-@pytest.mark.parametrize("path,split", [(-1, 0), (4, 0), (0, -1)])
+@pytest.mark.parametrize("path,split", [(-1, 0), (5, 0), (0, -1)])
 def test_accel_bad_path(L, path, split):
     assert accel(L, A, B, 10, 0.1, path, split) == nb.EINVAL
 

@@ -58,11 +58,25 @@ def test_traffic_needs_matching_kernel(tmp_path, monkeypatch):
     summary = tmp_path / "s.md"
     summary.write_text("- kernel_source_sha256_16: `deadbeef`\n- dram_bytes_per_launch: 1000\n"
                        "- n_captured: 10\n")
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(summary))
+    monkeypatch.setitem(bench.PROFILE_SUMMARIES, "force_tiled", str(summary))
     assert bench.profiled_traffic(20) is None
     summary.write_text(f"- kernel_source_sha256_16: `{bench.kernel_source_digest()}`\n"
                        "- dram_bytes_per_launch: 1000\n- n_captured: 10\n")
     assert bench.profiled_traffic(20) == pytest.approx(2000.0)
+    # reaction sums of the pair kernel grow with n^2
+    summary.write_text(f"- kernel_source_sha256_16: `{bench.kernel_source_digest()}`\n"
+                       "- dram_bytes_per_launch: 1000\n- n_captured: 10\n"
+                       "- traffic_scales_as: n^2\n")
+    monkeypatch.setitem(bench.PROFILE_SUMMARIES, "force_pairs", str(summary))
+    assert bench.profiled_traffic(20, "force_pairs") == pytest.approx(4000.0)
+    assert bench.profiled_traffic(20, "force_warp") is None
+
+
+def test_pair_roofline_counts_eight_ops():
+    one_sided = bench.alu_peak_ginter(152, 2070.0)
+    assert one_sided == pytest.approx(152 * 2070e6 * 128 / 12 / 1e9)
+    assert bench.alu_peak_ginter(152, 2070.0, bench.FP32_OPS_PER_INTERACTION_PAIRS) == \
+        pytest.approx(1.5 * one_sided)
 
 
 def test_reference_arm_prints_contract_line():

@@ -16,7 +16,7 @@ from parity import (ACC_TOL, POS_TOL, VEL_TOL, displacement_err, gpu_accel, gpu_
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [(0, 0), (1, 0), (2, 0), (2, 1), (2, 3), (2, 7), (3, 0), (3, 1), (3, 5)]
+PATHS = [(0, 0), (1, 0), (2, 0), (2, 1), (2, 3), (2, 7), (3, 0), (3, 1), (3, 5), (4, 0)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -118,7 +118,7 @@ RAGGED = [1, 2, 3, 7, 8, 9, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257
 
 
 @pytest.mark.parametrize("n", RAGGED)
-@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 0), (2, 3), (3, 0), (3, 2)])
+@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 0), (2, 3), (3, 0), (3, 2), (4, 0)])
 def test_ragged_sizes(n, path, split):
     pm = W.random_bodies(n, 1000 + n)
     a = gpu_accel(pm, 1e-2, path, split)
@@ -145,7 +145,7 @@ def test_two_body_closed_form():
 
 def test_coincident_and_single_bodies():
     pm = np.array([[0.5, 0.5, 0.5, 1.0]] * 5, dtype=np.float32)
-    for path, split in [(0, 0), (1, 0), (3, 0)]:
+    for path, split in [(0, 0), (1, 0), (3, 0), (4, 0)]:
         assert np.all(gpu_accel(pm, 1e-3, path, split)[:, :3] == 0.0)
 
 
@@ -162,7 +162,7 @@ def test_momentum_invariant():
 # ---------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 5), (3, 0)])
+@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 5), (3, 0), (4, 0)])
 def test_bitwise_deterministic(path, split):
     pm = W.cube_sweep(65537).pos_mass
     a1 = gpu_accel(pm, 1e-3, path, split)
@@ -212,13 +212,14 @@ def test_plan_is_consistent():
 
 
 def test_plan_shape_follows_streamk_model():
-    """Above the warp kernel the plan takes the 512- or the 256-source shape,
-    whichever gives the slowest CTA less work: ceil(units / grid) tiles of tj
-    sources at the shape's relative speed (1 and 0.973)."""
+    """Above the warp kernel the one-sided stream-K plan takes the 512- or the
+    256-source shape, whichever gives the slowest CTA less work:
+    ceil(units / grid) tiles of tj sources at the shape's relative speed (1
+    and 0.973)."""
     import all_pairs_body_gb300 as nb
     shapes = ((512, 1.0), (256, 0.973))
     for n in list(range(24577, 140000, 4099)) + [262144, 500000, 1048576, 4194304]:
-        p = nb.plan(n)
+        p = nb.plan(n, path=nb.PATH_SPLIT)
         assert p["bodies_per_cta"] == 2560
         cost = []
         for tj, speed in shapes:
@@ -229,8 +230,71 @@ def test_plan_shape_follows_streamk_model():
         assert p["tile"] == want, (n, cost, p)
         assert p["grid"] == min(p["units"], p["sms"])
     if nb.plan(32768)["sms"] == 152:  # the measured cases on a 152-SM GPU
-        assert [nb.plan(n)["tile"] for n in (32768, 49152, 65537, 81920, 1048576)] == \
-            [256, 512, 256, 512, 512]
+        assert [nb.plan(n, path=nb.PATH_SPLIT)["tile"]
+                for n in (32768, 49152, 65537, 81920, 1048576)] == [256, 512, 256, 512, 512]
+
+
+def pair_units(n, block=2560, tj=512):
+    """Units of the pair path: block I meets the tiles of itself and of every
+    later block."""
+    nb_, nt = -(-n // block), -(-n // tj)
+    return sum(nt - (block // tj) * i for i in range(nb_))
+
+
+def test_plan_pairs_path(monkeypatch):
+    import all_pairs_body_gb300 as nb
+    assert nb.plan(24576)["path"] == nb.PATH_WARP
+    for n in (24577, 65537, 1048576):
+        p = nb.plan(n)
+        assert p["path"] == nb.PATH_PAIRS and p["second_pass"] == 1
+        assert p["bodies_per_cta"] == 2560 and p["tile"] == 512
+        assert p["units"] == pair_units(n)
+        assert p["grid"] == min(p["units"], p["sms"])
+        assert p["launches_accel"] == 2
+    # 4M bodies need ~55 GB of reaction sums: the one-sided plan instead
+    assert nb.plan(4194304)["path"] == nb.PATH_SPLIT
+    monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", "1000")
+    assert nb.plan(65537)["path"] == nb.PATH_SPLIT
+
+
+N_PAIR_VARIANTS = 5
+
+
+@pytest.mark.parametrize("cfg", range(N_PAIR_VARIANTS))
+def test_every_pair_variant(cfg, monkeypatch):
+    monkeypatch.setenv("NBODY_PAIRS_CONFIG", str(cfg))
+    check_accel(W.cube_sweep(20000), path=4)
+    pm = W.random_bodies(9000, 78)
+    v = W.random_velocities(9000, 78)
+    p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, 3, path=4)
+    rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 3)
+    assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
+
+
+# block edges of the default pair shape (2560 targets, 512-source tiles):
+# one block, a block and one body, ragged tiles, several blocks
+@pytest.mark.parametrize("n", [511, 512, 513, 2559, 2560, 2561, 5119, 5120, 5121, 7681,
+                               12800, 12801, 30001])
+def test_pair_path_block_edges(n):
+    pm = W.random_bodies(n, 4000 + n)
+    a = gpu_accel(pm, 1e-3, path=4)
+    assert np.all(a[:, 3] == 0.0)
+    assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL, n
+
+
+def test_pair_path_masses():
+    """Zero, negative and one dominant mass: the reaction uses the target's
+    own mass, so a massless target must pull on nothing."""
+    pm = W.random_bodies(20000, 9)
+    pm[::7, 3] = 0.0
+    pm[1::11, 3] *= -1.0
+    a = gpu_accel(pm, 1e-3, path=4)
+    assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL
+    lone = np.zeros((20000, 4), dtype=np.float32)
+    lone[:, :3] = pm[:, :3]
+    lone[15000, 3] = 1.0  # the only mass sits in the last block: reactions only
+    a = gpu_accel(lone, 1e-3, path=4)
+    assert rel_err(a, oracle.accel(lone, 1e-3)) <= ACC_TOL
 
 
 # ---------------------------------------------------------------------------
