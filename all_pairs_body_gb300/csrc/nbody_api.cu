@@ -73,20 +73,28 @@ struct PairConfig {
   size_t smem() const { return pair_reduce_smem(nt, tj); }  // dynamic shared memory
 };
 
-// Shapes of the pair-symmetric kernel (targets per thread, threads, tile);
-// the first is the default.
+// Shapes of the pair-symmetric kernel (targets per thread, threads, tile;
+// template: + sources per reduction batch, batch-loop unroll); the first is
+// the default.
 const PairConfig kPairs[] = {
-    {10, 256, 512, force_pairs<10, 256, 512>},
-    {8, 256, 256, force_pairs<8, 256, 256>},
-    {10, 256, 256, force_pairs<10, 256, 256>},
-    {8, 256, 512, force_pairs<8, 256, 512>},
-    {8, 256, 128, force_pairs<8, 256, 128>},
+    {10, 256, 512, force_pairs<10, 256, 512, 16, 1>},
+    {10, 256, 512, force_pairs<10, 256, 512, 8, 1>},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 1>},
+    {8, 256, 256, force_pairs<8, 256, 256, 8, 1>},
+    {10, 256, 256, force_pairs<10, 256, 256, 8, 1>},
+    {8, 256, 128, force_pairs<8, 256, 128, 8, 1>},
+    {8, 256, 512, force_pairs<8, 256, 512, 16, 1>},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 2>},
+    {6, 256, 512, force_pairs<6, 256, 512, 16, 1>},
+    {8, 256, 256, force_pairs<8, 256, 256, 16, 1>},
+    {6, 256, 512, force_pairs<6, 256, 512, 8, 2>},
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
 // The automatic plan takes the pair path while its reaction partials stay
-// within this many bytes (units * tile * 16: about N^2 / 320 at the default
-// shape, 3.4 GB at N = 2^20); NBODY_PAIRS_MAX_BYTES overrides it.
+// within this many bytes (units * tile * 16: about 16 N^2 / (2 B) for B
+// targets per i-block, 3.4 GB at N = 2^20 and B = 2560);
+// NBODY_PAIRS_MAX_BYTES overrides it.
 constexpr long long kPairsMaxBytes = 16LL << 30;
 
 struct DeviceInfo {

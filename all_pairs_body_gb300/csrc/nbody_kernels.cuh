@@ -19,7 +19,7 @@
 //                       it writes a partial sum for the second pass.
 //   finish_streamk      second pass for the tiled kernel: sums the partials
 //                       of split i-blocks in CTA (= j) order and finishes.
-//   force_pairs<KI,NT,TJ>
+//   force_pairs<KI,NT,TJ,NB,UNRB>
 //                       the tiled kernel with each pair of bodies in
 //                       different i-blocks evaluated once (Newton's third
 //                       law): action on the targets in registers, reaction on
@@ -555,8 +555,8 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
 // that order; the (I, t) units are numbered block by block and divided
 // evenly over one wave of CTAs as in force_tiled.  For a tile past block I
 // the reaction on its TJ sources is reduced over the CTA's B targets (a warp
-// butterfly that scatters 8 sources over the lanes, then the NW warps in
-// order through shared memory) and stored as that unit's partial; the
+// butterfly that scatters a batch of NB sources over the lanes, then the NW
+// warps in order through shared memory) and stored as that unit's partial; the
 // second pass adds, for each body, its action and the reactions from the
 // blocks before its own in block order.
 
@@ -607,38 +607,39 @@ __device__ __forceinline__ void interact2_pair(float2 X, float2 Y, float2 Z, flo
   bz = __ffma2_rn(rz, sj, bz);
 }
 
-// Sum v[0..7] (one value per source of a batch of 8) over the 32 lanes of the
-// warp and leave source l >> 2's total in lane l: each butterfly level halves
-// the values a lane keeps (8, 4, 2, 1), the last two levels sum the one left.
-// 27 shuffles and 27 adds for 8 sources x 3 components.
-__device__ __forceinline__ float3 reduce_scatter8(const float (&vx)[8], const float (&vy)[8],
-                                                  const float (&vz)[8], int lane) {
-  const bool h = (lane >> 4) & 1, g = (lane >> 3) & 1, f = (lane >> 2) & 1;
+// Sum v[0..NB) (one value per source of a batch of NB = 8 or 16) over the 32
+// lanes of the warp, leaving source (lane >> (5 - log2 NB))'s total in that
+// lane: each butterfly level halves the values a lane keeps (the lanes with
+// the level's mask bit keep the upper half), then the remaining levels sum
+// the one value left.  3 * (NB - 1 + 5 - log2 NB) shuffles and as many adds.
+template <int NB>
+__device__ __forceinline__ float3 reduce_scatter(float (&vx)[NB], float (&vy)[NB],
+                                                 float (&vz)[NB], int lane) {
+  static_assert(NB == 8 || NB == 16, "batches of 8 or 16 sources");
   constexpr unsigned kAll = 0xffffffffu;
-  float wx[4], wy[4], wz[4];
+  constexpr int kLevels = NB == 8 ? 3 : 4;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    wx[q] = (h ? vx[q + 4] : vx[q]) + __shfl_xor_sync(kAll, h ? vx[q] : vx[q + 4], 16);
-    wy[q] = (h ? vy[q + 4] : vy[q]) + __shfl_xor_sync(kAll, h ? vy[q] : vy[q + 4], 16);
-    wz[q] = (h ? vz[q + 4] : vz[q]) + __shfl_xor_sync(kAll, h ? vz[q] : vz[q + 4], 16);
-  }
-  float ux[2], uy[2], uz[2];
+  for (int level = 0; level < kLevels; ++level) {
+    const int half = (NB >> level) >> 1;
+    const int m = 16 >> level;
+    const bool up = (lane & m) != 0;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    ux[q] = (g ? wx[q + 2] : wx[q]) + __shfl_xor_sync(kAll, g ? wx[q] : wx[q + 2], 8);
-    uy[q] = (g ? wy[q + 2] : wy[q]) + __shfl_xor_sync(kAll, g ? wy[q] : wy[q + 2], 8);
-    uz[q] = (g ? wz[q + 2] : wz[q]) + __shfl_xor_sync(kAll, g ? wz[q] : wz[q + 2], 8);
+    for (int q = 0; q < half; ++q) {
+      const float kx = up ? vx[q + half] : vx[q], sx = up ? vx[q] : vx[q + half];
+      const float ky = up ? vy[q + half] : vy[q], sy = up ? vy[q] : vy[q + half];
+      const float kz = up ? vz[q + half] : vz[q], sz = up ? vz[q] : vz[q + half];
+      vx[q] = kx + __shfl_xor_sync(kAll, sx, m);
+      vy[q] = ky + __shfl_xor_sync(kAll, sy, m);
+      vz[q] = kz + __shfl_xor_sync(kAll, sz, m);
+    }
   }
-  float x = (f ? ux[1] : ux[0]) + __shfl_xor_sync(kAll, f ? ux[0] : ux[1], 4);
-  float y = (f ? uy[1] : uy[0]) + __shfl_xor_sync(kAll, f ? uy[0] : uy[1], 4);
-  float z = (f ? uz[1] : uz[0]) + __shfl_xor_sync(kAll, f ? uz[0] : uz[1], 4);
-  x += __shfl_xor_sync(kAll, x, 2);
-  y += __shfl_xor_sync(kAll, y, 2);
-  z += __shfl_xor_sync(kAll, z, 2);
-  x += __shfl_xor_sync(kAll, x, 1);
-  y += __shfl_xor_sync(kAll, y, 1);
-  z += __shfl_xor_sync(kAll, z, 1);
-  return make_float3(x, y, z);
+#pragma unroll
+  for (int m = 16 >> kLevels; m >= 1; m >>= 1) {
+    vx[0] += __shfl_xor_sync(kAll, vx[0], m);
+    vy[0] += __shfl_xor_sync(kAll, vy[0], m);
+    vz[0] += __shfl_xor_sync(kAll, vz[0], m);
+  }
+  return make_float3(vx[0], vy[0], vz[0]);
 }
 
 // Dynamic shared memory of force_pairs: the per-warp reaction sums of a tile.
@@ -646,10 +647,11 @@ __host__ __device__ constexpr size_t pair_reduce_smem(int nt, int tj) {
   return static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float);
 }
 
-template <int KI, int NT, int TJ>
+template <int KI, int NT, int TJ, int NB, int UNRB>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
-  static_assert((KI * NT) % TJ == 0 && TJ % 8 == 0, "tiles tile an i-block; batches tile a tile");
+  static_assert((KI * NT) % TJ == 0 && TJ % NB == 0, "tiles tile an i-block; batches tile a tile");
+  constexpr int kShift = NB == 8 ? 2 : 1;  // lane l holds source l >> kShift of a batch
   constexpr int P = KI / 2;
   constexpr int NW = NT / 32;
   constexpr long long B = static_cast<long long>(KI) * NT;
@@ -767,11 +769,11 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
                       make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
         }
       } else {
-#pragma unroll 1
-        for (int b0 = 0; b0 < TJ; b0 += 8) {
-          float vx[8], vy[8], vz[8];
+#pragma unroll UNRB
+        for (int b0 = 0; b0 < TJ; b0 += NB) {
+          float vx[NB], vy[NB], vz[NB];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < NB; ++q) {
             const float4 lo = src[2 * (b0 + q)];
             const float4 hi = src[2 * (b0 + q) + 1];
             float2 bx = make_float2(0.f, 0.f), by = bx, bz = bx;
@@ -784,11 +786,11 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             vy[q] = by.x + by.y;
             vz[q] = bz.x + bz.y;
           }
-          const float3 r = reduce_scatter8(vx, vy, vz, lane);
-          if ((lane & 3) == 0) {
-            red[warp][0][b0 + (lane >> 2)] = r.x;
-            red[warp][1][b0 + (lane >> 2)] = r.y;
-            red[warp][2][b0 + (lane >> 2)] = r.z;
+          const float3 r = reduce_scatter<NB>(vx, vy, vz, lane);
+          if ((lane & ((1 << kShift) - 1)) == 0) {
+            red[warp][0][b0 + (lane >> kShift)] = r.x;
+            red[warp][1][b0 + (lane >> kShift)] = r.y;
+            red[warp][2][b0 + (lane >> kShift)] = r.z;
           }
         }
         __syncthreads();

@@ -257,7 +257,7 @@ def test_plan_pairs_path(monkeypatch):
     assert nb.plan(65537)["path"] == nb.PATH_SPLIT
 
 
-N_PAIR_VARIANTS = 5
+N_PAIR_VARIANTS = 11
 
 
 @pytest.mark.parametrize("cfg", range(N_PAIR_VARIANTS))
@@ -271,10 +271,10 @@ def test_every_pair_variant(cfg, monkeypatch):
     assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
 
 
-# block edges of the default pair shape (2560 targets, 512-source tiles):
+# block edges of the pair shapes (2048 or 2560 targets, 512-source tiles):
 # one block, a block and one body, ragged tiles, several blocks
-@pytest.mark.parametrize("n", [511, 512, 513, 2559, 2560, 2561, 5119, 5120, 5121, 7681,
-                               12800, 12801, 30001])
+@pytest.mark.parametrize("n", [511, 512, 513, 2047, 2048, 2049, 2559, 2560, 2561, 4095, 4096,
+                               4097, 5121, 6145, 7681, 12801, 30001])
 def test_pair_path_block_edges(n):
     pm = W.random_bodies(n, 4000 + n)
     a = gpu_accel(pm, 1e-3, path=4)
