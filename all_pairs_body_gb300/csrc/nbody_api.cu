@@ -77,6 +77,7 @@ struct PairConfig {
 // template: + sources per reduction batch, batch-loop unroll); the first is
 // the default.
 const PairConfig kPairs[] = {
+    {12, 256, 512, force_pairs<12, 256, 512, 16, 1>},
     {10, 256, 512, force_pairs<10, 256, 512, 16, 1>},
     {10, 256, 512, force_pairs<10, 256, 512, 8, 1>},
     {8, 256, 512, force_pairs<8, 256, 512, 8, 1>},
@@ -88,12 +89,19 @@ const PairConfig kPairs[] = {
     {6, 256, 512, force_pairs<6, 256, 512, 16, 1>},
     {8, 256, 256, force_pairs<8, 256, 256, 16, 1>},
     {6, 256, 512, force_pairs<6, 256, 512, 8, 2>},
+    {10, 256, 640, force_pairs<10, 256, 640, 16, 1>},
+    {10, 256, 320, force_pairs<10, 256, 320, 16, 1>},
+    {12, 256, 384, force_pairs<12, 256, 384, 16, 1>},
+    {14, 256, 512, force_pairs<14, 256, 512, 16, 1>},
+    {12, 256, 512, force_pairs<12, 256, 512, 8, 1>},
+    {16, 256, 512, force_pairs<16, 256, 512, 16, 1>},
+    {12, 256, 256, force_pairs<12, 256, 256, 16, 1>},
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
 // The automatic plan takes the pair path while its reaction partials stay
 // within this many bytes (units * tile * 16: about 16 N^2 / (2 B) for B
-// targets per i-block, 3.4 GB at N = 2^20 and B = 2560);
+// targets per i-block, 2.9 GB at N = 2^20 and B = 3072);
 // NBODY_PAIRS_MAX_BYTES overrides it.
 constexpr long long kPairsMaxBytes = 16LL << 30;
 
@@ -300,13 +308,44 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
   p->second_pass = p->slices > 1;
 }
 
-int pair_config() {
+// Pair shapes the plan chooses between, with their speed per interaction
+// relative to the first, measured at n = 2^20 (force kernel 283.5, 288.7 and
+// 295.8 ms): more targets per CTA are faster per interaction; fewer cut the
+// work into more units, which wins when a CTA's share of units is small.
+constexpr LargeShape kPairShapes[] = {{0, 1.0}, {1, 0.982}, {7, 0.959}};
+
+long long pair_units_of(long long n, const PairConfig& pc) {
+  const long long block = static_cast<long long>(pc.ki) * pc.nt;
+  return pair_units_before(ceil_div(n, block), ceil_div(n, pc.tj), block / pc.tj);
+}
+
+long long pair_grid(long long units, const DeviceInfo& d, int cfg) {
+  const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.pair_occupancy[cfg]);
+  return std::min(units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+}
+
+// The stream-K time model of choose_large_shape for the pair kernel: the
+// slowest CTA runs ceil(units / grid) units of B x TJ pairs each.
+int pair_config(long long n, const DeviceInfo& d) {
   const long long forced = env_int("NBODY_PAIRS_CONFIG", -1);
-  return forced >= 0 && forced < kNumPairs ? static_cast<int>(forced) : 0;
+  if (forced >= 0 && forced < kNumPairs) return static_cast<int>(forced);
+  int best = -1;
+  double best_cost = 0.0;
+  for (const LargeShape& s : kPairShapes) {
+    const PairConfig& pc = kPairs[s.cfg];
+    const long long units = pair_units_of(n, pc);
+    const double cost = static_cast<double>(ceil_div(units, pair_grid(units, d, s.cfg))) *
+                        pc.ki * pc.nt * pc.tj / s.speed;
+    if (best < 0 || cost < best_cost) {  // ties keep the earlier (faster) shape
+      best = s.cfg;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 void plan_pairs(long long n, const DeviceInfo& d, Plan* p) {
-  p->cfg = pair_config();
+  p->cfg = pair_config(n, d);
   const PairConfig& pc = kPairs[p->cfg];
   p->threads = pc.nt;
   p->block = static_cast<long long>(pc.ki) * pc.nt;
@@ -314,26 +353,22 @@ void plan_pairs(long long n, const DeviceInfo& d, Plan* p) {
   p->ntiles = ceil_div(n, pc.tj);
   p->nblocks = ceil_div(n, p->block);
   p->units = pair_units_before(p->nblocks, p->ntiles, p->block / pc.tj);
-  const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.pair_occupancy[p->cfg]);
-  p->grid = std::min(p->units, static_cast<long long>(d.sms) * std::max(1LL, per_sm));
+  p->grid = pair_grid(p->units, d, p->cfg);
   p->second_pass = true;  // reactions always come from other CTAs
 }
 
 // Reaction-partial bytes of the pair path's plan over n bodies.
-long long pair_react_bytes(long long n) {
-  const PairConfig& pc = kPairs[pair_config()];
-  const long long block = static_cast<long long>(pc.ki) * pc.nt;
-  const long long ntiles = ceil_div(n, pc.tj);
-  return pair_units_before(ceil_div(n, block), ntiles, block / pc.tj) * pc.tj *
-         static_cast<long long>(sizeof(float4));
+long long pair_react_bytes(long long n, const DeviceInfo& d) {
+  const PairConfig& pc = kPairs[pair_config(n, d)];
+  return pair_units_of(n, pc) * pc.tj * static_cast<long long>(sizeof(float4));
 }
 
 // AUTO: the warp kernel up to kWarpMaxN; above it the pair path while its
 // reaction partials fit kPairsMaxBytes, else the one-sided stream-K kernel.
-int auto_path(long long n) {
+int auto_path(long long n, const DeviceInfo& d) {
   if (n <= kWarpMaxN) return NBODY_PATH_WARP;
   const long long cap = env_int("NBODY_PAIRS_MAX_BYTES", kPairsMaxBytes);
-  return pair_react_bytes(n) <= cap ? NBODY_PATH_PAIRS : NBODY_PATH_SPLIT;
+  return pair_react_bytes(n, d) <= cap ? NBODY_PATH_PAIRS : NBODY_PATH_SPLIT;
 }
 
 int make_plan(long long n, int path, int split, int dev, Plan* p) {
@@ -343,7 +378,7 @@ int make_plan(long long n, int path, int split, int dev, Plan* p) {
   *p = Plan();
   p->sms = d.sms;
   int resolved = path;
-  if (resolved == NBODY_PATH_AUTO) resolved = auto_path(n);
+  if (resolved == NBODY_PATH_AUTO) resolved = auto_path(n, d);
   p->path = resolved;
   if (resolved == NBODY_PATH_WARP)
     plan_warp(n, split, d, p);

@@ -234,30 +234,44 @@ def test_plan_shape_follows_streamk_model():
                 for n in (32768, 49152, 65537, 81920, 1048576)] == [256, 512, 256, 512, 512]
 
 
-def pair_units(n, block=2560, tj=512):
+def pair_units(n, block, tj=512):
     """Units of the pair path: block I meets the tiles of itself and of every
     later block."""
     nb_, nt = -(-n // block), -(-n // tj)
     return sum(nt - (block // tj) * i for i in range(nb_))
 
 
+PAIR_SHAPES = ((3072, 1.0), (2560, 0.982), (2048, 0.959))  # targets per CTA, speed
+
+
 def test_plan_pairs_path(monkeypatch):
+    """Above the warp kernel the pair path, with the shape whose slowest CTA
+    has the least work: ceil(units / grid) units of B x 512 pairs at the
+    shape's relative speed."""
     import all_pairs_body_gb300 as nb
     assert nb.plan(24576)["path"] == nb.PATH_WARP
-    for n in (24577, 65537, 1048576):
+    for n in list(range(24577, 140000, 5003)) + [262144, 1048576, 2000000]:
         p = nb.plan(n)
         assert p["path"] == nb.PATH_PAIRS and p["second_pass"] == 1
-        assert p["bodies_per_cta"] == 2560 and p["tile"] == 512
-        assert p["units"] == pair_units(n)
+        cost = []
+        for block, speed in PAIR_SHAPES:
+            units = pair_units(n, block)
+            cost.append(-(-units // min(units, p["sms"])) * block * 512 / speed)
+        block = PAIR_SHAPES[cost.index(min(cost))][0]
+        assert p["bodies_per_cta"] == block and p["tile"] == 512, (n, cost, p)
+        assert p["units"] == pair_units(n, block)
         assert p["grid"] == min(p["units"], p["sms"])
         assert p["launches_accel"] == 2
-    # 4M bodies need ~55 GB of reaction sums: the one-sided plan instead
+    if nb.plan(32768)["sms"] == 152:
+        assert nb.plan(1048576)["bodies_per_cta"] == 3072
+        assert nb.plan(24577)["bodies_per_cta"] == 2560
+    # 4M bodies need ~46 GB of reaction sums: the one-sided plan instead
     assert nb.plan(4194304)["path"] == nb.PATH_SPLIT
     monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", "1000")
     assert nb.plan(65537)["path"] == nb.PATH_SPLIT
 
 
-N_PAIR_VARIANTS = 11
+N_PAIR_VARIANTS = 19
 
 
 @pytest.mark.parametrize("cfg", range(N_PAIR_VARIANTS))
@@ -271,10 +285,10 @@ def test_every_pair_variant(cfg, monkeypatch):
     assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
 
 
-# block edges of the pair shapes (2048 or 2560 targets, 512-source tiles):
+# block edges of the pair shapes (2048, 2560 or 3072 targets, 512-source tiles):
 # one block, a block and one body, ragged tiles, several blocks
-@pytest.mark.parametrize("n", [511, 512, 513, 2047, 2048, 2049, 2559, 2560, 2561, 4095, 4096,
-                               4097, 5121, 6145, 7681, 12801, 30001])
+@pytest.mark.parametrize("n", [511, 512, 513, 2047, 2048, 2049, 2559, 2560, 2561, 3071, 3072,
+                               3073, 4095, 4096, 4097, 5121, 6145, 7681, 9217, 12801, 30001])
 def test_pair_path_block_edges(n):
     pm = W.random_bodies(n, 4000 + n)
     a = gpu_accel(pm, 1e-3, path=4)
