@@ -25,9 +25,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per tile copy: only a f
 constexpr int kFinishThreads = 256;
 constexpr int kWarpKW = 4;  // targets per CTA of the small-n kernel (sweep: 4 beats 6-16)
 constexpr int kWarpNW = 4;
-// AUTO uses the warp kernel (one j slice: no second pass) up to this n, the
-// large tiled shape above it; both thresholds from a latency sweep over n.
+// Forced one-sided TILED/SPLIT passes use the smallest tiled blocks up to this
+// n, the large shapes above it (latency sweep over n).
 constexpr long long kWarpMaxN = 24576;
+// AUTO uses the warp kernel (one launch, one j slice) below this n and the
+// pair kernel from it on: the pair path's floor is one unit of work per CTA
+// (~110 us), which the warp kernel's time passes at about this size
+// (measured over n = 6144 ... 24576).
+constexpr long long kPairsMinN = 16384;
 
 using TiledKernel = void (*)(const TiledArgs, const Epilogue);
 
@@ -309,10 +314,11 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
 }
 
 // Pair shapes the plan chooses between, with their speed per interaction
-// relative to the first, measured at n = 2^20 (force kernel 283.5, 288.7 and
-// 295.8 ms): more targets per CTA are faster per interaction; fewer cut the
-// work into more units, which wins when a CTA's share of units is small.
-constexpr LargeShape kPairShapes[] = {{0, 1.0}, {1, 0.982}, {7, 0.959}};
+// relative to the first, measured at n = 2^20 (force kernel 283.5, 288.7,
+// 295.8 and 297.3 ms): more targets per CTA and longer tiles are faster per
+// interaction; smaller ones cut the work into more units, which wins when a
+// CTA's share of units is small.
+constexpr LargeShape kPairShapes[] = {{0, 1.0}, {1, 0.982}, {7, 0.959}, {10, 0.954}};
 
 long long pair_units_of(long long n, const PairConfig& pc) {
   const long long block = static_cast<long long>(pc.ki) * pc.nt;
@@ -363,10 +369,10 @@ long long pair_react_bytes(long long n, const DeviceInfo& d) {
   return pair_units_of(n, pc) * pc.tj * static_cast<long long>(sizeof(float4));
 }
 
-// AUTO: the warp kernel up to kWarpMaxN; above it the pair path while its
+// AUTO: the warp kernel below kPairsMinN; from it the pair path while its
 // reaction partials fit kPairsMaxBytes, else the one-sided stream-K kernel.
 int auto_path(long long n, const DeviceInfo& d) {
-  if (n <= kWarpMaxN) return NBODY_PATH_WARP;
+  if (n < kPairsMinN) return NBODY_PATH_WARP;
   const long long cap = env_int("NBODY_PAIRS_MAX_BYTES", kPairsMaxBytes);
   return pair_react_bytes(n, d) <= cap ? NBODY_PATH_PAIRS : NBODY_PATH_SPLIT;
 }

@@ -241,25 +241,26 @@ def pair_units(n, block, tj=512):
     return sum(nt - (block // tj) * i for i in range(nb_))
 
 
-PAIR_SHAPES = ((3072, 1.0), (2560, 0.982), (2048, 0.959))  # targets per CTA, speed
+PAIR_SHAPES = ((3072, 512, 1.0), (2560, 512, 0.982), (2048, 512, 0.959),
+               (2048, 256, 0.954))  # targets per CTA, tile, speed
 
 
 def test_plan_pairs_path(monkeypatch):
     """Above the warp kernel the pair path, with the shape whose slowest CTA
-    has the least work: ceil(units / grid) units of B x 512 pairs at the
+    has the least work: ceil(units / grid) units of B x TJ pairs at the
     shape's relative speed."""
     import all_pairs_body_gb300 as nb
-    assert nb.plan(24576)["path"] == nb.PATH_WARP
-    for n in list(range(24577, 140000, 5003)) + [262144, 1048576, 2000000]:
+    assert nb.plan(16383)["path"] == nb.PATH_WARP
+    for n in list(range(16384, 140000, 5003)) + [262144, 1048576, 2000000]:
         p = nb.plan(n)
         assert p["path"] == nb.PATH_PAIRS and p["second_pass"] == 1
         cost = []
-        for block, speed in PAIR_SHAPES:
-            units = pair_units(n, block)
-            cost.append(-(-units // min(units, p["sms"])) * block * 512 / speed)
-        block = PAIR_SHAPES[cost.index(min(cost))][0]
-        assert p["bodies_per_cta"] == block and p["tile"] == 512, (n, cost, p)
-        assert p["units"] == pair_units(n, block)
+        for block, tj, speed in PAIR_SHAPES:
+            units = pair_units(n, block, tj)
+            cost.append(-(-units // min(units, p["sms"])) * block * tj / speed)
+        block, tj, _ = PAIR_SHAPES[cost.index(min(cost))]
+        assert p["bodies_per_cta"] == block and p["tile"] == tj, (n, cost, p)
+        assert p["units"] == pair_units(n, block, tj)
         assert p["grid"] == min(p["units"], p["sms"])
         assert p["launches_accel"] == 2
     if nb.plan(32768)["sms"] == 152:
