@@ -75,38 +75,43 @@ using PairKernel = void (*)(const PairArgs);
 struct PairConfig {
   int ki, nt, tj;
   PairKernel kernel;
-  size_t smem() const { return pair_reduce_smem(nt, tj); }  // dynamic shared memory
+  int acc;  // running sums in shared memory (the kernel's ACC)
+  size_t smem() const { return pair_reduce_smem(ki, nt, tj, acc); }  // dynamic shared memory
 };
 
 // Shapes of the pair-symmetric kernel (targets per thread, threads, tile;
-// template: + sources per reduction batch, batch-loop unroll); the first is
-// the default.
+// template: + sources per reduction batch, batch-loop unroll, running sums
+// in shared memory); the first is the default.
 const PairConfig kPairs[] = {
-    {12, 256, 512, force_pairs<12, 256, 512, 16, 1>},
-    {10, 256, 512, force_pairs<10, 256, 512, 16, 1>},
-    {10, 256, 512, force_pairs<10, 256, 512, 8, 1>},
-    {8, 256, 512, force_pairs<8, 256, 512, 8, 1>},
-    {8, 256, 256, force_pairs<8, 256, 256, 8, 1>},
-    {10, 256, 256, force_pairs<10, 256, 256, 8, 1>},
-    {8, 256, 128, force_pairs<8, 256, 128, 8, 1>},
-    {8, 256, 512, force_pairs<8, 256, 512, 16, 1>},
-    {8, 256, 512, force_pairs<8, 256, 512, 8, 2>},
-    {6, 256, 512, force_pairs<6, 256, 512, 16, 1>},
-    {8, 256, 256, force_pairs<8, 256, 256, 16, 1>},
-    {6, 256, 512, force_pairs<6, 256, 512, 8, 2>},
-    {10, 256, 640, force_pairs<10, 256, 640, 16, 1>},
-    {10, 256, 320, force_pairs<10, 256, 320, 16, 1>},
-    {12, 256, 384, force_pairs<12, 256, 384, 16, 1>},
-    {14, 256, 512, force_pairs<14, 256, 512, 16, 1>},
-    {12, 256, 512, force_pairs<12, 256, 512, 8, 1>},
-    {16, 256, 512, force_pairs<16, 256, 512, 16, 1>},
-    {12, 256, 256, force_pairs<12, 256, 256, 16, 1>},
+    {14, 256, 512, force_pairs<14, 256, 512, 16, 1, 1>, 1},
+    {12, 256, 512, force_pairs<12, 256, 512, 16, 1>, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 16, 1>, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 8, 1>, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 1>, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 8, 1>, 0},
+    {10, 256, 256, force_pairs<10, 256, 256, 8, 1>, 0},
+    {8, 256, 128, force_pairs<8, 256, 128, 8, 1>, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 16, 1>, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 2>, 0},
+    {6, 256, 512, force_pairs<6, 256, 512, 16, 1>, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 16, 1>, 0},
+    {6, 256, 512, force_pairs<6, 256, 512, 8, 2>, 0},
+    {10, 256, 640, force_pairs<10, 256, 640, 16, 1>, 0},
+    {10, 256, 320, force_pairs<10, 256, 320, 16, 1>, 0},
+    {12, 256, 384, force_pairs<12, 256, 384, 16, 1>, 0},
+    {14, 256, 512, force_pairs<14, 256, 512, 16, 1>, 0},
+    {12, 256, 512, force_pairs<12, 256, 512, 8, 1>, 0},
+    {16, 256, 512, force_pairs<16, 256, 512, 16, 1>, 0},
+    {12, 256, 256, force_pairs<12, 256, 256, 16, 1>, 0},
+    {12, 256, 512, force_pairs<12, 256, 512, 16, 1, 1>, 1},
+    {16, 256, 512, force_pairs<16, 256, 512, 16, 1, 1>, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 16, 1, 1>, 1},
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
 // The automatic plan takes the pair path while its reaction partials stay
 // within this many bytes (units * tile * 16: about 16 N^2 / (2 B) for B
-// targets per i-block, 2.9 GB at N = 2^20 and B = 3072);
+// targets per i-block, 2.5 GB at N = 2^20 and B = 3584);
 // NBODY_PAIRS_MAX_BYTES overrides it.
 constexpr long long kPairsMaxBytes = 16LL << 30;
 
@@ -314,11 +319,13 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
 }
 
 // Pair shapes the plan chooses between, with their speed per interaction
-// relative to the first, measured at n = 2^20 (force kernel 283.5, 288.7,
-// 295.8 and 297.3 ms): more targets per CTA and longer tiles are faster per
+// relative to the first, measured at n = 2^20 (force kernel 281.5, 284.2,
+// 288.7, 295.8 and 297.3 ms, the last three scaled from a build where the
+// second took 283.5): more targets per CTA and longer tiles are faster per
 // interaction; smaller ones cut the work into more units, which wins when a
 // CTA's share of units is small.
-constexpr LargeShape kPairShapes[] = {{0, 1.0}, {1, 0.982}, {7, 0.959}, {10, 0.954}};
+constexpr LargeShape kPairShapes[] = {
+    {0, 1.0}, {1, 0.990}, {2, 0.973}, {8, 0.950}, {11, 0.945}};
 
 long long pair_units_of(long long n, const PairConfig& pc) {
   const long long block = static_cast<long long>(pc.ki) * pc.nt;

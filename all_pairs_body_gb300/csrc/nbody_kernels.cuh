@@ -19,7 +19,7 @@
 //                       it writes a partial sum for the second pass.
 //   finish_streamk      second pass for the tiled kernel: sums the partials
 //                       of split i-blocks in CTA (= j) order and finishes.
-//   force_pairs<KI,NT,TJ,NB,UNRB>
+//   force_pairs<KI,NT,TJ,NB,UNRB,ACC>
 //                       the tiled kernel with each pair of bodies in
 //                       different i-blocks evaluated once (Newton's third
 //                       law): action on the targets in registers, reaction on
@@ -642,12 +642,18 @@ __device__ __forceinline__ float3 reduce_scatter(float (&vx)[NB], float (&vy)[NB
   return make_float3(vx[0], vy[0], vz[0]);
 }
 
-// Dynamic shared memory of force_pairs: the per-warp reaction sums of a tile.
-__host__ __device__ constexpr size_t pair_reduce_smem(int nt, int tj) {
-  return static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float);
+// Dynamic shared memory of force_pairs: the per-warp reaction sums of a tile,
+// and with ACC = 1 the targets' running action sums.
+__host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, int acc) {
+  return static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float) +
+         (acc ? static_cast<size_t>(3) * ki * nt * sizeof(float) : 0);
 }
 
-template <int KI, int NT, int TJ, int NB, int UNRB>
+// ACC = 0: the running action sums of a segment live in registers beside the
+// per-tile sums.  ACC = 1: they live in shared memory ([3][KI/2][NT] float2,
+// one column per thread) and are touched once per tile, when the per-tile sums
+// are folded in, which leaves 3 KI registers to the inner loop.
+template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   static_assert((KI * NT) % TJ == 0 && TJ % NB == 0, "tiles tile an i-block; batches tile a tile");
@@ -660,8 +666,10 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   __shared__ __align__(128) float4 raw[2][TJ];    // TMA targets: the caller's rows
   __shared__ __align__(128) float4 tile[2 * TJ];  // expanded: (x,x,y,y),(z,z,m,m)
   __shared__ __align__(8) unsigned long long bar[2];
-  extern __shared__ __align__(16) float react_smem[];  // [NW][3][TJ]
+  extern __shared__ __align__(16) float react_smem[];  // [NW][3][TJ] (+ running sums)
   auto red = reinterpret_cast<float(*)[3][TJ]>(react_smem);
+  float2* const acc_s = reinterpret_cast<float2*>(react_smem + NW * 3 * TJ);  // ACC = 1
+  auto acc_at = [&](int c, int p) -> float2& { return acc_s[(c * P + p) * NT + threadIdx.x]; };
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -737,7 +745,11 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
       nz[p] = make_float2(-q0.z, -q1.z);
       // targets past n exert no reaction
       nm[p] = make_float2(i0 < a.n ? -q0.w : 0.f, i1 < a.n ? -q1.w : 0.f);
-      ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+      if constexpr (ACC == 1) {
+        acc_at(0, p) = acc_at(1, p) = acc_at(2, p) = make_float2(0.f, 0.f);
+      } else {
+        ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+      }
     }
 
     for (; t < te; ++t, ++k) {
@@ -809,9 +821,15 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
       }
 #pragma unroll
       for (int p = 0; p < P; ++p) {
-        ax[p] = __fadd2_rn(ax[p], tx[p]);
-        ay[p] = __fadd2_rn(ay[p], ty[p]);
-        az[p] = __fadd2_rn(az[p], tz[p]);
+        if constexpr (ACC == 1) {
+          acc_at(0, p) = __fadd2_rn(acc_at(0, p), tx[p]);
+          acc_at(1, p) = __fadd2_rn(acc_at(1, p), ty[p]);
+          acc_at(2, p) = __fadd2_rn(acc_at(2, p), tz[p]);
+        } else {
+          ax[p] = __fadd2_rn(ax[p], tx[p]);
+          ay[p] = __fadd2_rn(ay[p], ty[p]);
+          az[p] = __fadd2_rn(az[p], tz[p]);
+        }
       }
     }
     if (timed_out) break;
@@ -825,8 +843,18 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
         const long long local = (2 * p + h) * NT + tid;
         const long long i = blk * B + local;
         if (i < a.n) {
-          const float4 v = make_float4(h ? ax[p].y : ax[p].x, h ? ay[p].y : ay[p].x,
-                                       h ? az[p].y : az[p].x, 0.f);
+          float2 sx2, sy2, sz2;
+          if constexpr (ACC == 1) {
+            sx2 = acc_at(0, p);
+            sy2 = acc_at(1, p);
+            sz2 = acc_at(2, p);
+          } else {
+            sx2 = ax[p];
+            sy2 = ay[p];
+            sz2 = az[p];
+          }
+          const float4 v = make_float4(h ? sx2.y : sx2.x, h ? sy2.y : sy2.x,
+                                       h ? sz2.y : sz2.x, 0.f);
           if (whole)
             a.act[i] = v;
           else

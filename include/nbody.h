@@ -98,7 +98,7 @@ typedef enum nbody_path {
        of the FP32 work of the one-sided paths.  The reactions on a tile's
        sources are summed over the CTA's targets in fixed order and stored
        per (i-block, tile) unit; the second pass adds them to the action in
-       block order.  Scratch: about n^2 / 384 bytes of reaction sums (2.9 GB
+       block order.  Scratch: about n^2 / 448 bytes of reaction sums (2.5 GB
        at n = 2^20).  AUTO takes this path above the warp kernel's range
        while that scratch is at most 16 GiB (or NBODY_PAIRS_MAX_BYTES), and
        falls back to NBODY_PATH_SPLIT's plan if it cannot be allocated. */

@@ -241,8 +241,8 @@ def pair_units(n, block, tj=512):
     return sum(nt - (block // tj) * i for i in range(nb_))
 
 
-PAIR_SHAPES = ((3072, 512, 1.0), (2560, 512, 0.982), (2048, 512, 0.959),
-               (2048, 256, 0.954))  # targets per CTA, tile, speed
+PAIR_SHAPES = ((3584, 512, 1.0), (3072, 512, 0.990), (2560, 512, 0.973), (2048, 512, 0.950),
+               (2048, 256, 0.945))  # targets per CTA, tile, speed
 
 
 def test_plan_pairs_path(monkeypatch):
@@ -264,15 +264,14 @@ def test_plan_pairs_path(monkeypatch):
         assert p["grid"] == min(p["units"], p["sms"])
         assert p["launches_accel"] == 2
     if nb.plan(32768)["sms"] == 152:
-        assert nb.plan(1048576)["bodies_per_cta"] == 3072
-        assert nb.plan(24577)["bodies_per_cta"] == 2560
+        assert nb.plan(1048576)["bodies_per_cta"] == 3584
     # 4M bodies need ~46 GB of reaction sums: the one-sided plan instead
     assert nb.plan(4194304)["path"] == nb.PATH_SPLIT
     monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", "1000")
     assert nb.plan(65537)["path"] == nb.PATH_SPLIT
 
 
-N_PAIR_VARIANTS = 19
+N_PAIR_VARIANTS = 23
 
 
 @pytest.mark.parametrize("cfg", range(N_PAIR_VARIANTS))
@@ -286,10 +285,11 @@ def test_every_pair_variant(cfg, monkeypatch):
     assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
 
 
-# block edges of the pair shapes (2048, 2560 or 3072 targets, 512-source tiles):
-# one block, a block and one body, ragged tiles, several blocks
+# block edges of the pair shapes (2048, 2560, 3072 or 3584 targets, 512-source
+# tiles): one block, a block and one body, ragged tiles, several blocks
 @pytest.mark.parametrize("n", [511, 512, 513, 2047, 2048, 2049, 2559, 2560, 2561, 3071, 3072,
-                               3073, 4095, 4096, 4097, 5121, 6145, 7681, 9217, 12801, 30001])
+                               3073, 3583, 3584, 3585, 4095, 4096, 4097, 5121, 6145, 7169,
+                               7681, 9217, 12801, 30001])
 def test_pair_path_block_edges(n):
     pm = W.random_bodies(n, 4000 + n)
     a = gpu_accel(pm, 1e-3, path=4)
