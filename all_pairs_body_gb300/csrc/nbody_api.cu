@@ -5,6 +5,7 @@
 // of nbody_kernels.cuh.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -109,11 +110,13 @@ const PairConfig kPairs[] = {
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
-// The automatic plan takes the pair path while its reaction partials stay
-// within this many bytes (units * tile * 16: about 16 N^2 / (2 B) for B
-// targets per i-block, 2.5 GB at N = 2^20 and B = 3584);
+// The pair path keeps one reaction row of TJ float4 per unit; all of them
+// come to about 16 N^2 / (2 B) bytes for B targets per i-block (2.5 GB at
+// N = 2^20 and B = 3584).  Where they exceed this many bytes the pass runs
+// in chunks of consecutive i-blocks whose rows fit, each chunk's reactions
+// folded into a per-body accumulator before the next chunk reuses the rows;
 // NBODY_PAIRS_MAX_BYTES overrides it.
-constexpr long long kPairsMaxBytes = 16LL << 30;
+constexpr long long kPairsMaxBytes = 4LL << 30;
 
 struct DeviceInfo {
   int sms = 0;
@@ -133,6 +136,11 @@ struct Plan {
   int slices = 1;  // warp path
   long long slice_len = 0;
   int sms = 0;
+  // pair path: chunks of i-blocks, chunk k = [chunk_start[k], chunk_start[k+1])
+  std::vector<long long> chunk_start;
+  long long grid_max = 0;     // CTAs of a full wave (each chunk: min(its units, this))
+  long long chunk_units = 0;  // units of the largest chunk
+  int chunks() const { return chunk_start.empty() ? 1 : static_cast<int>(chunk_start.size()) - 1; }
 };
 
 struct Buf {
@@ -143,6 +151,7 @@ struct Buf {
 struct Scratch {
   Buf pos_alt, partial;
   Buf act, react;  // pair path: whole-block action sums, per-unit reaction sums
+  Buf pair_acc;    // pair path in chunks: per-body running sums
 };
 
 std::mutex g_mu;
@@ -365,24 +374,34 @@ void plan_pairs(long long n, const DeviceInfo& d, Plan* p) {
   p->tj = pc.tj;
   p->ntiles = ceil_div(n, pc.tj);
   p->nblocks = ceil_div(n, p->block);
-  p->units = pair_units_before(p->nblocks, p->ntiles, p->block / pc.tj);
-  p->grid = pair_grid(p->units, d, p->cfg);
+  const long long tb = p->block / pc.tj;
+  p->units = pair_units_before(p->nblocks, p->ntiles, tb);
+  p->grid_max = pair_grid(LLONG_MAX, d, p->cfg);
+  p->grid = std::min(p->units, p->grid_max);
   p->second_pass = true;  // reactions always come from other CTAs
+  // Chunks: consecutive i-blocks while their reaction rows fit the cap (one
+  // block at least).  Block I has ntiles - TB * I units.
+  const long long row = static_cast<long long>(pc.tj) * static_cast<long long>(sizeof(float4));
+  const long long cap = std::max(row, env_int("NBODY_PAIRS_MAX_BYTES", kPairsMaxBytes));
+  p->chunk_start.assign(1, 0);
+  p->chunk_units = 0;
+  long long acc = 0;
+  for (long long I = 0; I < p->nblocks; ++I) {
+    const long long u = p->ntiles - tb * I;
+    if (acc > 0 && (acc + u) * row > cap) {
+      p->chunk_start.push_back(I);
+      p->chunk_units = std::max(p->chunk_units, acc);
+      acc = 0;
+    }
+    acc += u;
+  }
+  p->chunk_start.push_back(p->nblocks);
+  p->chunk_units = std::max(p->chunk_units, acc);
+  if (p->chunks() == 1) p->chunk_start.clear();
 }
 
-// Reaction-partial bytes of the pair path's plan over n bodies.
-long long pair_react_bytes(long long n, const DeviceInfo& d) {
-  const PairConfig& pc = kPairs[pair_config(n, d)];
-  return pair_units_of(n, pc) * pc.tj * static_cast<long long>(sizeof(float4));
-}
-
-// AUTO: the warp kernel below kPairsMinN; from it the pair path while its
-// reaction partials fit kPairsMaxBytes, else the one-sided stream-K kernel.
-int auto_path(long long n, const DeviceInfo& d) {
-  if (n < kPairsMinN) return NBODY_PATH_WARP;
-  const long long cap = env_int("NBODY_PAIRS_MAX_BYTES", kPairsMaxBytes);
-  return pair_react_bytes(n, d) <= cap ? NBODY_PATH_PAIRS : NBODY_PATH_SPLIT;
-}
+// AUTO: the warp kernel below kPairsMinN, the pair path from it.
+int auto_path(long long n) { return n < kPairsMinN ? NBODY_PATH_WARP : NBODY_PATH_PAIRS; }
 
 int make_plan(long long n, int path, int split, int dev, Plan* p) {
   DeviceInfo d;
@@ -391,7 +410,7 @@ int make_plan(long long n, int path, int split, int dev, Plan* p) {
   *p = Plan();
   p->sms = d.sms;
   int resolved = path;
-  if (resolved == NBODY_PATH_AUTO) resolved = auto_path(n, d);
+  if (resolved == NBODY_PATH_AUTO) resolved = auto_path(n);
   p->path = resolved;
   if (resolved == NBODY_PATH_WARP)
     plan_warp(n, split, d, p);
@@ -402,7 +421,10 @@ int make_plan(long long n, int path, int split, int dev, Plan* p) {
   return NBODY_OK;
 }
 
-int launches_accel(const Plan& p) { return 1 + (p.second_pass ? 1 : 0); }
+int launches_accel(const Plan& p) {
+  if (p.path == NBODY_PATH_PAIRS && p.chunks() > 1) return 2 * p.chunks() + 1;
+  return 1 + (p.second_pass ? 1 : 0);
+}
 
 int launches_step1(const Plan& p) { return launches_accel(p); }
 
@@ -439,8 +461,11 @@ int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapf
   if (p.path == NBODY_PATH_PAIRS) {
     rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
     if (rc == NBODY_OK) rc = ensure(s.act, static_cast<size_t>(n) * sizeof(float4), st);
+    const long long rows = p.chunks() > 1 ? p.chunk_units : p.units;
     if (rc == NBODY_OK)
-      rc = ensure(s.react, static_cast<size_t>(p.units) * p.tj * sizeof(float4), st);
+      rc = ensure(s.react, static_cast<size_t>(rows) * p.tj * sizeof(float4), st);
+    if (rc == NBODY_OK && p.chunks() > 1)
+      rc = ensure(s.pair_acc, static_cast<size_t>(n) * sizeof(float4), st);
   } else if (p.path != NBODY_PATH_WARP) {
     if (p.second_pass)
       rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
@@ -542,21 +567,45 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
   float4* partial = static_cast<float4*>(s.partial.p);
   if (p.path == NBODY_PATH_PAIRS) {
     const PairConfig& pc = kPairs[p.cfg];
-    PairArgs a{pos,     static_cast<int>(n),
-               eps2,    p.ntiles,
-               p.nblocks, p.units,
-               p.grid,  static_cast<float4*>(s.act.p),
-               partial, static_cast<float4*>(s.react.p),
-               kWaitLimitNs, -1};
-    cudaEvent_t e0 = prof_event(st);
-    pc.kernel<<<static_cast<unsigned>(p.grid), p.threads, pc.smem(), st>>>(a);
-    cudaEvent_t e1 = prof_event(st);
-    if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
-    count_launches(2);
-    PairFinishArgs f{a.act, partial, a.react, static_cast<int>(n), p.block, p.tj,
-                     p.ntiles, p.units, p.grid};
-    const long long blocks = ceil_div(n, kFinishThreads);
-    finish_pairs<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(f, epi);
+    const long long tb = p.block / p.tj;
+    float4* act = static_cast<float4*>(s.act.p);
+    float4* react = static_cast<float4*>(s.react.p);
+    // one launch over the i-blocks [I0, I1)
+    auto force_chunk = [&](long long I0, long long I1, long long* u_base, long long* units,
+                           long long* grid) {
+      *u_base = pair_units_before(I0, p.ntiles, tb);
+      *units = pair_units_before(I1, p.ntiles, tb) - *u_base;
+      *grid = std::min(*units, p.grid_max);
+      PairArgs a{pos,    static_cast<int>(n), eps2,    p.ntiles, p.nblocks,    *u_base,
+                 *units, *grid,               act,     partial,  react,        kWaitLimitNs,
+                 -1};
+      cudaEvent_t e0 = prof_event(st);
+      pc.kernel<<<static_cast<unsigned>(*grid), p.threads, pc.smem(), st>>>(a);
+      cudaEvent_t e1 = prof_event(st);
+      if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+    };
+    count_launches(launches_accel(p));
+    long long u_base = 0, units = 0, grid = 0;
+    if (p.chunks() == 1) {
+      force_chunk(0, p.nblocks, &u_base, &units, &grid);
+      PairFinishArgs f{act,  partial, react,  static_cast<int>(n), p.block, p.tj,
+                       p.ntiles, u_base, units, grid, 0, p.nblocks};
+      finish_pairs<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0, st>>>(
+          f, epi);
+      return;
+    }
+    float4* acc = static_cast<float4*>(s.pair_acc.p);
+    for (int k = 0; k < p.chunks(); ++k) {
+      const long long I0 = p.chunk_start[k], I1 = p.chunk_start[k + 1];
+      force_chunk(I0, I1, &u_base, &units, &grid);
+      PairFinishArgs f{act,  partial, react,  static_cast<int>(n), p.block, p.tj,
+                       p.ntiles, u_base, units, grid, I0, I1};
+      const long long bodies = n - I0 * p.block;
+      accumulate_pairs<<<static_cast<unsigned>(ceil_div(bodies, kFinishThreads)), kFinishThreads,
+                         0, st>>>(f, acc, k == 0 ? 1 : 0);
+    }
+    finish_accumulated<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0,
+                         st>>>(acc, static_cast<int>(n), epi);
     return;
   }
   if (p.path == NBODY_PATH_WARP) {
@@ -1015,7 +1064,8 @@ void nbody_release(void) {
       continue;
     }
     cudaDeviceSynchronize();
-    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial, &kv.second.act, &kv.second.react}) {
+    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial, &kv.second.act,
+                          &kv.second.react, &kv.second.pair_acc}) {
       if (b->p != nullptr) cudaFree(b->p);
       b->p = nullptr;
       b->bytes = 0;
@@ -1074,7 +1124,7 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   const int s1 = nbody_sync(cuda_stream);
   if (rc1 == NBODY_OK) rc1 = s1;
 
-  PairArgs pa{buf[0], static_cast<int>(n2), 1.0f, nt2, 2, units2, 1, buf[1], buf[2], buf[3],
+  PairArgs pa{buf[0], static_cast<int>(n2), 1.0f, nt2, 2, 0, units2, 1, buf[1], buf[2], buf[3],
               limit, 0};
   pc.kernel<<<1, pc.nt, pc.smem(), st>>>(pa);
   int rc2 = launch_status();

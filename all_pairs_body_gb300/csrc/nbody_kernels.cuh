@@ -27,6 +27,9 @@
 //                       then warps in order) into one partial per unit.
 //   finish_pairs        its second pass: action + reactions in block order,
 //                       then the finish (accel or kick/drift) of every body.
+//   accumulate_pairs, finish_accumulated
+//                       the same in chunks of i-blocks where the reaction
+//                       sums of all units would not fit the scratch.
 //   force_warp<KW,NW>   small-n kernel: a CTA owns KW targets; its NW*32
 //                       threads stride over one j slice; warp shuffles then
 //                       shared memory (fixed order) combine the threads.
@@ -572,11 +575,12 @@ struct PairArgs {
   float eps2;
   long long ntiles;   // source tiles of TJ bodies over n
   long long nblocks;  // i-blocks of B bodies over n
-  long long units;    // pair_units_before(nblocks)
+  long long u_base;   // first unit of this launch (the first unit of its first i-block)
+  long long units;    // units of this launch, from u_base
   long long grid;     // CTAs launched
   float4* act;        // [n] action sums of i-blocks one CTA covered whole
   float4* partial;    // [grid][2][B] action sums of split i-blocks
-  float4* react;      // [units][TJ] reaction sums of the units past the diagonal
+  float4* react;      // [units][TJ] reaction sums of this launch's units (local index)
   uint64_t timeout_ns;
   long long withhold;  // failure-detection check only (see TiledArgs)
 };
@@ -675,8 +679,8 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long c = blockIdx.x;
-  const long long u_lo = unit_begin(a.units, a.grid, c);
-  const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
+  const long long u_lo = a.u_base + unit_begin(a.units, a.grid, c);  // global unit index
+  const long long count = unit_begin(a.units, a.grid, c + 1) - unit_begin(a.units, a.grid, c);
   const uint32_t bar0 = smem_u32(&bar[0]);
   const uint32_t raw0 = smem_u32(&raw[0][0]);
   constexpr uint32_t kRawStride = sizeof(raw[0]);
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             sy += red[w][1][j];
             sz += red[w][2][j];
           }
-          a.react[u * TJ + j] = make_float4(sx, sy, sz, 0.f);
+          a.react[(u - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
         }
       }
 #pragma unroll
@@ -878,6 +882,14 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
 // Second pass of force_pairs: one thread per body.  a_i = its action (whole
 // or the stream-K partials of its block, in CTA order) + the reactions of
 // its tile from blocks 0 .. I-1 in block order; then finish_body.
+//
+// Where the reaction sums of all units would not fit the scratch, the pass
+// runs in chunks of consecutive i-blocks [I0, I1) (one force_pairs launch
+// each, units numbered from u_base): accumulate_pairs then adds, for every
+// body from block I0 on, its action (if its block is in the chunk) and the
+// reactions from the chunk's blocks before its own to acc[i] (the first
+// chunk stores instead of adding), and finish_accumulated finishes every body
+// from acc.  The order of the additions is fixed by the chunking.
 struct PairFinishArgs {
   const float4* act;
   const float4* partial;
@@ -886,44 +898,85 @@ struct PairFinishArgs {
   long long block;  // B
   long long tj;
   long long ntiles;
-  long long units;
-  long long grid;
+  long long u_base;  // first unit of the launch whose sums are read
+  long long units;   // its units
+  long long grid;    // its CTAs
+  long long I0, I1;  // its i-blocks (all of them for finish_pairs)
 };
+
+// Action sum of body i of block I, whose units all belong to the launch
+// described by `a`: the whole-block row, or the partials of the CTAs that
+// shared the block, in CTA order.
+__device__ __forceinline__ float3 pair_action(const PairFinishArgs& a, long long i, long long I,
+                                              long long tb) {
+  const long long u0 = pair_units_before(I, a.ntiles, tb) - a.u_base;
+  const long long u1 = pair_units_before(I + 1, a.ntiles, tb) - 1 - a.u_base;
+  const long long c0 = unit_owner(a.units, a.grid, u0);
+  const long long c1 = unit_owner(a.units, a.grid, u1);
+  if (c0 == c1) {
+    const float4 v = a.act[i];
+    return make_float3(v.x, v.y, v.z);
+  }
+  float sx = 0.f, sy = 0.f, sz = 0.f;
+  const long long local = i - I * a.block;
+  for (long long cc = c0; cc <= c1; ++cc) {
+    const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
+    const float4 p = a.partial[(cc * 2 + side) * a.block + local];
+    sx += p.x;
+    sy += p.y;
+    sz += p.z;
+  }
+  return make_float3(sx, sy, sz);
+}
+
+// Adds to (sx, sy, sz) the reactions on body i (tile t, row j) from the
+// launch's blocks J in [a.I0, J1), in block order.
+__device__ __forceinline__ void pair_reactions(const PairFinishArgs& a, long long t, long long j,
+                                               long long J1, long long tb, float& sx, float& sy,
+                                               float& sz) {
+  for (long long J = a.I0; J < J1; ++J) {
+    const long long u = pair_units_before(J, a.ntiles, tb) + t - tb * J - a.u_base;
+    const float4 r = a.react[u * a.tj + j];
+    sx += r.x;
+    sy += r.y;
+    sz += r.z;
+  }
+}
 
 __global__ void finish_pairs(const PairFinishArgs a, const Epilogue e) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
   const long long tb = a.block / a.tj;
   const long long I = i / a.block;
-  const long long u0 = pair_units_before(I, a.ntiles, tb);
-  const long long u1 = pair_units_before(I + 1, a.ntiles, tb) - 1;
-  const long long c0 = unit_owner(a.units, a.grid, u0);
-  const long long c1 = unit_owner(a.units, a.grid, u1);
-  float sx = 0.f, sy = 0.f, sz = 0.f;
-  if (c0 == c1) {
-    const float4 v = a.act[i];
-    sx = v.x;
-    sy = v.y;
-    sz = v.z;
-  } else {
-    const long long local = i - I * a.block;
-    for (long long cc = c0; cc <= c1; ++cc) {
-      const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
-      const float4 p = a.partial[(cc * 2 + side) * a.block + local];
-      sx += p.x;
-      sy += p.y;
-      sz += p.z;
-    }
-  }
+  float3 s = pair_action(a, i, I, tb);
   const long long t = i / a.tj;
-  const long long j = i - t * a.tj;
-  for (long long J = 0; J < I; ++J) {
-    const float4 r = a.react[(pair_units_before(J, a.ntiles, tb) + t - tb * J) * a.tj + j];
-    sx += r.x;
-    sy += r.y;
-    sz += r.z;
+  pair_reactions(a, t, i - t * a.tj, I, tb, s.x, s.y, s.z);
+  finish_body(e, i, s.x, s.y, s.z);
+}
+
+__global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first) {
+  const long long i = a.I0 * a.block + static_cast<long long>(blockIdx.x) * blockDim.x +
+                      threadIdx.x;
+  if (i >= a.n) return;
+  const long long tb = a.block / a.tj;
+  const long long I = i / a.block;
+  float3 s = make_float3(0.f, 0.f, 0.f);
+  if (I < a.I1) s = pair_action(a, i, I, tb);
+  const long long t = i / a.tj;
+  pair_reactions(a, t, i - t * a.tj, min(I, a.I1), tb, s.x, s.y, s.z);
+  if (first) {
+    acc[i] = make_float4(s.x, s.y, s.z, 0.f);
+  } else {
+    const float4 o = acc[i];
+    acc[i] = make_float4(o.x + s.x, o.y + s.y, o.z + s.z, 0.f);
   }
-  finish_body(e, i, sx, sy, sz);
+}
+
+__global__ void finish_accumulated(const float4* acc, int n, const Epilogue e) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float4 v = acc[i];
+  finish_body(e, i, v.x, v.y, v.z);
 }
 
 // ---------------------------------------------------------------------------

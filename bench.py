@@ -386,9 +386,9 @@ def run_ours(args):
     value = aggregate_value(interactions * args.steps, world, total_s)
     if args.mode == "kdk":
         force_launches = max(force_launches, 1)
-        interactions_per_launch = float(n) * float(n)
+        interactions_per_pass = float(n) * float(n)
     else:
-        interactions_per_launch = interactions
+        interactions_per_pass = interactions
 
     # end to end through the same API with pinned host buffers
     e2e = None
@@ -425,7 +425,11 @@ def run_ours(args):
     # roofline of the force kernel
     sms = plan["sms"]
     f_max, f_src = measured_sm_max_mhz(clocks)
-    achieved = (interactions_per_launch / (force_ms / 1e3 / force_launches) / 1e9
+    # a pair pass in chunks launches the force kernel once per chunk
+    chunks = ((plan["launches_accel"] - 1) // 2
+              if plan["path"] == nb.PATH_PAIRS and plan["launches_accel"] > 2 else 1)
+    passes = force_launches / chunks if force_launches else 0
+    achieved = (interactions_per_pass / (force_ms / 1e3 / passes) / 1e9
                 if force_launches else None)
     kernel = {nb.PATH_WARP: "force_warp", nb.PATH_PAIRS: "force_pairs"}.get(plan["path"],
                                                                          "force_tiled")
@@ -437,7 +441,9 @@ def run_ours(args):
             "peak_basis": f"{sms} SMs x {f_max:g} MHz ({f_src}) x {FP32_LANES_PER_SM} FP32 lanes"
                           f" / {ops} FP32 ops per interaction",
             "kernel": kernel,
-            "force_ms_per_launch": force_ms / force_launches if force_launches else None}
+            "force_ms_per_launch": force_ms / force_launches if force_launches else None,
+            "force_ms_per_pass": force_ms / passes if force_launches else None,
+            "force_launches_per_pass": chunks}
     if kernel == "force_pairs" and achieved:
         # the same launch against the one-sided form's 12 ops per interaction
         roof["frac_of_one_sided_roofline"] = achieved / alu_peak_ginter(sms, f_max)

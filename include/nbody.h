@@ -74,11 +74,11 @@ typedef enum nbody_status {
 
 /* Force-pass path for the *_with entry points. */
 typedef enum nbody_path {
-    /* Library's choice: the warp-split kernel for small n, the
-       pair-symmetric kernel above it (NBODY_PATH_PAIRS), the one-sided
+    /* Library's choice: the warp-split kernel below n = 16384, the
+       pair-symmetric kernel from there on (NBODY_PATH_PAIRS); the one-sided
        tiled kernel with its (i-block, j-tile) units divided evenly over one
-       wave of CTAs (stream-K) where the pair path's scratch would be too
-       large. */
+       wave of CTAs (stream-K) if the pair path's scratch cannot be
+       allocated. */
     NBODY_PATH_AUTO = 0,
     /* One CTA per i-block over the whole j range; no second pass.  The
        pages' tiled design ("CUDA N-Body Simulation" §3.1). */
@@ -99,9 +99,12 @@ typedef enum nbody_path {
        sources are summed over the CTA's targets in fixed order and stored
        per (i-block, tile) unit; the second pass adds them to the action in
        block order.  Scratch: about n^2 / 448 bytes of reaction sums (2.5 GB
-       at n = 2^20).  AUTO takes this path above the warp kernel's range
-       while that scratch is at most 16 GiB (or NBODY_PAIRS_MAX_BYTES), and
-       falls back to NBODY_PATH_SPLIT's plan if it cannot be allocated. */
+       at n = 2^20); where that exceeds 4 GiB (or NBODY_PAIRS_MAX_BYTES) the
+       pass runs in chunks of consecutive i-blocks whose sums fit, each
+       chunk's sums folded into a per-body accumulator (16 B per body) before
+       the next chunk (two more launches per chunk, one at the end).  AUTO
+       takes this path from n = 16384 on, and falls back to
+       NBODY_PATH_SPLIT's plan if its scratch cannot be allocated. */
     NBODY_PATH_PAIRS = 4
 } nbody_path;
 

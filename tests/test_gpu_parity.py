@@ -262,13 +262,54 @@ def test_plan_pairs_path(monkeypatch):
         assert p["bodies_per_cta"] == block and p["tile"] == tj, (n, cost, p)
         assert p["units"] == pair_units(n, block, tj)
         assert p["grid"] == min(p["units"], p["sms"])
-        assert p["launches_accel"] == 2
+        chunks = pair_chunks(n, block, 4 << 30, tj)
+        assert p["launches_accel"] == (2 if chunks == 1 else 2 * chunks + 1)
     if nb.plan(32768)["sms"] == 152:
         assert nb.plan(1048576)["bodies_per_cta"] == 3584
-    # 4M bodies need ~46 GB of reaction sums: the one-sided plan instead
-    assert nb.plan(4194304)["path"] == nb.PATH_SPLIT
+    # 4M bodies need ~39 GB of reaction rows: the pass runs in chunks of
+    # i-blocks whose rows fit 4 GiB, one accumulation pass per chunk
+    p = nb.plan(4194304)
+    assert p["path"] == nb.PATH_PAIRS
+    assert p["launches_accel"] == 2 * pair_chunks(4194304, p["bodies_per_cta"], 4 << 30,
+                                                  p["tile"]) + 1
     monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", "1000")
-    assert nb.plan(65537)["path"] == nb.PATH_SPLIT
+    p = nb.plan(65537)
+    assert p["path"] == nb.PATH_PAIRS
+    assert p["launches_accel"] == 2 * -(-65537 // p["bodies_per_cta"]) + 1  # a block per chunk
+
+
+def pair_chunks(n, block, cap, tj=512):
+    """Chunks of consecutive i-blocks whose reaction rows (TJ float4 per
+    unit) fit `cap` bytes, one block at least."""
+    nb_, nt, tb = -(-n // block), -(-n // tj), block // tj
+    chunks, acc = 1, 0
+    for i in range(nb_):
+        u = nt - tb * i
+        if acc > 0 and (acc + u) * tj * 16 > cap:
+            chunks, acc = chunks + 1, 0
+        acc += u
+    return chunks
+
+
+@pytest.mark.parametrize("n,cap", [(20000, 1), (30001, 300000), (65537, 2000000),
+                                   (65537, 50000000)])
+def test_pair_path_in_chunks(n, cap, monkeypatch):
+    """The pair path with its reaction rows split into chunks of i-blocks
+    (forced by a small scratch cap) against the oracle, for accelerations, a
+    leapfrog step and a kick-drift-kick step; chunked runs are deterministic."""
+    import all_pairs_body_gb300 as nb
+    monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", str(cap))
+    p = nb.plan(n, path=nb.PATH_PAIRS)
+    chunks = pair_chunks(n, p["bodies_per_cta"], max(cap, p["tile"] * 16), p["tile"])
+    assert p["launches_accel"] == (2 * chunks + 1 if chunks > 1 else 2)
+    pm = W.random_bodies(n, 6000 + n)
+    a = gpu_accel(pm, 1e-3, path=4)
+    assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL
+    assert np.array_equal(a, gpu_accel(pm, 1e-3, path=4))
+    v = W.random_velocities(n, 6000 + n)
+    pp, vv, aa = gpu_leapfrog(pm, v, 1e-3, 1e-3, 2, path=4)
+    rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 2)
+    assert rel_err(aa, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(pp, rp) <= POS_TOL
 
 
 N_PAIR_VARIANTS = 23
