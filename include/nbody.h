@@ -289,8 +289,11 @@ int nbody_accel_noalloc(const float *pos_mass, float *accel, int64_t n,
  *   [0] path actually used (nbody_path value)   [1] grid (CTAs)
  *   [2] threads per CTA                         [3] target bodies per CTA
  *   [4] source bodies per tile                  [5] tiles over n
- *   [6] work units (i-blocks x tiles)           [7] 1 if a second pass runs
- *   [8] kernel launches of one nbody_accel call
+ *   [6] work units (i-blocks x tiles; for NBODY_PATH_PAIRS the (i-block,
+ *       tile) units from each block's own first tile on)
+ *   [7] 1 if a second pass runs
+ *   [8] kernel launches of one nbody_accel call (pair path in chunks:
+ *       2 per chunk + 1)
  *   [9] kernel launches of one nbody_leapfrog_step call with steps = 1
  *  [10] streaming multiprocessors on the device
  * Returns NBODY_OK, NBODY_EINVAL or NBODY_ECUDA.
