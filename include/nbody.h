@@ -54,6 +54,11 @@
  *                   copy expired; the kernel stopped and its outputs are
  *                   undefined.  The CUDA context stays usable.
  *   n == 0 and steps == 0 are valid no-ops that return NBODY_OK.
+ *
+ * Positions, masses and velocities are not checked: a non-finite value
+ * gives non-finite results for every body whose sum it enters (all of them,
+ * for a non-finite source), as in the pages' kernels.  Zero and negative
+ * masses are valid.
  */
 #ifndef NBODY_H
 #define NBODY_H
