@@ -338,6 +338,40 @@ def test_pair_path_block_edges(n):
     assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL, n
 
 
+def test_every_path_gives_zero_for_coincident_bodies():
+    """All bodies at one point: every term is m_j * 0 * d^(-3/2), exactly zero,
+    across and inside i-blocks, on every path (the pair path's reactions too)."""
+    pm = np.zeros((20000, 4), dtype=np.float32)
+    pm[:, :3] = (0.25, -0.5, 0.75)
+    pm[:, 3] = np.linspace(0.5, 1.5, 20000, dtype=np.float32) / 20000
+    for path, split in [(0, 0), (2, 0), (3, 0), (4, 0)]:
+        assert np.all(gpu_accel(pm, 1e-3, path, split)[:, :3] == 0.0), (path, split)
+
+
+def test_pair_path_two_distant_clusters():
+    """Two clusters of half the mass, 5 apart: each body's field is dominated
+    by its own cluster (RMS ~50), the other adds a pull of ~0.02 along x. The
+    forces inside a cluster cancel in its mean (action = -reaction), so the
+    near cluster's mean acceleration is the far cluster's pull, 0.5 / 5^2 to
+    within the clusters' size — a figure far below each body's own field that
+    the pair path must keep as the oracle does."""
+    rng = np.random.default_rng(31)
+    n = 30000
+    pos = rng.normal(scale=0.05, size=(n, 3))
+    pos[n // 2:, 0] += 5.0
+    pm = np.empty((n, 4), dtype=np.float32)
+    pm[:, :3] = pos
+    pm[:, 3] = 1.0 / n
+    a = gpu_accel(pm, 1e-4, path=4).astype(np.float64)
+    ref = oracle.accel(pm, 1e-4)
+    assert rel_err(a, ref) <= ACC_TOL
+    pull = 0.5 / 5.0 ** 2
+    near, far = slice(0, n // 2), slice(n // 2, n)
+    assert abs(ref[near, 0].mean() / pull - 1.0) < 1e-2  # the oracle's own mean
+    assert abs(a[near, 0].mean() - ref[near, 0].mean()) < 1e-3 * pull
+    assert abs(a[far, 0].mean() - ref[far, 0].mean()) < 1e-3 * pull
+
+
 def test_pair_path_masses():
     """Zero, negative and one dominant mass: the reaction uses the target's
     own mass, so a massless target must pull on nothing."""
