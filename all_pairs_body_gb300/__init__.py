@@ -22,7 +22,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libnbody_gb300.so")
 
 PATH_AUTO, PATH_TILED, PATH_SPLIT, PATH_WARP, PATH_PAIRS = 0, 1, 2, 3, 4
-OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBOUNDS = 0, 1, 2, 3, 4, 5
 PLAN_FIELDS = ("path", "grid", "threads", "bodies_per_cta", "tile", "tiles", "units",
                "second_pass", "launches_accel", "launches_step", "sms")
 
@@ -46,46 +46,53 @@ class NBodyError(RuntimeError):
 _lib = None
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of the C library at ``path`` with its C signatures
+    declared (the release build through lib(); tests also load the
+    index-checked build this way)."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with all_pairs_body_gb300.build.build() "
+            "(or __graft_entry__.build()); there is no CPU fallback")
+    L = ctypes.CDLL(path)
+    p, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    sig = {
+        "nbody_accel": [p, p, i64, f32],
+        "nbody_accel_on_stream": [p, p, i64, f32, p],
+        "nbody_accel_with": [p, p, i64, f32, i32, i32, p],
+        "nbody_accel_noalloc": [p, p, i64, f32, p],
+        "nbody_leapfrog_step": [p, p, p, i64, f32, f32, i32],
+        "nbody_leapfrog_step_on_stream": [p, p, p, i64, f32, f32, i32, p],
+        "nbody_leapfrog_step_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
+        "nbody_leapfrog_kdk_on_stream": [p, p, p, i64, f32, f32, i32, p],
+        "nbody_leapfrog_kdk_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
+        "nbody_render_points": [p, p, p, i64, f32, f32, f32, f32, f32, p],
+        "nbody_neighbors_2d": [p, p, i64, f32, i32, p, p, p],
+        "nbody_accel_layout": [p, p, i64, f32, i32, p],
+        "nbody_leapfrog_step_layout": [p, p, p, i64, f32, f32, i32, i32, p],
+        "nbody_sync": [p],
+        "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
+        "nbody_selftest_timeout": [i32, p],
+        "nbody_profile_enable": [i32],
+        "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
+                               ctypes.POINTER(i64)],
+        "nbody_strerror": [i32],
+        "nbody_release": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = i32
+    L.nbody_strerror.restype = ctypes.c_char_p
+    L.nbody_release.restype = None
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """The loaded C library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with all_pairs_body_gb300.build.build() "
-                "(or __graft_entry__.build()); there is no CPU fallback")
-        L = ctypes.CDLL(LIB_PATH)
-        p, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
-        sig = {
-            "nbody_accel": [p, p, i64, f32],
-            "nbody_accel_on_stream": [p, p, i64, f32, p],
-            "nbody_accel_with": [p, p, i64, f32, i32, i32, p],
-            "nbody_accel_noalloc": [p, p, i64, f32, p],
-            "nbody_leapfrog_step": [p, p, p, i64, f32, f32, i32],
-            "nbody_leapfrog_step_on_stream": [p, p, p, i64, f32, f32, i32, p],
-            "nbody_leapfrog_step_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
-            "nbody_leapfrog_kdk_on_stream": [p, p, p, i64, f32, f32, i32, p],
-            "nbody_leapfrog_kdk_with": [p, p, p, i64, f32, f32, i32, i32, i32, p],
-            "nbody_render_points": [p, p, p, i64, f32, f32, f32, f32, f32, p],
-            "nbody_neighbors_2d": [p, p, i64, f32, i32, p, p, p],
-            "nbody_accel_layout": [p, p, i64, f32, i32, p],
-            "nbody_leapfrog_step_layout": [p, p, p, i64, f32, f32, i32, i32, p],
-            "nbody_sync": [p],
-            "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
-            "nbody_selftest_timeout": [i32, p],
-            "nbody_profile_enable": [i32],
-            "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
-                                   ctypes.POINTER(i64)],
-            "nbody_strerror": [i32],
-            "nbody_release": [],
-        }
-        for name, args in sig.items():
-            fn = getattr(L, name)
-            fn.argtypes = args
-            fn.restype = i32
-        L.nbody_strerror.restype = ctypes.c_char_p
-        L.nbody_release.restype = None
-        _lib = L
+        _lib = load(LIB_PATH)
     return _lib
 
 

@@ -15,6 +15,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libnbody_gb300.so")
+# The index-checked build (NBODY_BOUNDS_CHECK): every computed index into a
+# scratch or output array is tested on the device; for tests, not for use.
+LIB_CHECKED = os.path.join(HERE, "libnbody_gb300_checked.so")
 SOURCES = ["nbody_api.cu"]
 DEPS = SOURCES + ["nbody_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -27,20 +30,23 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          checked: bool = False) -> str:
+    out = LIB_CHECKED if checked else LIB
     deps = [os.path.join(CSRC, s) for s in DEPS] + [os.path.join(INCLUDE, "nbody.h")]
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
+    if not force and os.path.exists(out):
+        t = os.path.getmtime(out)
         if all(os.path.getmtime(d) <= t for d in deps):
-            return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ([nvcc()] + ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra or [])
+            return out
+    tmp = out + f".tmp{os.getpid()}"
+    flags = ["-DNBODY_BOUNDS_CHECK"] if checked else []
+    cmd = ([nvcc()] + ARCH + NVCC_FLAGS + flags + ["-I", INCLUDE, "-I", CSRC] + list(extra or [])
            + ["-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcudart"])
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -184,6 +184,34 @@ cudaEvent_t prof_event(cudaStream_t st) {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// Capacities for the index checks of the checked build (a no-op otherwise):
+// rows of the per-body arrays, float4 rows of `partial` and of the reaction
+// sums, ints of the neighbour list.  NBODY_BOUNDS_SHRINK=<slot> (rows,
+// partial, react, neighbors) sets one capacity to 0 so that a test can see
+// the checks fire; every access they stop is skipped, none goes out of bounds.
+void set_caps(long long rows, long long partial, long long react, long long neighbors,
+              cudaStream_t st) {
+#ifdef NBODY_BOUNDS_CHECK
+  long long caps[kNumCaps] = {};
+  caps[kCapRows] = rows;
+  caps[kCapPartial] = partial;
+  caps[kCapReact] = react;
+  caps[kCapNeighbors] = neighbors;
+  if (const char* v = std::getenv("NBODY_BOUNDS_SHRINK")) {
+    const char* names[kNumCaps] = {"rows", "partial", "react", "neighbors"};
+    for (int k = 0; k < kNumCaps; ++k)
+      if (std::strcmp(v, names[k]) == 0) caps[k] = 0;
+  }
+  cudaMemcpyToSymbolAsync(g_caps, caps, sizeof(caps), 0, cudaMemcpyHostToDevice, st);
+#else
+  (void)rows, (void)partial, (void)react, (void)neighbors, (void)st;
+#endif
+}
+
+long long float4_rows(const void* p, size_t bytes) {
+  return p == nullptr ? 0 : static_cast<long long>(bytes / sizeof(float4));
+}
+
 bool env_flag(const char* name) {
   const char* v = std::getenv(name);
   return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
@@ -565,6 +593,8 @@ int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st
 void launch_force(const Plan& p, const float4* pos, long long n, float eps2, const Scratch& s,
                   const Epilogue& epi, cudaStream_t st) {
   float4* partial = static_cast<float4*>(s.partial.p);
+  set_caps(n, float4_rows(s.partial.p, s.partial.bytes), float4_rows(s.react.p, s.react.bytes), 0,
+           st);
   if (p.path == NBODY_PATH_PAIRS) {
     const PairConfig& pc = kPairs[p.cfg];
     const long long tb = p.block / p.tj;
@@ -751,6 +781,7 @@ int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float
   a.inv_range = static_cast<float>(1.0 / (static_cast<double>(max_w) - min_w));
   const long long blocks = std::min(ceil_div(n, 256), static_cast<long long>(d.sms) * 8);
   count_launches(1);
+  set_caps(n, 0, 0, 0, st);
   render_points<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return launch_status();
 }
@@ -791,6 +822,7 @@ int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int 
   NeighborArgs a{x, y, static_cast<int>(n), c2, max_neighbors, nn, nl, ceil_div(n, kNeighborNT)};
   const long long blocks = ceil_div(n, static_cast<long long>(kNeighborKI) * kNeighborNT);
   count_launches(1);
+  set_caps(n, 0, 0, n * static_cast<long long>(max_neighbors), st);
   neighbors_2d<kNeighborKI, kNeighborNT, kNeighborU>
       <<<static_cast<unsigned>(blocks), kNeighborNT, 0, st>>>(a);
   return launch_status();
@@ -885,6 +917,7 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   float4* partial = d.scratch;  // every slot a call reads, the same call writes first
   const Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, kRows4, n);
   TiledArgs a{pos, static_cast<int>(n), eps2, ntiles, units, grid, partial, kWaitLimitNs, -1};
+  set_caps(n, kNoAllocRows, 0, 0, st);
   tc.kernel<<<static_cast<unsigned>(grid), tc.nt, 0, st>>>(a, epi);
   if (second) {
     StreamkFinishArgs f{partial, static_cast<int>(n), block, ntiles, units, grid};
@@ -1050,6 +1083,7 @@ const char* nbody_strerror(int status) {
     case NBODY_ENOMEM: return "scratch allocation failed";
     case NBODY_ECUDA: return "CUDA error (no usable device or a failed launch)";
     case NBODY_ETIMEOUT: return "a bounded device-side wait expired";
+    case NBODY_EBOUNDS: return "a device-side index check failed (checked build)";
     default: return "unknown status";
   }
 }
@@ -1119,6 +1153,7 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   TiledArgs a{buf[0], static_cast<int>(n1), 1.0f, ceil_div(n1, tc.tj), ceil_div(n1, tc.tj), 1,
               nullptr, limit, 0};
   const Epilogue epi = make_epilogue(buf[0], buf[1], nullptr, nullptr, 0.f, 0.f, kRows4, n1);
+  set_caps(n2, 2 * pb, units2 * pc.tj, 0, st);
   tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
   int rc1 = launch_status();
   const int s1 = nbody_sync(cuda_stream);

@@ -58,6 +58,31 @@ namespace nbody {
 // nbody_sync on the host).  This header is compiled into one translation unit.
 __device__ int g_status = 0;
 
+// Index checks of the checked build (compiled with NBODY_BOUNDS_CHECK): each
+// computed index into a scratch or output array is tested against the
+// capacity the host allocated (g_caps, set before the launches); a failed
+// check records NBODY_EBOUNDS (the first error wins) and the access is
+// skipped.  In the release build NBODY_IN_BOUNDS is the constant true, so
+// every guarded access compiles exactly as unguarded.
+enum CapSlot : int {
+  kCapRows = 0,   // rows of pos/accel/vel/pos_next/ndc/rgba and of per-body scratch
+  kCapPartial,    // float4 rows of `partial`
+  kCapReact,      // float4 rows of the pair path's reaction sums
+  kCapNeighbors,  // ints of the neighbour list
+  kNumCaps
+};
+#ifdef NBODY_BOUNDS_CHECK
+__device__ long long g_caps[kNumCaps];
+__device__ __noinline__ bool index_in_bounds(long long idx, int slot) {
+  if (idx >= 0 && idx < g_caps[slot]) return true;
+  atomicCAS(&g_status, 0, static_cast<int>(NBODY_EBOUNDS));
+  return false;
+}
+#define NBODY_IN_BOUNDS(idx, slot) index_in_bounds((idx), (slot))
+#else
+#define NBODY_IN_BOUNDS(idx, slot) true
+#endif
+
 // ---------------------------------------------------------------------------
 // small PTX wrappers
 // ---------------------------------------------------------------------------
@@ -260,6 +285,7 @@ __device__ __forceinline__ float4 load_vec3(const float* base, int layout, long 
 // schedule of the inner loop (up to 2.5% in a measured sweep).
 __device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
                                          float az) {
+  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
   store_vec3(e.accel, e.layout, e.n, i, ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
     float4 v = load_vec3(e.vel, e.layout, e.n, i);
@@ -492,7 +518,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
           const float fz = h ? az[p].y : az[p].x;
           if (whole)
             finish_body(e, i, fx, fy, fz);
-          else
+          else if (NBODY_IN_BOUNDS(slot + local, kCapPartial))
             a.partial[slot + local] = make_float4(fx, fy, fz, 0.f);
         }
       }
@@ -532,7 +558,8 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
   for (long long c = c0; c <= c1; ++c) {
     // the block's segment is CTA c's first segment unless c started earlier
     const int side = unit_begin(a.units, a.grid, c) >= u0 ? 0 : 1;
-    const float4 p = a.partial[(c * 2 + side) * a.block + local];
+    const long long at = (c * 2 + side) * a.block + local;
+    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -820,7 +847,8 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             sy += red[w][1][j];
             sz += red[w][2][j];
           }
-          a.react[(u - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
+          if (NBODY_IN_BOUNDS((u - a.u_base) * TJ + j, kCapReact))
+            a.react[(u - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
         }
       }
 #pragma unroll
@@ -859,9 +887,9 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
           }
           const float4 v = make_float4(h ? sx2.y : sx2.x, h ? sy2.y : sy2.x,
                                        h ? sz2.y : sz2.x, 0.f);
-          if (whole)
+          if (whole && NBODY_IN_BOUNDS(i, kCapRows))
             a.act[i] = v;
-          else
+          else if (!whole && NBODY_IN_BOUNDS(slot + local, kCapPartial))
             a.partial[slot + local] = v;
         }
       }
@@ -914,14 +942,15 @@ __device__ __forceinline__ float3 pair_action(const PairFinishArgs& a, long long
   const long long c0 = unit_owner(a.units, a.grid, u0);
   const long long c1 = unit_owner(a.units, a.grid, u1);
   if (c0 == c1) {
-    const float4 v = a.act[i];
+    const float4 v = NBODY_IN_BOUNDS(i, kCapRows) ? a.act[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     return make_float3(v.x, v.y, v.z);
   }
   float sx = 0.f, sy = 0.f, sz = 0.f;
   const long long local = i - I * a.block;
   for (long long cc = c0; cc <= c1; ++cc) {
     const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
-    const float4 p = a.partial[(cc * 2 + side) * a.block + local];
+    const long long at = (cc * 2 + side) * a.block + local;
+    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -936,7 +965,8 @@ __device__ __forceinline__ void pair_reactions(const PairFinishArgs& a, long lon
                                                float& sz) {
   for (long long J = a.I0; J < J1; ++J) {
     const long long u = pair_units_before(J, a.ntiles, tb) + t - tb * J - a.u_base;
-    const float4 r = a.react[u * a.tj + j];
+    const float4 r = NBODY_IN_BOUNDS(u * a.tj + j, kCapReact) ? a.react[u * a.tj + j]
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += r.x;
     sy += r.y;
     sz += r.z;
@@ -964,6 +994,7 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
   if (I < a.I1) s = pair_action(a, i, I, tb);
   const long long t = i / a.tj;
   pair_reactions(a, t, i - t * a.tj, min(I, a.I1), tb, s.x, s.y, s.z);
+  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
   if (first) {
     acc[i] = make_float4(s.x, s.y, s.z, 0.f);
   } else {
@@ -975,6 +1006,7 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
 __global__ void finish_accumulated(const float4* acc, int n, const Epilogue e) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
   const float4 v = acc[i];
   finish_body(e, i, v.x, v.y, v.z);
 }
@@ -1064,7 +1096,8 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
       if (a.slices == 1)
         finish_body(e, i, sx, sy, sz);
       else
-        a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
+        if (NBODY_IN_BOUNDS(static_cast<long long>(blockIdx.y) * a.n + i, kCapPartial))
+          a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
     }
   }
 }
@@ -1076,7 +1109,8 @@ __global__ void finish_slices(const float4* __restrict__ partial, int n, int sli
   if (i >= n) return;
   float sx = 0.f, sy = 0.f, sz = 0.f;
   for (int s = 0; s < slices; ++s) {
-    const float4 p = partial[static_cast<long long>(s) * n + i];
+    const long long at = static_cast<long long>(s) * n + i;
+    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -1219,7 +1253,8 @@ __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
               if ((h ? d2[u][p].y : d2[u][p].x) < c2 && j != i) {
                 int& c = cnt[2 * p + h];
                 if (c < a.max_neighbors)
-                  a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
+                  if (NBODY_IN_BOUNDS(static_cast<long long>(c) * a.n + i, kCapNeighbors))
+                    a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
                 ++c;
               }
             }
@@ -1233,7 +1268,9 @@ __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
     const long long i = base + k * NT + tid;
     if (i < a.n) {
       a.nn[i] = cnt[k];
-      for (int q = cnt[k]; q < a.max_neighbors; ++q) a.nl[static_cast<long long>(q) * a.n + i] = -1;
+      for (int q = cnt[k]; q < a.max_neighbors; ++q)
+        if (NBODY_IN_BOUNDS(static_cast<long long>(q) * a.n + i, kCapNeighbors))
+          a.nl[static_cast<long long>(q) * a.n + i] = -1;
     }
   }
 }

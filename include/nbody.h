@@ -53,6 +53,10 @@
  *   NBODY_ETIMEOUT  (nbody_sync only) a kernel's bounded wait for a tile
  *                   copy expired; the kernel stopped and its outputs are
  *                   undefined.  The CUDA context stays usable.
+ *   NBODY_EBOUNDS   (nbody_sync only, index-checked builds only) an index
+ *                   into a scratch or output array fell outside what the
+ *                   host allocated; the access was skipped, the outputs are
+ *                   undefined.  The release build has no such checks.
  *   n == 0 and steps == 0 are valid no-ops that return NBODY_OK.
  *
  * Positions, masses and velocities are not checked: a non-finite value
@@ -74,7 +78,10 @@ typedef enum nbody_status {
     NBODY_EINVAL = 1,
     NBODY_ENOMEM = 2,
     NBODY_ECUDA = 3,
-    NBODY_ETIMEOUT = 4
+    NBODY_ETIMEOUT = 4,
+    /* Index-checked builds only (compiled with NBODY_BOUNDS_CHECK): a
+       device-side index check failed and the access was skipped. */
+    NBODY_EBOUNDS = 5
 } nbody_status;
 
 /* Force-pass path for the *_with entry points. */
