@@ -328,6 +328,18 @@ __device__ __noinline__ bool expand_tile(const float4* raw, float4* tile, int tj
   return odd;
 }
 
+// The same expansion with the two halves in separate arrays: tile[b] =
+// (x, x, y, y), tile[tj + b] = (z, z, m, m).  Lanes that read consecutive
+// sources then read consecutive 16-byte rows (no bank conflicts).
+__device__ __noinline__ void expand_tile_split(const float4* raw, float4* tile, int tj, int nt,
+                                               int tid, long long live) {
+  for (int b = tid; b < tj; b += nt) {
+    const float4 x = b < live ? raw[b] : make_float4(0.f, 0.f, 0.f, 0.f);
+    tile[b] = make_float4(x.x, x.x, x.y, x.y);
+    tile[tj + b] = make_float4(x.z, x.z, x.w, x.w);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // tiled force kernel with an even (stream-K) division of the work
 // ---------------------------------------------------------------------------
@@ -684,10 +696,20 @@ __host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, in
 // per-tile sums.  ACC = 1: they live in shared memory ([3][KI/2][NT] float2,
 // one column per thread) and are touched once per tile, when the per-tile sums
 // are folded in, which leaves 3 KI registers to the inner loop.
-template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0>
+//
+// ROT = 0: a tile's reactions are reduced over the lanes in batches of NB
+// sources (reduce_scatter).  ROT = 1: the sources rotate through the lanes
+// instead.  In each group of 32 sources, at step s lane l evaluates source
+// (l + s) mod 32 against its targets and adds to that source's reaction sum,
+// which it takes from lane l + 1 (the lane that evaluated the source at step
+// s - 1); after 32 steps lane l holds the warp's whole sum for source
+// (l + 31) mod 32.  That costs 6 shuffles per source and step and no adds or
+// selects; UNRB then unrolls the 32 steps.
+template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0, int ROT = 0>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   static_assert((KI * NT) % TJ == 0 && TJ % NB == 0, "tiles tile an i-block; batches tile a tile");
+  static_assert(ROT == 0 || TJ % 32 == 0, "rotation groups of 32 sources tile a tile");
   constexpr int kShift = NB == 8 ? 2 : 1;  // lane l holds source l >> kShift of a batch
   constexpr int P = KI / 2;
   constexpr int NW = NT / 32;
@@ -793,25 +815,58 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
         break;
       }
       if (tid == 0 && k + 1 < count) issue_next(k + 1);
-      (void)expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
+      if constexpr (ROT == 1)
+        expand_tile_split(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
+      else
+        (void)expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
       __syncthreads();
 
       float2 tx[P], ty[P], tz[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
       const float4* src = tile;
+      constexpr int kLo = ROT == 1 ? 1 : 2;   // row of source j's first half: kLo * j
+      constexpr int kHi = ROT == 1 ? TJ : 1;  // its second half: kLo * j + kHi
       if (t < TB * (blk + 1)) {
         // a tile of the block itself: both sides of each pair, as in force_tiled
 #pragma unroll 2
         for (int j = 0; j < TJ; ++j) {
-          const float4 lo = src[2 * j];
-          const float4 hi = src[2 * j + 1];
+          const float4 lo = src[kLo * j];
+          const float4 hi = src[kLo * j + kHi];
 #pragma unroll
           for (int p = 0; p < P; ++p)
             interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w), make_float2(hi.x, hi.y),
                       make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
         }
       } else {
+        if constexpr (ROT == 1) {
+          constexpr unsigned kAll = 0xffffffffu;
+          const int from = (lane + 1) & 31;
+          for (int g = 0; g < TJ; g += 32) {
+            float2 bx = make_float2(0.f, 0.f), by = bx, bz = bx;
+#pragma unroll UNRB
+            for (int st = 0; st < 32; ++st) {
+              const int j = g + ((lane + st) & 31);
+              const float4 lo = src[j];
+              const float4 hi = src[TJ + j];
+              bx.x = __shfl_sync(kAll, bx.x, from);
+              bx.y = __shfl_sync(kAll, bx.y, from);
+              by.x = __shfl_sync(kAll, by.x, from);
+              by.y = __shfl_sync(kAll, by.y, from);
+              bz.x = __shfl_sync(kAll, bz.x, from);
+              bz.y = __shfl_sync(kAll, bz.y, from);
+#pragma unroll
+              for (int p = 0; p < P; ++p)
+                interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                               make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                               nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+            }
+            const int jj = g + ((lane + 31) & 31);
+            red[warp][0][jj] = bx.x + bx.y;
+            red[warp][1][jj] = by.x + by.y;
+            red[warp][2][jj] = bz.x + bz.y;
+          }
+        } else {
 #pragma unroll UNRB
         for (int b0 = 0; b0 < TJ; b0 += NB) {
           float vx[NB], vy[NB], vz[NB];
@@ -835,6 +890,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             red[warp][1][b0 + (lane >> kShift)] = r.y;
             red[warp][2][b0 + (lane >> kShift)] = r.z;
           }
+        }
         }
         __syncthreads();
         // the unit's reaction partial: the NW warps' sums in warp order

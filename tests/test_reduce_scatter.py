@@ -8,6 +8,11 @@ levels one value is left per lane; the remaining masks sum it over the rest
 of the warp. The kernel then reads source l >> (5 - log2 NB) in lane l, and
 the lanes whose low 5 - log2 NB bits are zero write it. These tests pin that
 mapping and that every source's total is the sum over all 32 lanes.
+
+The kernel's other variant rotates the sources through the lanes instead: at
+step s of a group of 32 sources lane l evaluates source (l + s) mod 32 and
+carries that source's running sum, taken from lane l + 1; after 32 steps lane
+l holds the total of source (l + 31) mod 32.
 """
 import numpy as np
 import pytest
@@ -65,3 +70,44 @@ def test_integer_sums_are_exact():
     v = np.arange(LANES * 16, dtype=np.float64).reshape(LANES, 16) % 7
     out = reduce_scatter(v)
     assert np.array_equal(out, v.sum(axis=0)[np.arange(LANES) >> 1])
+
+
+def rotate_through_lanes(c):
+    """c: (32, 32) contribution of lane l to source s of a group.
+
+    Each step every lane takes the running sum from lane l + 1 (mod 32), then
+    adds its contribution to source (l + step) mod 32.  Returns the (32,) sum
+    each lane holds after the 32 steps, the additions in the order they ran.
+    """
+    lane = np.arange(LANES)
+    carry = np.zeros(LANES)
+    order = [[] for _ in range(LANES)]  # lanes each source's sum passed through
+    held = (lane - 1) % LANES  # source whose (zero) sum each lane carries before step 0
+    for step in range(LANES):
+        carry = carry[(lane + 1) % LANES]
+        held = held[(lane + 1) % LANES]
+        src = (lane + step) % LANES
+        assert np.array_equal(held, src)  # the sum arrives where its source is evaluated
+        carry = carry + c[lane, src]
+        for l in range(LANES):
+            order[src[l]].append(l)
+    return carry, order
+
+
+def test_rotation_leaves_each_source_total_in_lane_before():
+    rng = np.random.default_rng(7)
+    c = rng.standard_normal((LANES, LANES))
+    out, order = rotate_through_lanes(c)
+    totals = c.sum(axis=0)
+    for lane in range(LANES):
+        src = (lane + 31) % LANES
+        assert out[lane] == pytest.approx(totals[src], rel=1e-12, abs=1e-12)
+    # every source visited every lane exactly once, in a fixed order
+    for src in range(LANES):
+        assert sorted(order[src]) == list(range(LANES))
+
+
+def test_rotation_integer_sums_are_exact():
+    c = (np.arange(LANES * LANES).reshape(LANES, LANES) * 37 % 11).astype(np.float64)
+    out, _ = rotate_through_lanes(c)
+    assert np.array_equal(out, c.sum(axis=0)[(np.arange(LANES) + 31) % LANES])
