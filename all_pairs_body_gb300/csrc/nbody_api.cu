@@ -82,16 +82,16 @@ struct PairConfig {
 
 // Shapes of the pair-symmetric kernel (targets per thread, threads, tile;
 // template: + reduction batch, batch or step unroll, running sums in shared
-// memory, lane rotation).  Rows 0-4 rotate the sources through the lanes
-// (ROT = 1) and are the plan's candidates, the first the default; rows 5-27
-// reduce the reactions in batches (ROT = 0); rows 28- are further rotation
-// shapes.
+// memory, lane rotation: 1 group of 32 sources or 2 side by side).  Rows
+// 0-4 rotate the sources through the lanes and are the plan's candidates,
+// the first the default; rows 5-27 reduce the reactions in batches
+// (ROT = 0); rows 28- are further rotation shapes.
 const PairConfig kPairs[] = {
     {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 1>, 1},
     {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 1>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 1>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 1>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 1>, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 2>, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 2>, 1},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 2>, 0},
     {14, 256, 512, force_pairs<14, 256, 512, 16, 1, 1>, 1},
     {12, 256, 512, force_pairs<12, 256, 512, 16, 1>, 0},
     {10, 256, 512, force_pairs<10, 256, 512, 16, 1>, 0},
@@ -115,6 +115,9 @@ const PairConfig kPairs[] = {
     {12, 256, 512, force_pairs<12, 256, 512, 16, 1, 1>, 1},
     {16, 256, 512, force_pairs<16, 256, 512, 16, 1, 1>, 1},
     {10, 256, 512, force_pairs<10, 256, 512, 16, 1, 1>, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 1>, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 1>, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 1>, 0},
     {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 1>, 1},
     {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 1>, 1},
     {16, 256, 512, force_pairs<16, 256, 512, 32, 2, 1, 1>, 1},
@@ -131,6 +134,16 @@ const PairConfig kPairs[] = {
     {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 1>, 1},
     {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 0, 1>, 0},
     {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 1>, 0},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 2>, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 2>, 1},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 2>, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 2>, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 2>, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 2>, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 0, 2>, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 2>, 1},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 1, 2>, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 1, 2>, 1},
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
@@ -380,12 +393,12 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
 }
 
 // Pair shapes the plan chooses between, with their speed per interaction
-// relative to the first, measured at n = 2^20 (force kernel 270.8, 275.2,
-// 281.0, 286.1 and 284.0 ms per pass, the last two in two chunks): more
+// relative to the first, measured at n = 2^20 (force kernel 270.7, 275.2,
+// 276.5, 277.4 and 279.8 ms per pass, the last two in two chunks): more
 // targets per CTA are faster per interaction; smaller blocks and tiles cut
 // the work into more units, which wins when a CTA's share of units is small.
 constexpr LargeShape kPairShapes[] = {
-    {0, 1.0}, {1, 0.984}, {2, 0.964}, {3, 0.947}, {4, 0.954}};
+    {0, 1.0}, {1, 0.984}, {2, 0.979}, {3, 0.976}, {4, 0.967}};
 
 long long pair_units_of(long long n, const PairConfig& pc) {
   const long long block = static_cast<long long>(pc.ki) * pc.nt;

@@ -709,7 +709,7 @@ template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0, int ROT = 0>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   static_assert((KI * NT) % TJ == 0 && TJ % NB == 0, "tiles tile an i-block; batches tile a tile");
-  static_assert(ROT == 0 || TJ % 32 == 0, "rotation groups of 32 sources tile a tile");
+  static_assert(ROT == 0 || TJ % (32 * ROT) == 0, "rotation groups of 32 sources tile a tile");
   constexpr int kShift = NB == 8 ? 2 : 1;  // lane l holds source l >> kShift of a batch
   constexpr int P = KI / 2;
   constexpr int NW = NT / 32;
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
         break;
       }
       if (tid == 0 && k + 1 < count) issue_next(k + 1);
-      if constexpr (ROT == 1)
+      if constexpr (ROT >= 1)
         expand_tile_split(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
       else
         (void)expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
@@ -825,8 +825,8 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
 #pragma unroll
       for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
       const float4* src = tile;
-      constexpr int kLo = ROT == 1 ? 1 : 2;   // row of source j's first half: kLo * j
-      constexpr int kHi = ROT == 1 ? TJ : 1;  // its second half: kLo * j + kHi
+      constexpr int kLo = ROT >= 1 ? 1 : 2;   // row of source j's first half: kLo * j
+      constexpr int kHi = ROT >= 1 ? TJ : 1;  // its second half: kLo * j + kHi
       if (t < TB * (blk + 1)) {
         // a tile of the block itself: both sides of each pair, as in force_tiled
 #pragma unroll 2
@@ -865,6 +865,51 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             red[warp][0][jj] = bx.x + bx.y;
             red[warp][1][jj] = by.x + by.y;
             red[warp][2][jj] = bz.x + bz.y;
+          }
+        } else if constexpr (ROT == 2) {
+          // two groups of 32 sources rotate side by side: two independent
+          // reaction sums per lane and step
+          constexpr unsigned kAll = 0xffffffffu;
+          const int from = (lane + 1) & 31;
+          for (int g = 0; g < TJ; g += 64) {
+            float2 bx0 = make_float2(0.f, 0.f), by0 = bx0, bz0 = bx0;
+            float2 bx1 = bx0, by1 = bx0, bz1 = bx0;
+#pragma unroll UNRB
+            for (int st = 0; st < 32; ++st) {
+              const int j = g + ((lane + st) & 31);
+              const float4 lo0 = src[j];
+              const float4 hi0 = src[TJ + j];
+              const float4 lo1 = src[j + 32];
+              const float4 hi1 = src[TJ + j + 32];
+              bx0.x = __shfl_sync(kAll, bx0.x, from);
+              bx0.y = __shfl_sync(kAll, bx0.y, from);
+              by0.x = __shfl_sync(kAll, by0.x, from);
+              by0.y = __shfl_sync(kAll, by0.y, from);
+              bz0.x = __shfl_sync(kAll, bz0.x, from);
+              bz0.y = __shfl_sync(kAll, bz0.y, from);
+              bx1.x = __shfl_sync(kAll, bx1.x, from);
+              bx1.y = __shfl_sync(kAll, bx1.y, from);
+              by1.x = __shfl_sync(kAll, by1.x, from);
+              by1.y = __shfl_sync(kAll, by1.y, from);
+              bz1.x = __shfl_sync(kAll, bz1.x, from);
+              bz1.y = __shfl_sync(kAll, bz1.y, from);
+#pragma unroll
+              for (int p = 0; p < P; ++p) {
+                interact2_pair(make_float2(lo0.x, lo0.y), make_float2(lo0.z, lo0.w),
+                               make_float2(hi0.x, hi0.y), make_float2(hi0.z, hi0.w), nx[p],
+                               ny[p], nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx0, by0, bz0);
+                interact2_pair(make_float2(lo1.x, lo1.y), make_float2(lo1.z, lo1.w),
+                               make_float2(hi1.x, hi1.y), make_float2(hi1.z, hi1.w), nx[p],
+                               ny[p], nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx1, by1, bz1);
+              }
+            }
+            const int jj = g + ((lane + 31) & 31);
+            red[warp][0][jj] = bx0.x + bx0.y;
+            red[warp][1][jj] = by0.x + by0.y;
+            red[warp][2][jj] = bz0.x + bz0.y;
+            red[warp][0][jj + 32] = bx1.x + bx1.y;
+            red[warp][1][jj + 32] = by1.x + by1.y;
+            red[warp][2][jj + 32] = bz1.x + bz1.y;
           }
         } else {
 #pragma unroll UNRB

@@ -241,8 +241,8 @@ def pair_units(n, block, tj=512):
     return sum(nt - (block // tj) * i for i in range(nb_))
 
 
-PAIR_SHAPES = ((3584, 512, 1.0), (3072, 512, 0.984), (2560, 512, 0.964), (2048, 512, 0.947),
-               (2048, 256, 0.954))  # targets per CTA, tile, speed
+PAIR_SHAPES = ((3584, 512, 1.0), (3072, 512, 0.984), (2560, 512, 0.979), (2048, 512, 0.976),
+               (2048, 256, 0.967))  # targets per CTA, tile, speed
 
 
 def test_plan_pairs_path(monkeypatch):
@@ -312,7 +312,7 @@ def test_pair_path_in_chunks(n, cap, monkeypatch):
     assert rel_err(aa, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(pp, rp) <= POS_TOL
 
 
-N_PAIR_VARIANTS = 44
+N_PAIR_VARIANTS = 57
 
 
 @pytest.mark.parametrize("cfg", range(N_PAIR_VARIANTS))
