@@ -704,7 +704,8 @@ __host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, in
 // which it takes from lane l + 1 (the lane that evaluated the source at step
 // s - 1); after 32 steps lane l holds the warp's whole sum for source
 // (l + 31) mod 32.  That costs 6 shuffles per source and step and no adds or
-// selects; UNRB then unrolls the 32 steps.
+// selects; UNRB then unrolls the 32 steps.  ROT = 2: two groups of 32 sources
+// rotate side by side, each lane carrying two independent sums.
 template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0, int ROT = 0>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
@@ -913,29 +914,29 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
           }
         } else {
 #pragma unroll UNRB
-        for (int b0 = 0; b0 < TJ; b0 += NB) {
-          float vx[NB], vy[NB], vz[NB];
+          for (int b0 = 0; b0 < TJ; b0 += NB) {
+            float vx[NB], vy[NB], vz[NB];
 #pragma unroll
-          for (int q = 0; q < NB; ++q) {
-            const float4 lo = src[2 * (b0 + q)];
-            const float4 hi = src[2 * (b0 + q) + 1];
-            float2 bx = make_float2(0.f, 0.f), by = bx, bz = bx;
+            for (int q = 0; q < NB; ++q) {
+              const float4 lo = src[2 * (b0 + q)];
+              const float4 hi = src[2 * (b0 + q) + 1];
+              float2 bx = make_float2(0.f, 0.f), by = bx, bz = bx;
 #pragma unroll
-            for (int p = 0; p < P; ++p)
-              interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
-                             make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
-                             nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
-            vx[q] = bx.x + bx.y;
-            vy[q] = by.x + by.y;
-            vz[q] = bz.x + bz.y;
+              for (int p = 0; p < P; ++p)
+                interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                               make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                               nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+              vx[q] = bx.x + bx.y;
+              vy[q] = by.x + by.y;
+              vz[q] = bz.x + bz.y;
+            }
+            const float3 r = reduce_scatter<NB>(vx, vy, vz, lane);
+            if ((lane & ((1 << kShift) - 1)) == 0) {
+              red[warp][0][b0 + (lane >> kShift)] = r.x;
+              red[warp][1][b0 + (lane >> kShift)] = r.y;
+              red[warp][2][b0 + (lane >> kShift)] = r.z;
+            }
           }
-          const float3 r = reduce_scatter<NB>(vx, vy, vz, lane);
-          if ((lane & ((1 << kShift) - 1)) == 0) {
-            red[warp][0][b0 + (lane >> kShift)] = r.x;
-            red[warp][1][b0 + (lane >> kShift)] = r.y;
-            red[warp][2][b0 + (lane >> kShift)] = r.z;
-          }
-        }
         }
         __syncthreads();
         // the unit's reaction partial: the NW warps' sums in warp order
