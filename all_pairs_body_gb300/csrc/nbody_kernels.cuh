@@ -19,12 +19,14 @@
 //                       it writes a partial sum for the second pass.
 //   finish_streamk      second pass for the tiled kernel: sums the partials
 //                       of split i-blocks in CTA (= j) order and finishes.
-//   force_pairs<KI,NT,TJ,NB,UNRB,ACC>
+//   force_pairs<KI,NT,TJ,NB,UNRB,ACC,ROT>
 //                       the tiled kernel with each pair of bodies in
 //                       different i-blocks evaluated once (Newton's third
 //                       law): action on the targets in registers, reaction on
-//                       the sources reduced over the CTA (warp butterfly,
-//                       then warps in order) into one partial per unit.
+//                       the sources summed over each warp (carried from lane
+//                       to lane as the sources rotate through the lanes, or
+//                       a warp butterfly), then over the warps in order, into
+//                       one partial per unit.
 //   finish_pairs        its second pass: action + reactions in block order,
 //                       then the finish (accel or kick/drift) of every body.
 //   accumulate_pairs, finish_accumulated
@@ -596,11 +598,11 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
 // block and of every later block, tiles [TB*I, ntiles) with TB = B / TJ, in
 // that order; the (I, t) units are numbered block by block and divided
 // evenly over one wave of CTAs as in force_tiled.  For a tile past block I
-// the reaction on its TJ sources is reduced over the CTA's B targets (a warp
-// butterfly that scatters a batch of NB sources over the lanes, then the NW
-// warps in order through shared memory) and stored as that unit's partial; the
-// second pass adds, for each body, its action and the reactions from the
-// blocks before its own in block order.
+// the reaction on its TJ sources is summed over the CTA's B targets (in each
+// warp by the lane rotation or the butterfly described at force_pairs, then
+// over the NW warps in order through shared memory) and stored as that unit's
+// partial; the second pass adds, for each body, its action and the reactions
+// from the blocks before its own in block order.
 
 // Units of blocks 0 .. I-1: block I' has ntiles - TB * I' units.
 __host__ __device__ __forceinline__ long long pair_units_before(long long I, long long ntiles,

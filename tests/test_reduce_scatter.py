@@ -111,3 +111,20 @@ def test_rotation_integer_sums_are_exact():
     c = (np.arange(LANES * LANES).reshape(LANES, LANES) * 37 % 11).astype(np.float64)
     out, _ = rotate_through_lanes(c)
     assert np.array_equal(out, c.sum(axis=0)[(np.arange(LANES) + 31) % LANES])
+
+
+@pytest.mark.parametrize("tj,groups", [(512, 1), (512, 2), (256, 2), (640, 1)])
+def test_rotation_covers_each_source_of_a_tile(tj, groups):
+    """The kernel's indices for a tile of tj sources: group g (32 * groups
+    sources), step s, lane l and group h read source g + 32 h + (l + s) mod 32;
+    lane l stores the sum of source g + 32 h + (l + 31) mod 32.  Every source
+    is read once by every lane and stored by exactly one lane."""
+    lane = np.arange(LANES)
+    reads = np.zeros((tj, LANES), dtype=np.int64)
+    stores = np.zeros(tj, dtype=np.int64)
+    for g in range(0, tj, 32 * groups):
+        for h in range(groups):
+            for step in range(LANES):
+                np.add.at(reads, (g + 32 * h + (lane + step) % LANES, lane), 1)
+            np.add.at(stores, g + 32 * h + (lane + 31) % LANES, 1)
+    assert np.all(reads == 1) and np.all(stores == 1)
