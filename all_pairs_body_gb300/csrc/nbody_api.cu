@@ -13,6 +13,7 @@
 #include <map>
 #include <mutex>
 #include <algorithm>
+#include <atomic>
 #include <utility>
 #include <vector>
 
@@ -195,21 +196,23 @@ std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 
-// measurement hooks (nbody_profile_enable / nbody_profile_read)
+// measurement hooks (nbody_profile_enable / nbody_profile_read), with a lock
+// of their own: calls on several threads may record while another reads
 struct Profile {
-  bool enabled = false;
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> force_events;
-  long long kernel_launches = 0;
+  std::atomic<bool> enabled{false};
+  std::mutex mu;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> force_events;  // guarded by mu
+  std::atomic<long long> kernel_launches{0};
 };
 Profile g_prof;
 
 void count_launches(int k) {
-  if (g_prof.enabled) g_prof.kernel_launches += k;
+  if (g_prof.enabled.load(std::memory_order_relaxed)) g_prof.kernel_launches += k;
 }
 
 // Record an event on `st` (profiling only); returns nullptr when disabled.
 cudaEvent_t prof_event(cudaStream_t st) {
-  if (!g_prof.enabled) return nullptr;
+  if (!g_prof.enabled.load(std::memory_order_relaxed)) return nullptr;
   cudaEvent_t ev = nullptr;
   if (cudaEventCreate(&ev) != cudaSuccess) {
     cudaGetLastError();
@@ -217,6 +220,18 @@ cudaEvent_t prof_event(cudaStream_t st) {
   }
   cudaEventRecord(ev, st);
   return ev;
+}
+
+// Keep the events around one force launch for nbody_profile_read; a lone
+// event (the other could not be created) is destroyed.
+void record_force(cudaEvent_t e0, cudaEvent_t e1) {
+  if (e0 != nullptr && e1 != nullptr) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.force_events.emplace_back(e0, e1);
+    return;
+  }
+  if (e0 != nullptr) cudaEventDestroy(e0);
+  if (e1 != nullptr) cudaEventDestroy(e1);
 }
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
@@ -648,7 +663,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
       cudaEvent_t e0 = prof_event(st);
       pc.kernel<<<static_cast<unsigned>(*grid), p.threads, pc.smem(), st>>>(a);
       cudaEvent_t e1 = prof_event(st);
-      if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+      record_force(e0, e1);
     };
     count_launches(launches_accel(p));
     long long u_base = 0, units = 0, grid = 0;
@@ -680,7 +695,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     cudaEvent_t e0 = prof_event(st);
     force_warp<kWarpKW, kWarpNW><<<grid, p.threads, 0, st>>>(a, epi);
     cudaEvent_t e1 = prof_event(st);
-    if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+    record_force(e0, e1);
     count_launches(1 + (p.second_pass ? 1 : 0));
     if (p.second_pass) {
       const long long blocks = ceil_div(n, kFinishThreads);
@@ -693,7 +708,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
   cudaEvent_t e0 = prof_event(st);
   kTiled[p.cfg].kernel<<<static_cast<unsigned>(p.grid), p.threads, 0, st>>>(a, epi);
   cudaEvent_t e1 = prof_event(st);
-  if (e0 != nullptr && e1 != nullptr) g_prof.force_events.emplace_back(e0, e1);
+  record_force(e0, e1);
   count_launches(1 + (p.second_pass ? 1 : 0));
   if (p.second_pass) {
     StreamkFinishArgs f{partial, static_cast<int>(n), p.block, p.ntiles, p.units, p.grid};
@@ -1084,13 +1099,12 @@ int nbody_plan(int64_t n, int path, int split, int64_t* out, int len) {
 }
 
 int nbody_profile_enable(int enable) {
-  std::lock_guard<std::mutex> lk(nbody::g_mu);
   nbody::g_prof.enabled = enable != 0;
   return NBODY_OK;
 }
 
 int nbody_profile_read(double* force_ms, int64_t* force_launches, int64_t* kernel_launches) {
-  std::lock_guard<std::mutex> lk(nbody::g_mu);
+  std::lock_guard<std::mutex> lk(nbody::g_prof.mu);
   double total = 0.0;
   int rc = NBODY_OK;
   for (auto& ev : nbody::g_prof.force_events) {
@@ -1106,9 +1120,9 @@ int nbody_profile_read(double* force_ms, int64_t* force_launches, int64_t* kerne
   }
   if (force_ms != nullptr) *force_ms = total;
   if (force_launches != nullptr) *force_launches = static_cast<int64_t>(nbody::g_prof.force_events.size());
-  if (kernel_launches != nullptr) *kernel_launches = nbody::g_prof.kernel_launches;
+  const long long launched = nbody::g_prof.kernel_launches.exchange(0);
+  if (kernel_launches != nullptr) *kernel_launches = launched;
   nbody::g_prof.force_events.clear();
-  nbody::g_prof.kernel_launches = 0;
   return rc;
 }
 
