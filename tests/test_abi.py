@@ -191,3 +191,32 @@ def test_layout_entry_points_validate(L):
                                         10, f(0.1), f(0.1), 1, 2, S) == nb.EINVAL  # vel/accel overlap
     assert L.nbody_leapfrog_step_layout(ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(C),
                                         10, f(0.1), f(0.1), 1, -1, S) == nb.EINVAL
+
+
+def test_strerror_covers_ebounds(L):
+    assert L.nbody_strerror(nb.EBOUNDS) == b"a device-side index check failed (checked build)"
+
+
+def test_checked_build_exports_every_declared_symbol():
+    """The index-checked library builds without a GPU and exports the same C ABI."""
+    Lc = nb.load(nbuild.build(checked=True))
+    for name in declared_functions():
+        assert hasattr(Lc, name), name
+    assert Lc.nbody_strerror(nb.EBOUNDS).startswith(b"a device-side index check")
+    # argument checks happen before any CUDA call, as in the release build
+    assert Lc.nbody_accel_with(ctypes.c_void_p(A), ctypes.c_void_p(B), -1, 0.1, 0, 0, S) == nb.EINVAL
+
+
+def test_binding_rejects_tensors_before_any_cuda_call():
+    """The Python binding checks device, dtype, layout and shape first; these
+    tensors live on the CPU or are malformed, so nothing reaches the library."""
+    torch = pytest.importorskip("torch")
+    good_shape = torch.zeros((8, 4), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        nb.accel(good_shape, 0.1, out=torch.zeros_like(good_shape))
+    with pytest.raises(TypeError, match="must be a torch.Tensor"):
+        nb.accel(good_shape.numpy(), 0.1, out=torch.zeros_like(good_shape))
+    with pytest.raises(ValueError):
+        nb.neighbors_2d(torch.zeros(8), torch.zeros(8), 0.5, 4)
+    with pytest.raises(ValueError):
+        nb.accel_layout(good_shape, torch.zeros(24), 0.1, nb.ROWS3)
