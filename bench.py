@@ -248,9 +248,27 @@ def profiled_traffic(n: int, kernel: str = "force_tiled") -> float | None:
 # ---------------------------------------------------------------------------
 
 
+# accelerations: max_i |a_gpu,i - a_ref,i| / RMS_i |a_ref,i| (3-vectors) must not pass this
+ACC_TOL = 1e-4
+
+
+def parity_errors(got, ref) -> tuple[float, float]:
+    """(max, RMS) over the bodies of |a_got,i - a_ref,i| / RMS_i |a_ref,i|,
+    |.| the Euclidean norm of the 3-vector."""
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)[:, :3]
+    ref = np.asarray(ref, dtype=np.float64)[:, :3]
+    diff = np.linalg.norm(got - ref, axis=1)
+    scale = float(np.sqrt(np.mean(np.sum(ref * ref, axis=1)))) if len(ref) else 0.0
+    scale = scale if scale > 0.0 else 1.0
+    return (float(diff.max(initial=0.0)) / scale,
+            float(np.sqrt(np.mean(diff * diff))) / scale if len(diff) else 0.0)
+
+
 def oracle_sample_rate(pos_mass, eps2: float, seconds: float, seed: int):
     """FP64 oracle on seeded target samples x all sources; returns
-    (Ginteractions/s, targets, threads, wall seconds)."""
+    (Ginteractions/s, targets, threads, wall seconds, target indices, their
+    accelerations)."""
     import numpy as np
 
     import oracle
@@ -264,9 +282,9 @@ def oracle_sample_rate(pos_mass, eps2: float, seconds: float, seed: int):
     k = int(max(64, min(n, seconds / max(per_target, 1e-9))))
     idx = np.sort(rng.choice(n, size=k, replace=False))
     t0 = time.perf_counter()
-    oracle.accel(pos_mass, eps2, idx=idx)
+    ref = oracle.accel(pos_mass, eps2, idx=idx)
     wall = time.perf_counter() - t0
-    return k * n / wall / 1e9, k, oracle.threads(), wall
+    return k * n / wall / 1e9, k, oracle.threads(), wall, idx, ref
 
 
 MODE_TEXT = {
@@ -453,11 +471,27 @@ def run_ours(args):
         roof["frac_at_measured_clock"] = achieved / pc
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, k, cores, wall = oracle_sample_rate(w.pos_mass, w.eps2, args.cpu_seconds, 12345)
+        rate, k, cores, wall, idx, ref = oracle_sample_rate(w.pos_mass, w.eps2, args.cpu_seconds,
+                                                            12345)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{k} seeded target bodies x all {n} sources, FP64, one acceleration "
                          f"evaluation ({wall:.1f} s)"}
+    if cpu is not None and not layout:
+        # the same bodies once more through the timed path (untimed here), at the
+        # oracle's sample; a failure is reported in the line, never raised
+        try:
+            a_gpu = nb.accel(torch.from_numpy(w.pos_mass).cuda(), w.eps2, path=path,
+                             split=args.split)
+            nb.sync()
+            worst, rms = parity_errors(a_gpu.cpu().numpy()[idx], ref)
+            parity = {"max_rel_err": worst, "rms_rel_err": rms, "tolerance": ACC_TOL,
+                      "pass": worst <= ACC_TOL, "against": "FP64 oracle",
+                      "sample": f"the cpu_baseline's {k} target bodies, accelerations at the "
+                                f"initial positions"}
+        except Exception as exc:  # noqa: BLE001
+            parity = {"error": f"{type(exc).__name__}: {exc}"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -465,7 +499,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(w, args.mode, world),
         "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
-        "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "parity": parity,
         "plan": plan, "layout": args.layout, "path": args.path, "impl": "ours",
     }
     if rank == 0:

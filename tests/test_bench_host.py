@@ -140,3 +140,15 @@ def test_reference_arm_other_ranks_exit_quietly(monkeypatch):
     with contextlib.redirect_stdout(buf):
         bench.main(["--impl", "reference", "--workload", "cube-sweep-1000"])
     assert buf.getvalue() == ""
+
+
+def test_parity_errors_definition():
+    """max and RMS of |a_got,i - a_ref,i| over RMS_i |a_ref,i|, 3-vectors only."""
+    import numpy as np
+    ref = np.array([[3.0, 4.0, 0.0], [0.0, 0.0, 5.0]])  # |a| = 5 each: RMS 5
+    got = np.array([[3.0, 4.0, 0.5, 9.0], [0.0, 0.0, 5.0, -9.0]])  # w ignored
+    worst, rms = bench.parity_errors(got, ref)
+    assert worst == pytest.approx(0.5 / 5.0)
+    assert rms == pytest.approx(np.sqrt((0.25 + 0.0) / 2) / 5.0)
+    assert bench.parity_errors(ref, ref) == (0.0, 0.0)
+    assert bench.ACC_TOL == 1e-4
