@@ -32,7 +32,7 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
            "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
            "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d",
-           "nbody_accel_layout", "nbody_leapfrog_step_layout")
+           "nbody_accel_layout", "nbody_leapfrog_step_layout", "nbody_table")
 ROWS4, ROWS3, BLOCKS3 = 0, 1, 2
 NOALLOC_MAX_N = 65536
 
@@ -73,6 +73,7 @@ def load(path: str) -> ctypes.CDLL:
         "nbody_sync": [p],
         "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
         "nbody_selftest_timeout": [i32, p],
+        "nbody_table": [i32, i32, ctypes.POINTER(i64), i32],
         "nbody_profile_enable": [i32],
         "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
                                ctypes.POINTER(i64)],
@@ -260,6 +261,16 @@ def plan(n: int, path: int = PATH_AUTO, split: int = 0) -> dict:
     out = (ctypes.c_int64 * len(PLAN_FIELDS))()
     _check(lib().nbody_plan(int(n), int(path), int(split), out, len(PLAN_FIELDS)), "nbody_plan")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+TABLE_FIELDS = ("rows", "targets_per_thread", "threads", "tile", "form_or_acc", "rot")
+
+
+def table_row(which: int, row: int) -> dict:
+    """Shape of row ``row`` of this build's tiled (0) or pair (1) kernel table."""
+    out = (ctypes.c_int64 * len(TABLE_FIELDS))()
+    _check(lib().nbody_table(int(which), int(row), out, len(TABLE_FIELDS)), "nbody_table")
+    return dict(zip(TABLE_FIELDS, (int(v) for v in out)))
 
 
 def release() -> None:

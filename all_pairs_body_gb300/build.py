@@ -18,6 +18,10 @@ LIB = os.path.join(HERE, "libnbody_gb300.so")
 # The index-checked build (NBODY_BOUNDS_CHECK): every computed index into a
 # scratch or output array is tested on the device; for tests, not for use.
 LIB_CHECKED = os.path.join(HERE, "libnbody_gb300_checked.so")
+# The tuning build (NBODY_TUNING_TABLE): the release library plus every other
+# kernel shape and scheme measured while choosing the release rows, reachable
+# through NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG; for tests and sweeps.
+LIB_TUNING = os.path.join(HERE, "libnbody_gb300_tuning.so")
 SOURCES = ["nbody_api.cu"]
 DEPS = SOURCES + ["nbody_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,15 +35,17 @@ def nvcc() -> str:
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
-          checked: bool = False) -> str:
-    out = LIB_CHECKED if checked else LIB
+          checked: bool = False, tuning: bool = False) -> str:
+    if checked and tuning:
+        raise ValueError("the checked and the tuning builds are separate libraries")
+    out = LIB_CHECKED if checked else (LIB_TUNING if tuning else LIB)
     deps = [os.path.join(CSRC, s) for s in DEPS] + [os.path.join(INCLUDE, "nbody.h")]
     if not force and os.path.exists(out):
         t = os.path.getmtime(out)
         if all(os.path.getmtime(d) <= t for d in deps):
             return out
     tmp = out + f".tmp{os.getpid()}"
-    flags = ["-DNBODY_BOUNDS_CHECK"] if checked else []
+    flags = ["-DNBODY_BOUNDS_CHECK"] if checked else (["-DNBODY_TUNING_TABLE"] if tuning else [])
     cmd = ([nvcc()] + ARCH + NVCC_FLAGS + flags + ["-I", INCLUDE, "-I", CSRC] + list(extra or [])
            + ["-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcudart"])
     if verbose:

@@ -45,11 +45,17 @@ struct TiledConfig {
 };
 
 // Target bodies per thread, threads per CTA, sources per tile (kernel
-// template: + minimum CTAs per SM for the register cap, + j unroll).
+// template: + minimum CTAs per SM for the register cap, + j unroll).  The
+// release build holds the rows the plans use; the tuning build
+// (NBODY_TUNING_TABLE) appends the other shapes and the mixed
+// rsqrt/logarithmic loop, reachable through NBODY_TILED_CONFIG.
 const TiledConfig kTiled[] = {
+    {10, 256, 512, 0, force_tiled<10, 256, 512, 1, 2, 0, 0>},  // large n, 512-source tiles
+    {10, 256, 256, 0, force_tiled<10, 256, 256, 1, 2, 0, 0>},  // large n, 256-source tiles
+    {4, 128, 128, 0, force_tiled<4, 128, 128, 2, 4, 0, 0>},  // no-allocation entry point
+    {2, 128, 64, 0, force_tiled<2, 128, 64, 4, 4, 0, 0>},  // forced one-sided paths at small n
+#ifdef NBODY_TUNING_TABLE
     {8, 256, 256, 0, force_tiled<8, 256, 256, 1, 4, 0, 0>},
-    {4, 128, 128, 0, force_tiled<4, 128, 128, 2, 4, 0, 0>},
-    {2, 128, 64, 0, force_tiled<2, 128, 64, 4, 4, 0, 0>},
     {8, 128, 256, 0, force_tiled<8, 128, 256, 2, 4, 0, 0>},
     {8, 128, 256, 0, force_tiled<8, 128, 256, 3, 4, 0, 0>},
     {6, 256, 256, 0, force_tiled<6, 256, 256, 1, 4, 0, 0>},
@@ -67,10 +73,10 @@ const TiledConfig kTiled[] = {
     {4, 256, 256, 1, force_tiled<4, 256, 256, 2, 4, 1, 1>},
     {6, 256, 256, 1, force_tiled<6, 256, 256, 1, 4, 1, 2>},
     {8, 128, 256, 1, force_tiled<8, 128, 256, 3, 2, 1, 2>},
-    {10, 256, 256, 0, force_tiled<10, 256, 256, 1, 2, 0, 0>},
-    {10, 256, 512, 0, force_tiled<10, 256, 512, 1, 2, 0, 0>},
+#endif
 };
 constexpr int kNumTiled = sizeof(kTiled) / sizeof(kTiled[0]);
+constexpr int kTiledLarge512 = 0, kTiledLarge256 = 1, kTiledNoAlloc = 2, kTiledSmall = 3;
 
 using PairKernel = void (*)(const PairArgs);
 
@@ -78,73 +84,103 @@ struct PairConfig {
   int ki, nt, tj;
   PairKernel kernel;
   int acc;  // running sums in shared memory (the kernel's ACC)
-  size_t smem() const { return pair_reduce_smem(ki, nt, tj, acc); }  // dynamic shared memory
+  int rot;  // the kernel's ROT
+  size_t smem() const { return pair_reduce_smem(ki, nt, tj, acc, rot); }  // dynamic shared memory
 };
 
 // Shapes of the pair-symmetric kernel (targets per thread, threads, tile;
 // template: + reduction batch, batch or step unroll, running sums in shared
-// memory, lane rotation: 1 group of 32 sources or 2 side by side).  Rows
-// 0-4 rotate the sources through the lanes and are the plan's candidates,
-// the first the default; rows 5-27 reduce the reactions in batches
-// (ROT = 0); rows 28- are further rotation shapes.
+// memory, reaction scheme ROT).  The release build holds the plan's
+// candidates: the lane rotation with one-step-ahead loads, scalar carries and
+// duplicated groups (ROT 3; two groups side by side, ROT 4, for the smaller
+// shapes), the first the default.  The tuning build (NBODY_TUNING_TABLE)
+// appends the earlier schemes and shapes: batches reduced by a warp butterfly
+// (ROT 0) and the plain lane rotation (ROT 1, 2), reachable through
+// NBODY_PAIRS_CONFIG.
 const PairConfig kPairs[] = {
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 1>, 1},
-    {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 1>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 2>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 2>, 1},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 2>, 0},
-    {14, 256, 512, force_pairs<14, 256, 512, 16, 1, 1>, 1},
-    {12, 256, 512, force_pairs<12, 256, 512, 16, 1>, 0},
-    {10, 256, 512, force_pairs<10, 256, 512, 16, 1>, 0},
-    {10, 256, 512, force_pairs<10, 256, 512, 8, 1>, 0},
-    {8, 256, 512, force_pairs<8, 256, 512, 8, 1>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 8, 1>, 0},
-    {10, 256, 256, force_pairs<10, 256, 256, 8, 1>, 0},
-    {8, 256, 128, force_pairs<8, 256, 128, 8, 1>, 0},
-    {8, 256, 512, force_pairs<8, 256, 512, 16, 1>, 0},
-    {8, 256, 512, force_pairs<8, 256, 512, 8, 2>, 0},
-    {6, 256, 512, force_pairs<6, 256, 512, 16, 1>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 16, 1>, 0},
-    {6, 256, 512, force_pairs<6, 256, 512, 8, 2>, 0},
-    {10, 256, 640, force_pairs<10, 256, 640, 16, 1>, 0},
-    {10, 256, 320, force_pairs<10, 256, 320, 16, 1>, 0},
-    {12, 256, 384, force_pairs<12, 256, 384, 16, 1>, 0},
-    {14, 256, 512, force_pairs<14, 256, 512, 16, 1>, 0},
-    {12, 256, 512, force_pairs<12, 256, 512, 8, 1>, 0},
-    {16, 256, 512, force_pairs<16, 256, 512, 16, 1>, 0},
-    {12, 256, 256, force_pairs<12, 256, 256, 16, 1>, 0},
-    {12, 256, 512, force_pairs<12, 256, 512, 16, 1, 1>, 1},
-    {16, 256, 512, force_pairs<16, 256, 512, 16, 1, 1>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 16, 1, 1>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 1>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 1>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 1>, 0},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 1>, 1},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 1>, 1},
-    {16, 256, 512, force_pairs<16, 256, 512, 32, 2, 1, 1>, 1},
-    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 1>, 1},
-    {18, 256, 512, force_pairs<18, 256, 512, 32, 2, 1, 1>, 1},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 8, 1, 1>, 1},
-    {16, 256, 512, force_pairs<16, 256, 512, 32, 4, 1, 1>, 1},
-    {16, 256, 512, force_pairs<16, 256, 512, 32, 1, 1, 1>, 1},
-    {14, 256, 256, force_pairs<14, 256, 256, 32, 2, 1, 1>, 1},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 0, 1>, 0},
-    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 0, 1>, 0},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 1>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 1>, 1},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 1>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 0, 1>, 0},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 1>, 0},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 2>, 1},
-    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 2>, 1},
-    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 2>, 1},
-    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 2>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 2>, 0},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 2>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 0, 2>, 0},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 2>, 1},
-    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 1, 2>, 1},
-    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 1, 2>, 1},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 8, 1, 3>, 1, 3},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 0, 3>, 0, 3},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 4>, 1, 4},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 4>, 1, 4},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 0, 4>, 0, 4},
+#ifdef NBODY_TUNING_TABLE
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 1>, 1, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 2>, 1, 2},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 2>, 1, 2},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 2>, 0, 2},
+    {14, 256, 512, force_pairs<14, 256, 512, 16, 1, 1>, 1, 0},
+    {12, 256, 512, force_pairs<12, 256, 512, 16, 1>, 0, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 16, 1>, 0, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 8, 1>, 0, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 1>, 0, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 8, 1>, 0, 0},
+    {10, 256, 256, force_pairs<10, 256, 256, 8, 1>, 0, 0},
+    {8, 256, 128, force_pairs<8, 256, 128, 8, 1>, 0, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 16, 1>, 0, 0},
+    {8, 256, 512, force_pairs<8, 256, 512, 8, 2>, 0, 0},
+    {6, 256, 512, force_pairs<6, 256, 512, 16, 1>, 0, 0},
+    {8, 256, 256, force_pairs<8, 256, 256, 16, 1>, 0, 0},
+    {6, 256, 512, force_pairs<6, 256, 512, 8, 2>, 0, 0},
+    {10, 256, 640, force_pairs<10, 256, 640, 16, 1>, 0, 0},
+    {10, 256, 320, force_pairs<10, 256, 320, 16, 1>, 0, 0},
+    {12, 256, 384, force_pairs<12, 256, 384, 16, 1>, 0, 0},
+    {14, 256, 512, force_pairs<14, 256, 512, 16, 1>, 0, 0},
+    {12, 256, 512, force_pairs<12, 256, 512, 8, 1>, 0, 0},
+    {16, 256, 512, force_pairs<16, 256, 512, 16, 1>, 0, 0},
+    {12, 256, 256, force_pairs<12, 256, 256, 16, 1>, 0, 0},
+    {12, 256, 512, force_pairs<12, 256, 512, 16, 1, 1>, 1, 0},
+    {16, 256, 512, force_pairs<16, 256, 512, 16, 1, 1>, 1, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 16, 1, 1>, 1, 0},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 1>, 1, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 1>, 0, 1},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 1>, 0, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 1>, 1, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 1>, 1, 1},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {18, 256, 512, force_pairs<18, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 8, 1, 1>, 1, 1},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 4, 1, 1>, 1, 1},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 1, 1, 1>, 1, 1},
+    {14, 256, 256, force_pairs<14, 256, 256, 32, 2, 1, 1>, 1, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 0, 1>, 0, 1},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 0, 1>, 0, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 1, 1>, 1, 1},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 1>, 1, 1},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 2, 0, 1>, 0, 1},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 1>, 0, 1},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 2>, 1, 2},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 2>, 1, 2},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 2>, 1, 2},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 2>, 1, 2},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 2, 0, 2>, 0, 2},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 0, 2>, 0, 2},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 0, 2>, 0, 2},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 2, 1, 2>, 1, 2},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 1, 2>, 1, 2},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 1, 2>, 1, 2},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 2, 1, 3>, 1, 3},
+    {10, 256, 512, force_pairs<10, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {8, 256, 512, force_pairs<8, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {8, 256, 256, force_pairs<8, 256, 256, 32, 4, 0, 3>, 0, 3},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 8, 1, 3>, 1, 3},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 2, 1, 3>, 1, 3},
+    {18, 256, 512, force_pairs<18, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {18, 256, 512, force_pairs<18, 256, 512, 32, 2, 1, 3>, 1, 3},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 2, 1, 3>, 1, 3},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 8, 1, 3>, 1, 3},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 0, 3>, 0, 3},
+    {16, 256, 512, force_pairs<16, 256, 512, 32, 1, 1, 3>, 1, 3},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 1, 1, 3>, 1, 3},
+    {20, 256, 512, force_pairs<20, 256, 512, 32, 4, 1, 3>, 1, 3},
+    {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 4>, 1, 4},
+    {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 4>, 1, 4},
+#endif
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
@@ -332,7 +368,7 @@ struct LargeShape {
   int cfg;
   double speed;
 };
-constexpr LargeShape kLargeShapes[] = {{21, 1.0}, {20, 0.973}};
+constexpr LargeShape kLargeShapes[] = {{kTiledLarge512, 1.0}, {kTiledLarge256, 0.973}};
 
 long long streamk_grid(long long units, const DeviceInfo& d, int cfg) {
   const long long per_sm = env_int("NBODY_CTAS_PER_SM", d.occupancy[cfg]);
@@ -362,7 +398,7 @@ int choose_large_shape(long long n, const DeviceInfo& d) {
 int auto_tiled_config(long long n, bool streamk, const DeviceInfo& d) {
   const long long forced = env_int("NBODY_TILED_CONFIG", -1);
   if (forced >= 0 && forced < kNumTiled) return static_cast<int>(forced);
-  if (n <= kWarpMaxN) return 2;  // forced TILED/SPLIT at small n: the smallest blocks
+  if (n <= kWarpMaxN) return kTiledSmall;  // forced TILED/SPLIT at small n: the smallest blocks
   return streamk ? choose_large_shape(n, d) : kLargeShapes[0].cfg;
 }
 
@@ -407,13 +443,13 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
   p->second_pass = p->slices > 1;
 }
 
-// Pair shapes the plan chooses between, with their speed per interaction
-// relative to the first, measured at n = 2^20 (force kernel 270.7, 275.2,
-// 276.5, 277.4 and 279.8 ms per pass, the last two in two chunks): more
-// targets per CTA are faster per interaction; smaller blocks and tiles cut
-// the work into more units, which wins when a CTA's share of units is small.
-constexpr LargeShape kPairShapes[] = {
-    {0, 1.0}, {1, 0.984}, {2, 0.979}, {3, 0.976}, {4, 0.967}};
+// Pair shapes the plan chooses between (the release rows), with their speed
+// per interaction relative to the first, measured at n = 2^20 (force kernel
+// 264.9, 265.0, 272.0, 271.4, 277.0 and 275.6 ms per pass): more targets per
+// CTA are faster per interaction; smaller blocks and tiles cut the work into
+// more units, which wins when a CTA's share of units is small.
+constexpr LargeShape kPairShapes[] = {{0, 1.0},   {1, 0.9995}, {2, 0.974},
+                                      {3, 0.976}, {4, 0.956},  {5, 0.961}};
 
 long long pair_units_of(long long n, const PairConfig& pc) {
   const long long block = static_cast<long long>(pc.ki) * pc.nt;
@@ -889,7 +925,7 @@ int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int 
 namespace nbody {
 namespace {
 // force_tiled<4, 128, 128, 2, 4, 0, 0>: 512 targets per i-block, 128-source tiles.
-constexpr int kNoAllocCfg = 1;
+constexpr int kNoAllocCfg = kTiledNoAlloc;
 constexpr long long kNoAllocMaxGrid = 384;
 constexpr long long kNoAllocRows = kNoAllocMaxGrid * 2 * 512;  // partial sums: 6 MiB of float4
 constexpr int kNoAllocMaxDevices = 64;
@@ -1098,6 +1134,27 @@ int nbody_plan(int64_t n, int path, int split, int64_t* out, int len) {
   return NBODY_OK;
 }
 
+int nbody_table(int which, int row, int64_t* out, int len) {
+  using namespace nbody;
+  if (out == nullptr && len > 0) return NBODY_EINVAL;
+  int64_t v[6] = {};
+  if (which == 0) {
+    if (row < 0 || row >= kNumTiled) return NBODY_EINVAL;
+    const TiledConfig& c = kTiled[row];
+    const int64_t w[] = {kNumTiled, c.ki, c.nt, c.tj, c.form, 0};
+    std::copy(w, w + 6, v);
+  } else if (which == 1) {
+    if (row < 0 || row >= kNumPairs) return NBODY_EINVAL;
+    const PairConfig& c = kPairs[row];
+    const int64_t w[] = {kNumPairs, c.ki, c.nt, c.tj, c.acc, c.rot};
+    std::copy(w, w + 6, v);
+  } else {
+    return NBODY_EINVAL;
+  }
+  for (int k = 0; k < len && k < 6; ++k) out[k] = v[k];
+  return NBODY_OK;
+}
+
 int nbody_profile_enable(int enable) {
   nbody::g_prof.enabled = enable != 0;
   return NBODY_OK;
@@ -1173,7 +1230,7 @@ int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   // One CTA of each tile-copying kernel whose first copy is never issued:
   // the smallest one-sided tiled kernel over one i-block, and the default
   // pair kernel over two i-blocks (zero bodies; only the wait matters).
-  constexpr int kCfg = 2;  // smallest tiled kernel (4 KB tiles)
+  constexpr int kCfg = kTiledSmall;  // smallest tiled kernel (4 KB tiles)
   const TiledConfig& tc = kTiled[kCfg];
   const PairConfig& pc = kPairs[0];
   const long long n1 = static_cast<long long>(tc.ki) * tc.nt;

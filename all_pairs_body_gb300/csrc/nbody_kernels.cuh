@@ -24,9 +24,9 @@
 //                       different i-blocks evaluated once (Newton's third
 //                       law): action on the targets in registers, reaction on
 //                       the sources summed over each warp (carried from lane
-//                       to lane as the sources rotate through the lanes, or
-//                       a warp butterfly), then over the warps in order, into
-//                       one partial per unit.
+//                       to lane as the sources rotate through the lanes, or,
+//                       in the tuning build, a warp butterfly), then over the
+//                       warps in order, into one partial per unit.
 //   finish_pairs        its second pass: action + reactions in block order,
 //                       then the finish (accel or kick/drift) of every body.
 //   accumulate_pairs, finish_accumulated
@@ -176,6 +176,8 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // against two target bodies whose NEGATED coordinates are (nx, ny, nz):
 //   r = x_j - x_i, d = |r|^2 + eps2, q = d^(-1/2), s = m_j q^3, a += s r.
 // 12 packed-pair FP32 instructions and 2 MUFU.RSQ for two interactions.
+// q^3 is formed as (q q) q and then scaled by the mass, the order the
+// pair-symmetric kernel uses, so that both kernels round every term alike.
 __device__ __forceinline__ void interact2(float2 X, float2 Y, float2 Z, float2 M, float2 nx,
                                           float2 ny, float2 nz, float2 e2, float2& ax, float2& ay,
                                           float2& az) {
@@ -186,8 +188,8 @@ __device__ __forceinline__ void interact2(float2 X, float2 Y, float2 Z, float2 M
   d = __ffma2_rn(ry, ry, d);
   d = __ffma2_rn(rz, rz, d);
   const float2 q = make_float2(rsqrt_approx(d.x), rsqrt_approx(d.y));
-  const float2 q2 = __fmul2_rn(q, q);
-  const float2 s = __fmul2_rn(__fmul2_rn(M, q), q2);
+  const float2 q3 = __fmul2_rn(__fmul2_rn(q, q), q);
+  const float2 s = __fmul2_rn(M, q3);
   ax = __ffma2_rn(rx, s, ax);
   ay = __ffma2_rn(ry, s, ay);
   az = __ffma2_rn(rz, s, az);
@@ -339,6 +341,27 @@ __device__ __noinline__ void expand_tile_split(const float4* raw, float4* tile, 
     const float4 x = b < live ? raw[b] : make_float4(0.f, 0.f, 0.f, 0.f);
     tile[b] = make_float4(x.x, x.x, x.y, x.y);
     tile[tj + b] = make_float4(x.z, x.z, x.w, x.w);
+  }
+}
+
+// The same with every group of 32 sources stored twice in a row, so that a
+// lane reading the sources of its group in rotated order, (l + s) mod 32 for
+// steps s = 0..31, reads rows l, l + 1, ..., l + 31 of the group's 64 rows:
+// constant offsets from one base address, no wrap-around.  Source b of the
+// tile sits at rows 64 (b / 32) + (b mod 32) and 32 rows further, first half
+// (x, x, y, y) in rows [0, 2 tj), second half (z, z, m, m) in rows
+// [2 tj, 4 tj).
+__device__ __noinline__ void expand_tile_dup(const float4* raw, float4* tile, int tj, int nt,
+                                             int tid, long long live) {
+  for (int b = tid; b < tj; b += nt) {
+    const float4 x = b < live ? raw[b] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int r = 64 * (b >> 5) + (b & 31);
+    const float4 lo = make_float4(x.x, x.x, x.y, x.y);
+    const float4 hi = make_float4(x.z, x.z, x.w, x.w);
+    tile[r] = lo;
+    tile[r + 32] = lo;
+    tile[2 * tj + r] = hi;
+    tile[2 * tj + r + 32] = hi;
   }
 }
 
@@ -687,10 +710,12 @@ __device__ __forceinline__ float3 reduce_scatter(float (&vx)[NB], float (&vy)[NB
   return make_float3(vx[0], vy[0], vz[0]);
 }
 
-// Dynamic shared memory of force_pairs: the per-warp reaction sums of a tile,
-// and with ACC = 1 the targets' running action sums.
-__host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, int acc) {
-  return static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float) +
+// Dynamic shared memory of force_pairs: with ROT >= 3 first the two-stage
+// ring of the caller's source rows (the TMA targets), then the per-warp
+// reaction sums of a tile, and with ACC = 1 the targets' running action sums.
+__host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, int acc, int rot) {
+  return (rot >= 3 ? static_cast<size_t>(2) * tj * sizeof(float4) : 0) +
+         static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float) +
          (acc ? static_cast<size_t>(3) * ki * nt * sizeof(float) : 0);
 }
 
@@ -708,21 +733,36 @@ __host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, in
 // (l + 31) mod 32.  That costs 6 shuffles per source and step and no adds or
 // selects; UNRB then unrolls the 32 steps.  ROT = 2: two groups of 32 sources
 // rotate side by side, each lane carrying two independent sums.
+//
+// ROT = 3 (the default shapes): the rotation of ROT = 1 with three changes
+// that each measured faster in isolation.  (a) The lane passes on one scalar
+// per component: its 7 target pairs add to (carried sum, 0) in the packed
+// chain and the two halves are added before the shuffle, 3 shuffles and 3
+// scalar adds per step instead of 6 shuffles.  (b) The next step's source is
+// loaded from shared memory one step ahead into registers.  (c) The tile
+// keeps each group of 32 sources twice in a row (expand_tile_dup), so the 32
+// steps read 32 consecutive rows from one base address with constant offsets.
+// The expanded tile then needs 32 KB, so the TMA ring moves into dynamic
+// shared memory.  ROT = 4: the same with two groups side by side.
 template <int KI, int NT, int TJ, int NB, int UNRB, int ACC = 0, int ROT = 0>
 __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   static_assert(KI % 2 == 0, "targets are processed in packed pairs");
   static_assert((KI * NT) % TJ == 0 && TJ % NB == 0, "tiles tile an i-block; batches tile a tile");
-  static_assert(ROT == 0 || TJ % (32 * ROT) == 0, "rotation groups of 32 sources tile a tile");
+  constexpr int kGroups = ROT == 2 || ROT == 4 ? 2 : 1;  // rotation groups side by side
+  static_assert(ROT == 0 || TJ % (32 * kGroups) == 0, "rotation groups of 32 sources tile a tile");
   constexpr int kShift = NB == 8 ? 2 : 1;  // lane l holds source l >> kShift of a batch
   constexpr int P = KI / 2;
   constexpr int NW = NT / 32;
   constexpr long long B = static_cast<long long>(KI) * NT;
   constexpr long long TB = B / TJ;
+  constexpr bool kDup = ROT >= 3;  // duplicated-group tile (expand_tile_dup)
 
-  __shared__ __align__(128) float4 raw[2][TJ];    // TMA targets: the caller's rows
-  __shared__ __align__(128) float4 tile[2 * TJ];  // expanded: (x,x,y,y),(z,z,m,m)
+  __shared__ __align__(128) float4 raw_s[kDup ? 1 : 2 * TJ];  // TMA targets (ROT < 3)
+  __shared__ __align__(128) float4 tile[kDup ? 4 * TJ : 2 * TJ];  // expanded sources
   __shared__ __align__(8) unsigned long long bar[2];
-  extern __shared__ __align__(16) float react_smem[];  // [NW][3][TJ] (+ running sums)
+  extern __shared__ __align__(128) float4 pair_smem[];  // (ring) + [NW][3][TJ] (+ running sums)
+  float4* const raw = kDup ? pair_smem : raw_s;  // [2][TJ]: the caller's rows
+  float* const react_smem = reinterpret_cast<float*>(kDup ? pair_smem + 2 * TJ : pair_smem);
   auto red = reinterpret_cast<float(*)[3][TJ]>(react_smem);
   float2* const acc_s = reinterpret_cast<float2*>(react_smem + NW * 3 * TJ);  // ACC = 1
   auto acc_at = [&](int c, int p) -> float2& { return acc_s[(c * P + p) * NT + threadIdx.x]; };
@@ -734,8 +774,8 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   const long long u_lo = a.u_base + unit_begin(a.units, a.grid, c);  // global unit index
   const long long count = unit_begin(a.units, a.grid, c + 1) - unit_begin(a.units, a.grid, c);
   const uint32_t bar0 = smem_u32(&bar[0]);
-  const uint32_t raw0 = smem_u32(&raw[0][0]);
-  constexpr uint32_t kRawStride = sizeof(raw[0]);
+  const uint32_t raw0 = smem_u32(raw);
+  constexpr uint32_t kRawStride = TJ * sizeof(float4);
   auto bar_of = [&](long long k) { return bar0 + static_cast<uint32_t>(k & 1) * 8u; };
   auto raw_of = [&](long long k) { return raw0 + static_cast<uint32_t>(k & 1) * kRawStride; };
 
@@ -818,10 +858,12 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
         break;
       }
       if (tid == 0 && k + 1 < count) issue_next(k + 1);
-      if constexpr (ROT >= 1)
-        expand_tile_split(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
+      if constexpr (kDup)
+        expand_tile_dup(raw + s * TJ, tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
+      else if constexpr (ROT >= 1)
+        expand_tile_split(raw + s * TJ, tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
       else
-        (void)expand_tile(raw[s], tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
+        (void)expand_tile(raw + s * TJ, tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
       __syncthreads();
 
       float2 tx[P], ty[P], tz[P];
@@ -832,17 +874,82 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
       constexpr int kHi = ROT >= 1 ? TJ : 1;  // its second half: kLo * j + kHi
       if (t < TB * (blk + 1)) {
         // a tile of the block itself: both sides of each pair, as in force_tiled
+        if constexpr (kDup) {
+          for (int g = 0; g < TJ; g += 32) {
 #pragma unroll 2
-        for (int j = 0; j < TJ; ++j) {
-          const float4 lo = src[kLo * j];
-          const float4 hi = src[kLo * j + kHi];
+            for (int j = 0; j < 32; ++j) {
+              const float4 lo = src[2 * g + j];
+              const float4 hi = src[2 * TJ + 2 * g + j];
 #pragma unroll
-          for (int p = 0; p < P; ++p)
-            interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w), make_float2(hi.x, hi.y),
-                      make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+              for (int p = 0; p < P; ++p)
+                interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                          make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p], nz[p],
+                          e2, tx[p], ty[p], tz[p]);
+            }
+          }
+        } else {
+#pragma unroll 2
+          for (int j = 0; j < TJ; ++j) {
+            const float4 lo = src[kLo * j];
+            const float4 hi = src[kLo * j + kHi];
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+              interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w), make_float2(hi.x, hi.y),
+                        make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+          }
         }
       } else {
-        if constexpr (ROT == 1) {
+        if constexpr (ROT == 3 || ROT == 4) {
+          constexpr unsigned kAll = 0xffffffffu;
+          const int from = (lane + 1) & 31;
+          for (int g = 0; g < TJ; g += 32 * kGroups) {
+            // rows of this lane's step-0 sources; step st reads st rows further
+            const float4* lo0 = src + 2 * g + lane;
+            const float4* hi0 = src + 2 * TJ + 2 * g + lane;
+            float4 clo[kGroups], chi[kGroups];
+            float bxs[kGroups], bys[kGroups], bzs[kGroups];
+#pragma unroll
+            for (int h = 0; h < kGroups; ++h) {
+              clo[h] = lo0[64 * h];
+              chi[h] = hi0[64 * h];
+              bxs[h] = bys[h] = bzs[h] = 0.f;
+            }
+#pragma unroll UNRB
+            for (int st = 0; st < 32; ++st) {
+#pragma unroll
+              for (int h = 0; h < kGroups; ++h) {
+                const float4 lo = clo[h];
+                const float4 hi = chi[h];
+                if (st + 1 < 32) {  // the next step's source, one step ahead
+                  clo[h] = lo0[64 * h + st + 1];
+                  chi[h] = hi0[64 * h + st + 1];
+                }
+                // this source's sum over the lanes before, from lane + 1
+                bxs[h] = __shfl_sync(kAll, bxs[h], from);
+                bys[h] = __shfl_sync(kAll, bys[h], from);
+                bzs[h] = __shfl_sync(kAll, bzs[h], from);
+                float2 bx = make_float2(bxs[h], 0.f), by = make_float2(bys[h], 0.f),
+                       bz = make_float2(bzs[h], 0.f);
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                  interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                                 make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                                 nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+                bxs[h] = bx.x + bx.y;
+                bys[h] = by.x + by.y;
+                bzs[h] = bz.x + bz.y;
+              }
+            }
+            // lane l now holds the warp's sum for source (l + 31) mod 32 of each group
+#pragma unroll
+            for (int h = 0; h < kGroups; ++h) {
+              const int jj = g + 32 * h + ((lane + 31) & 31);
+              red[warp][0][jj] = bxs[h];
+              red[warp][1][jj] = bys[h];
+              red[warp][2][jj] = bzs[h];
+            }
+          }
+        } else if constexpr (ROT == 1) {
           constexpr unsigned kAll = 0xffffffffu;
           const int from = (lane + 1) & 31;
           for (int g = 0; g < TJ; g += 32) {

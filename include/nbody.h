@@ -313,6 +313,24 @@ int nbody_accel_noalloc(const float *pos_mass, float *accel, int64_t n,
 int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
 
 /*
+ * Rows of this build's kernel tables (for tests and tuning sweeps; the
+ * NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG environment variables select a row
+ * by its index).  which = 0: the one-sided tiled kernel, 1: the
+ * pair-symmetric kernel.  out[0..len) receives, as far as len allows:
+ *   [0] rows in the table   [1] target bodies per thread   [2] threads per CTA
+ *   [3] sources per tile    [4] tiled: 1 for the mixed rsqrt/logarithmic
+ *                               loop; pairs: 1 for running sums in shared
+ *                               memory
+ *   [5] pairs: the reaction scheme (0 warp butterfly over batches, 1 and 2
+ *       lane rotation with one or two groups, 3 and 4 the same with loads one
+ *       step ahead, scalar carries and duplicated groups); tiled: 0.
+ * The release build holds only the rows its plans use; the tuning build
+ * (compiled with NBODY_TUNING_TABLE) appends the others.  Needs no device.
+ * Returns NBODY_OK or NBODY_EINVAL (unknown table or row).
+ */
+int nbody_table(int which, int row, int64_t *out, int len);
+
+/*
  * Measurement hooks.  While enabled (nonzero), every force-kernel launch is
  * bracketed by a pair of CUDA events recorded on its own stream, and every
  * kernel launch of the library is counted.  nbody_profile_read waits for the
