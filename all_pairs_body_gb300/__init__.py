@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(HERE, "libnbody_gb300.so")
 PATH_AUTO, PATH_TILED, PATH_SPLIT, PATH_WARP, PATH_PAIRS = 0, 1, 2, 3, 4
 OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBOUNDS = 0, 1, 2, 3, 4, 5
 PLAN_FIELDS = ("path", "grid", "threads", "bodies_per_cta", "tile", "tiles", "units",
-               "second_pass", "launches_accel", "launches_step", "sms")
+               "second_pass", "launches_accel", "launches_step", "sms", "react_bytes", "chunks")
 
 EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_leapfrog_step", "nbody_leapfrog_step_on_stream",
@@ -32,7 +32,8 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_release", "nbody_selftest_timeout", "nbody_profile_enable",
            "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
            "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d",
-           "nbody_accel_layout", "nbody_leapfrog_step_layout", "nbody_table")
+           "nbody_accel_layout", "nbody_leapfrog_step_layout", "nbody_table",
+           "nbody_last_plan", "nbody_selftest_timeout_enqueue")
 ROWS4, ROWS3, BLOCKS3 = 0, 1, 2
 NOALLOC_MAX_N = 65536
 
@@ -73,6 +74,8 @@ def load(path: str) -> ctypes.CDLL:
         "nbody_sync": [p],
         "nbody_plan": [i64, i32, i32, ctypes.POINTER(i64), i32],
         "nbody_selftest_timeout": [i32, p],
+        "nbody_selftest_timeout_enqueue": [i32, p],
+        "nbody_last_plan": [p, ctypes.POINTER(i64), i32],
         "nbody_table": [i32, i32, ctypes.POINTER(i64), i32],
         "nbody_profile_enable": [i32],
         "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
@@ -144,9 +147,11 @@ def accel_noalloc(pos_mass, out, eps2: float, stream=None):
     """Accelerations into ``out`` without any allocation by the library.
 
     For callers that must not allocate device memory when they ask for
-    accelerations; the work memory is one fixed 6 MiB array per GPU that the
-    library holds until exit.  n <= NOALLOC_MAX_N.  Calls must not overlap on
-    the GPU (they share the array).  ``out`` must be allocated by the caller.
+    accelerations (a host whose own pool owns the device memory, a loop that
+    bans allocation after start-up); the work memory is one fixed 6 MiB array
+    per GPU that the library holds until exit.  n <= NOALLOC_MAX_N.  Calls
+    must not overlap on the GPU (they share the array).  ``out`` must be
+    allocated by the caller.
     """
     n = int(pos_mass.shape[0])
     rc = lib().nbody_accel_noalloc(_rows(pos_mass, None, "pos_mass"), _rows(out, n, "out"), n,
@@ -252,7 +257,8 @@ def leapfrog_step_layout(pos_mass, vel, accel_out, eps2: float, dt: float, steps
 
 
 def sync(stream=None) -> None:
-    """Wait for the stream and raise if a kernel reported a device-side failure."""
+    """Wait for the stream and raise if a kernel this library enqueued on it
+    reported a device-side failure."""
     _check(lib().nbody_sync(_stream(stream)), "nbody_sync")
 
 
@@ -271,6 +277,14 @@ def table_row(which: int, row: int) -> dict:
     out = (ctypes.c_int64 * len(TABLE_FIELDS))()
     _check(lib().nbody_table(int(which), int(row), out, len(TABLE_FIELDS)), "nbody_table")
     return dict(zip(TABLE_FIELDS, (int(v) for v in out)))
+
+
+def last_plan(stream=None) -> dict:
+    """Plan of the last force pass enqueued on the stream (the one that ran,
+    after any fallback when the pair path's scratch could not be allocated)."""
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(lib().nbody_last_plan(_stream(stream), out, len(PLAN_FIELDS)), "nbody_last_plan")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
 
 
 def release() -> None:
@@ -296,3 +310,9 @@ def profile_read() -> tuple[float, int, int]:
 def selftest_timeout(timeout_ms: int = 100, stream=None) -> int:
     """Run the bounded-wait check; a correct build returns ETIMEOUT."""
     return int(lib().nbody_selftest_timeout(int(timeout_ms), _stream(stream)))
+
+
+def selftest_timeout_enqueue(timeout_ms: int = 100, stream=None) -> int:
+    """Enqueue the bounded-wait check without waiting; its ETIMEOUT stays in
+    the stream's status word for nbody_sync on that stream."""
+    return int(lib().nbody_selftest_timeout_enqueue(int(timeout_ms), _stream(stream)))

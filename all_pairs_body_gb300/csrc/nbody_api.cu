@@ -189,8 +189,9 @@ constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 // N = 2^20 and B = 3584).  Where they exceed this many bytes the pass runs
 // in chunks of consecutive i-blocks whose rows fit, each chunk's reactions
 // folded into a per-body accumulator before the next chunk reuses the rows;
-// NBODY_PAIRS_MAX_BYTES overrides it.
-constexpr long long kPairsMaxBytes = 4LL << 30;
+// NBODY_PAIRS_MAX_BYTES overrides it.  The chunks cost nothing measurable
+// (two more launches each and 32 bytes per body of accumulator traffic).
+constexpr long long kPairsMaxBytes = 1LL << 30;
 
 struct DeviceInfo {
   int sms = 0;
@@ -222,10 +223,17 @@ struct Buf {
   size_t bytes = 0;
 };
 
+// Everything the library keeps for one (device, stream): the stream's status
+// word, the scratch of its calls, and the plan of the last force pass it
+// enqueued there (nbody_last_plan).
 struct Scratch {
+  Buf status;      // int: NBODY_OK until a kernel on this stream records a failure
   Buf pos_alt, partial;
   Buf act, react;  // pair path: whole-block action sums, per-unit reaction sums
   Buf pair_acc;    // pair path in chunks: per-body running sums
+  Buf check[4];    // nbody_selftest_timeout_enqueue: its private problem
+  Plan last;       // the last force pass enqueued on this stream
+  bool has_last = false;
 };
 
 std::mutex g_mu;
@@ -272,37 +280,35 @@ void record_force(cudaEvent_t e0, cudaEvent_t e1) {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// Capacities for the index checks of the checked build (a no-op otherwise):
-// rows of the per-body arrays, float4 rows of `partial` and of the reaction
-// sums, ints of the neighbour list.  NBODY_BOUNDS_SHRINK=<slot> (rows,
-// partial, react, neighbors) sets one capacity to 0 so that a test can see
-// the checks fire; every access they stop is skipped, none goes out of bounds.
-void set_caps(long long rows, long long partial, long long react, long long neighbors,
-              cudaStream_t st) {
+// The control block of one launch: the stream's status word and, in the
+// checked build, the capacities for the index checks: rows of the per-body
+// arrays, float4 rows of `partial` and of the reaction sums, ints of the
+// neighbour list.  They travel as a kernel argument, so calls on different
+// streams never see each other's.  NBODY_BOUNDS_SHRINK=<slot> (rows, partial,
+// react, neighbors) sets one capacity to 0 so that a test can see the checks
+// fire; every access they stop is skipped, none goes out of bounds.
+Ctl make_ctl(int* status, long long rows, long long partial, long long react,
+             long long neighbors) {
+  Ctl c;
+  c.status = status;
 #ifdef NBODY_BOUNDS_CHECK
-  long long caps[kNumCaps] = {};
-  caps[kCapRows] = rows;
-  caps[kCapPartial] = partial;
-  caps[kCapReact] = react;
-  caps[kCapNeighbors] = neighbors;
+  c.caps[kCapRows] = rows;
+  c.caps[kCapPartial] = partial;
+  c.caps[kCapReact] = react;
+  c.caps[kCapNeighbors] = neighbors;
   if (const char* v = std::getenv("NBODY_BOUNDS_SHRINK")) {
     const char* names[kNumCaps] = {"rows", "partial", "react", "neighbors"};
     for (int k = 0; k < kNumCaps; ++k)
-      if (std::strcmp(v, names[k]) == 0) caps[k] = 0;
+      if (std::strcmp(v, names[k]) == 0) c.caps[k] = 0;
   }
-  cudaMemcpyToSymbolAsync(g_caps, caps, sizeof(caps), 0, cudaMemcpyHostToDevice, st);
 #else
-  (void)rows, (void)partial, (void)react, (void)neighbors, (void)st;
+  (void)rows, (void)partial, (void)react, (void)neighbors;
 #endif
+  return c;
 }
 
 long long float4_rows(const void* p, size_t bytes) {
   return p == nullptr ? 0 : static_cast<long long>(bytes / sizeof(float4));
-}
-
-bool env_flag(const char* name) {
-  const char* v = std::getenv(name);
-  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
 }
 
 long long env_int(const char* name, long long dflt) {
@@ -543,23 +549,46 @@ int launches_accel(const Plan& p) {
 
 int launches_step1(const Plan& p) { return launches_accel(p); }
 
+// Bytes of reaction rows the pair path keeps (0 for the other paths).
+long long react_bytes(const Plan& p) {
+  if (p.path != NBODY_PATH_PAIRS) return 0;
+  const long long rows = p.chunks() > 1 ? p.chunk_units : p.units;
+  return rows * p.tj * static_cast<long long>(sizeof(float4));
+}
+
+// The fields nbody_plan and nbody_last_plan report, as far as len allows.
+void write_plan(const Plan& p, int64_t* out, int len) {
+  const int64_t v[] = {p.path,  p.grid,  p.threads, p.block,
+                       p.tj,    p.ntiles, p.units,  p.second_pass ? 1 : 0,
+                       launches_accel(p), launches_step1(p), p.sms, react_bytes(p), p.chunks()};
+  const int nv = static_cast<int>(sizeof(v) / sizeof(v[0]));
+  for (int k = 0; k < len && k < nv; ++k) out[k] = v[k];
+}
+
 // --------------------------------------------------------------------------
 // scratch
 // --------------------------------------------------------------------------
 
-int ensure(Buf& b, size_t bytes, cudaStream_t st) {
+// Grow `b` to at least `bytes` with stream-ordered allocation on `st`: the
+// old block is released after the stream's earlier work and the new one is
+// ready for its later work, with no host synchronisation.  Host-side fault
+// injection: NBODY_FAULT_ALLOC=1 fails every allocation, NBODY_FAULT_ALLOC=
+// <kind> only those of that kind ("pairs": the pair path's reaction rows).
+int ensure(Buf& b, size_t bytes, cudaStream_t st, const char* kind = "") {
   if (bytes == 0 || b.bytes >= bytes) return NBODY_OK;
-  if (env_flag("NBODY_FAULT_ALLOC")) return NBODY_ENOMEM;  // host-side fault injection
+  if (const char* v = std::getenv("NBODY_FAULT_ALLOC")) {
+    if (std::strcmp(v, "1") == 0 || (kind[0] != '\0' && std::strcmp(v, kind) == 0))
+      return NBODY_ENOMEM;
+  }
   if (b.p != nullptr) {
-    if (cudaStreamSynchronize(st) != cudaSuccess) {
+    if (cudaFreeAsync(b.p, st) != cudaSuccess) {
       cudaGetLastError();
       return NBODY_ECUDA;
     }
-    cudaFree(b.p);
     b.p = nullptr;
     b.bytes = 0;
   }
-  if (cudaMalloc(&b.p, bytes) != cudaSuccess) {
+  if (cudaMallocAsync(&b.p, bytes, st) != cudaSuccess) {
     cudaGetLastError();
     b.p = nullptr;
     return NBODY_ENOMEM;
@@ -568,17 +597,39 @@ int ensure(Buf& b, size_t bytes, cudaStream_t st) {
   return NBODY_OK;
 }
 
+// The status word of (dev, st): allocated and zeroed on the stream's first
+// use.  Called with g_mu held.
+int ensure_status(Scratch& s, cudaStream_t st) {
+  if (s.status.p != nullptr) return NBODY_OK;
+  if (cudaMallocAsync(&s.status.p, sizeof(int4), st) != cudaSuccess) {
+    cudaGetLastError();
+    s.status.p = nullptr;
+    return NBODY_ENOMEM;
+  }
+  s.status.bytes = sizeof(int4);
+  if (cudaMemsetAsync(s.status.p, 0, sizeof(int4), st) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  return NBODY_OK;
+}
+
+Scratch& scratch_of(int dev, cudaStream_t st) {
+  return g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
+}
+
 int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapfrog,
                 Scratch** out) {
   std::lock_guard<std::mutex> lk(g_mu);
-  Scratch& s = g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
-  int rc = NBODY_OK;
+  Scratch& s = scratch_of(dev, st);
+  int rc = ensure_status(s, st);
+  if (rc != NBODY_OK) return rc;
   if (p.path == NBODY_PATH_PAIRS) {
-    rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
-    if (rc == NBODY_OK) rc = ensure(s.act, static_cast<size_t>(n) * sizeof(float4), st);
     const long long rows = p.chunks() > 1 ? p.chunk_units : p.units;
+    rc = ensure(s.react, static_cast<size_t>(rows) * p.tj * sizeof(float4), st, "pairs");
     if (rc == NBODY_OK)
-      rc = ensure(s.react, static_cast<size_t>(rows) * p.tj * sizeof(float4), st);
+      rc = ensure(s.partial, static_cast<size_t>(p.grid) * 2 * p.block * sizeof(float4), st);
+    if (rc == NBODY_OK) rc = ensure(s.act, static_cast<size_t>(n) * sizeof(float4), st);
     if (rc == NBODY_OK && p.chunks() > 1)
       rc = ensure(s.pair_acc, static_cast<size_t>(n) * sizeof(float4), st);
   } else if (p.path != NBODY_PATH_WARP) {
@@ -647,6 +698,7 @@ Epilogue make_epilogue(const float4* pos, void* accel, void* vel, float4* pos_ne
   e.dt = dt;
   e.layout = layout;
   e.n = n;
+  e.ctl = Ctl{};  // set by the launch
   return e;
 }
 
@@ -660,11 +712,20 @@ bool vec_aligned(const void* p, int layout) {
   return layout == kRows4 ? (a & 15u) == 0 : (a & 3u) == 0;
 }
 
-// One force pass (plus its second pass): sources and targets `pos`, finished
-// through `epi`.
+// The status word of the calling stream, for launches that need no other
+// scratch (the point shaders, the neighbour list).
+int stream_status(int dev, cudaStream_t st, int** status) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Scratch& s = scratch_of(dev, st);
+  const int rc = ensure_status(s, st);
+  *status = static_cast<int*>(s.status.p);
+  return rc;
+}
+
 // Plan a force pass and get its scratch.  When the automatic plan chose the
 // pair path and its reaction partials cannot be allocated, the one-sided
-// stream-K plan (far less scratch) is taken instead.
+// stream-K plan (far less scratch) is taken instead; nbody_last_plan reports
+// which plan a call used.
 int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st, bool leapfrog,
                       Plan* p, Scratch** s) {
   int rc = make_plan(n, path, split, dev, p);
@@ -674,14 +735,23 @@ int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st
     if ((rc = make_plan(n, NBODY_PATH_SPLIT, 0, dev, p)) != NBODY_OK) return rc;
     rc = get_scratch(dev, st, *p, n, leapfrog, s);
   }
+  if (rc == NBODY_OK) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    (*s)->last = *p;
+    (*s)->has_last = true;
+  }
   return rc;
 }
 
+// One force pass (plus its second pass): sources and targets `pos`, finished
+// through `epi`, with the stream's status word and the scratch of `s`.
 void launch_force(const Plan& p, const float4* pos, long long n, float eps2, const Scratch& s,
-                  const Epilogue& epi, cudaStream_t st) {
+                  const Epilogue& epi_in, cudaStream_t st) {
   float4* partial = static_cast<float4*>(s.partial.p);
-  set_caps(n, float4_rows(s.partial.p, s.partial.bytes), float4_rows(s.react.p, s.react.bytes), 0,
-           st);
+  const Ctl ctl = make_ctl(static_cast<int*>(s.status.p), n, float4_rows(s.partial.p, s.partial.bytes),
+                           float4_rows(s.react.p, s.react.bytes), 0);
+  Epilogue epi = epi_in;
+  epi.ctl = ctl;
   if (p.path == NBODY_PATH_PAIRS) {
     const PairConfig& pc = kPairs[p.cfg];
     const long long tb = p.block / p.tj;
@@ -695,7 +765,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
       *grid = std::min(*units, p.grid_max);
       PairArgs a{pos,    static_cast<int>(n), eps2,    p.ntiles, p.nblocks,    *u_base,
                  *units, *grid,               act,     partial,  react,        kWaitLimitNs,
-                 -1};
+                 -1,     ctl};
       cudaEvent_t e0 = prof_event(st);
       pc.kernel<<<static_cast<unsigned>(*grid), p.threads, pc.smem(), st>>>(a);
       cudaEvent_t e1 = prof_event(st);
@@ -705,8 +775,9 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     long long u_base = 0, units = 0, grid = 0;
     if (p.chunks() == 1) {
       force_chunk(0, p.nblocks, &u_base, &units, &grid);
-      PairFinishArgs f{act,  partial, react,  static_cast<int>(n), p.block, p.tj,
-                       p.ntiles, u_base, units, grid, 0, p.nblocks};
+      PairFinishArgs f{act,      partial, react, static_cast<int>(n), p.block, p.tj,
+                       p.ntiles, u_base,  units, grid,                0,       p.nblocks,
+                       ctl};
       finish_pairs<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0, st>>>(
           f, epi);
       return;
@@ -715,8 +786,9 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     for (int k = 0; k < p.chunks(); ++k) {
       const long long I0 = p.chunk_start[k], I1 = p.chunk_start[k + 1];
       force_chunk(I0, I1, &u_base, &units, &grid);
-      PairFinishArgs f{act,  partial, react,  static_cast<int>(n), p.block, p.tj,
-                       p.ntiles, u_base, units, grid, I0, I1};
+      PairFinishArgs f{act,      partial, react, static_cast<int>(n), p.block, p.tj,
+                       p.ntiles, u_base,  units, grid,                I0,      I1,
+                       ctl};
       const long long bodies = n - I0 * p.block;
       accumulate_pairs<<<static_cast<unsigned>(ceil_div(bodies, kFinishThreads)), kFinishThreads,
                          0, st>>>(f, acc, k == 0 ? 1 : 0);
@@ -856,6 +928,8 @@ int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float
     if ((rc = check_device_pointer(ptr, dev)) != NBODY_OK) return rc;
   DeviceInfo d;
   if ((rc = device_info(dev, &d)) != NBODY_OK) return rc;
+  int* status = nullptr;
+  if ((rc = stream_status(dev, st, &status)) != NBODY_OK) return rc;
   RenderArgs a;
   a.pos = reinterpret_cast<const float4*>(pos_mass);
   a.ndc = reinterpret_cast<float4*>(ndc);
@@ -866,9 +940,9 @@ int render_impl(const float* pos_mass, float* ndc, float* rgba, int64_t n, float
                         static_cast<float>(2.0 / (2.0 * max_z)));
   a.min_w = min_w;
   a.inv_range = static_cast<float>(1.0 / (static_cast<double>(max_w) - min_w));
+  a.ctl = make_ctl(status, n, 0, 0, 0);
   const long long blocks = std::min(ceil_div(n, 256), static_cast<long long>(d.sms) * 8);
   count_launches(1);
-  set_caps(n, 0, 0, 0, st);
   render_points<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return launch_status();
 }
@@ -906,10 +980,12 @@ int neighbors_impl(const float* x, const float* y, int64_t n, float cutoff, int 
                           static_cast<const void*>(nn)})
     if ((rc = check_device_pointer(ptr, dev)) != NBODY_OK) return rc;
   if (max_neighbors > 0 && (rc = check_device_pointer(nl, dev)) != NBODY_OK) return rc;
-  NeighborArgs a{x, y, static_cast<int>(n), c2, max_neighbors, nn, nl, ceil_div(n, kNeighborNT)};
+  int* status = nullptr;
+  if ((rc = stream_status(dev, st, &status)) != NBODY_OK) return rc;
+  NeighborArgs a{x,  y,  static_cast<int>(n), c2, max_neighbors, nn, nl, ceil_div(n, kNeighborNT),
+                 make_ctl(status, n, 0, 0, n * static_cast<long long>(max_neighbors))};
   const long long blocks = ceil_div(n, static_cast<long long>(kNeighborKI) * kNeighborNT);
   count_launches(1);
-  set_caps(n, 0, 0, n * static_cast<long long>(max_neighbors), st);
   neighbors_2d<kNeighborKI, kNeighborNT, kNeighborU>
       <<<static_cast<unsigned>(blocks), kNeighborNT, 0, st>>>(a);
   return launch_status();
@@ -933,15 +1009,20 @@ constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
   bool ready = false;
   float4* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int* status = nullptr;      // device address of g_noalloc_status on this device
   int sms = 0;
   int occupancy = 0;
+  bool called = false;        // a call was enqueued since nbody_sync last read the status
+  uintptr_t last_stream = 0;  // the stream of the last call
 };
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];  // fixed table: no allocation
 }  // namespace
 }  // namespace nbody
 
-// Working memory of nbody_accel_noalloc: the partial sums of split i-blocks.
+// Working memory of nbody_accel_noalloc: the partial sums of split i-blocks,
+// and the status word its kernels report a failed bounded wait in.
 static __device__ __align__(256) float4 g_noalloc_scratch[nbody::kNoAllocRows];
+static __device__ int g_noalloc_status;
 
 namespace nbody {
 namespace {
@@ -954,7 +1035,9 @@ int noalloc_setup(int dev, NoAllocDevice* out) {
   NoAllocDevice& d = g_noalloc_dev[dev];
   if (!d.ready) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
+        cudaGetSymbolAddress(&status, g_noalloc_status) != cudaSuccess || status == nullptr) {
       cudaGetLastError();
       return NBODY_ECUDA;
     }
@@ -966,6 +1049,7 @@ int noalloc_setup(int dev, NoAllocDevice* out) {
       return NBODY_ECUDA;
     }
     d.scratch = static_cast<float4*>(ptr);
+    d.status = static_cast<int*>(status);
     d.sms = sms;
     d.occupancy = occ > 0 ? occ : 1;
     d.ready = true;
@@ -990,6 +1074,11 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
   if ((rc = check_device_pointer(accel, dev)) != NBODY_OK) return rc;
   NoAllocDevice d;
   if ((rc = noalloc_setup(dev, &d)) != NBODY_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_noalloc_dev[dev].called = true;
+    g_noalloc_dev[dev].last_stream = reinterpret_cast<uintptr_t>(st);
+  }
 
   const TiledConfig& tc = kTiled[kNoAllocCfg];
   const long long block = static_cast<long long>(tc.ki) * tc.nt;
@@ -1002,9 +1091,9 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
 
   const float4* pos = reinterpret_cast<const float4*>(pos_mass);
   float4* partial = d.scratch;  // every slot a call reads, the same call writes first
-  const Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, kRows4, n);
+  Epilogue epi = make_epilogue(pos, accel, nullptr, nullptr, 0.f, 0.f, kRows4, n);
+  epi.ctl = make_ctl(d.status, n, kNoAllocRows, 0, 0);
   TiledArgs a{pos, static_cast<int>(n), eps2, ntiles, units, grid, partial, kWaitLimitNs, -1};
-  set_caps(n, kNoAllocRows, 0, 0, st);
   tc.kernel<<<static_cast<unsigned>(grid), tc.nt, 0, st>>>(a, epi);
   if (second) {
     StreamkFinishArgs f{partial, static_cast<int>(n), block, ntiles, units, grid};
@@ -1012,6 +1101,64 @@ int accel_noalloc_impl(const float* pos_mass, float* accel, int64_t n, float eps
                                                                                                epi);
   }
   return launch_status();
+}
+
+// The failure-detection check: one CTA of each tile-copying kernel whose
+// first copy is never issued, with a wait limit of timeout_ms: the smallest
+// one-sided tiled kernel over one i-block (which & 1), and the default pair
+// kernel over two i-blocks (which & 2), on zero bodies (only the wait
+// matters).  Its buffers are the stream's scratch; the expired waits go to
+// the stream's status word.
+int selftest_enqueue(int timeout_ms, cudaStream_t st, int which) {
+  if (timeout_ms <= 0) return NBODY_EINVAL;
+  int rc = NBODY_OK, dev = 0;
+  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
+  DeviceInfo d;
+  if ((rc = device_info(dev, &d)) != NBODY_OK) return rc;  // sets the kernels' attributes
+  const uint64_t limit = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+  const TiledConfig& tc = kTiled[kTiledSmall];
+  const PairConfig& pc = kPairs[0];
+  const long long n1 = static_cast<long long>(tc.ki) * tc.nt;
+  const long long pb = static_cast<long long>(pc.ki) * pc.nt;
+  const long long n2 = 2 * pb;
+  const long long nt2 = ceil_div(n2, pc.tj);
+  const long long units2 = pair_units_before(2, nt2, pb / pc.tj);
+  const size_t sizes[] = {static_cast<size_t>(n2) * sizeof(float4),  // positions (both)
+                          static_cast<size_t>(n2) * sizeof(float4),  // accel / action
+                          static_cast<size_t>(2 * pb) * sizeof(float4),
+                          static_cast<size_t>(units2 * pc.tj) * sizeof(float4)};
+  float4* buf[4] = {};
+  int* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Scratch& s = scratch_of(dev, st);
+    if ((rc = ensure_status(s, st)) != NBODY_OK) return rc;
+    for (int k = 0; k < 4; ++k) {
+      if ((rc = ensure(s.check[k], sizes[k], st)) != NBODY_OK) return rc;
+      buf[k] = static_cast<float4*>(s.check[k].p);
+    }
+    status = static_cast<int*>(s.status.p);
+  }
+  if (cudaMemsetAsync(buf[0], 0, sizes[0], st) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  const Ctl ctl = make_ctl(status, n2, 2 * pb, units2 * pc.tj, 0);
+  if (which & 1) {
+    TiledArgs a{buf[0], static_cast<int>(n1), 1.0f, ceil_div(n1, tc.tj), ceil_div(n1, tc.tj), 1,
+                nullptr, limit, 0};
+    Epilogue epi = make_epilogue(buf[0], buf[1], nullptr, nullptr, 0.f, 0.f, kRows4, n1);
+    epi.ctl = ctl;
+    tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
+    if ((rc = launch_status()) != NBODY_OK) return rc;
+  }
+  if (which & 2) {
+    PairArgs pa{buf[0], static_cast<int>(n2), 1.0f, nt2, 2, 0, units2, 1, buf[1], buf[2], buf[3],
+                limit, 0, ctl};
+    pc.kernel<<<1, pc.nt, pc.smem(), st>>>(pa);
+    if ((rc = launch_status()) != NBODY_OK) return rc;
+  }
+  return NBODY_OK;
 }
 
 }  // namespace
@@ -1099,23 +1246,65 @@ int nbody_leapfrog_step_layout(float* pos_mass, float* vel, float* accel, int64_
 }
 
 int nbody_sync(void* cuda_stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+  using namespace nbody;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
     cudaGetLastError();
     return NBODY_ECUDA;
   }
-  int status = 0;
-  if (cudaMemcpyFromSymbol(&status, nbody::g_status, sizeof(int)) != cudaSuccess) {
-    cudaGetLastError();
-    return NBODY_ECUDA;
+  int dev = 0;
+  if (current_device(&dev) != NBODY_OK) return NBODY_ECUDA;
+  // the status words this stream's kernels write: the stream's own, and the
+  // no-allocation entry point's if its last call ran on this stream
+  int* words[2] = {nullptr, nullptr};
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(st)));
+    if (it != g_scratch.end()) words[0] = static_cast<int*>(it->second.status.p);
+    if (dev >= 0 && dev < kNoAllocMaxDevices) {
+      NoAllocDevice& d = g_noalloc_dev[dev];
+      if (d.ready && d.called && d.last_stream == reinterpret_cast<uintptr_t>(st)) {
+        words[1] = d.status;
+        d.called = false;
+      }
+    }
   }
-  if (status != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(nbody::g_status, &zero, sizeof(int)) != cudaSuccess) {
+  int status = NBODY_OK;
+  for (int* w : words) {
+    if (w == nullptr) continue;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, w, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
       cudaGetLastError();
       return NBODY_ECUDA;
     }
+    if (v != NBODY_OK) {
+      if (status == NBODY_OK) status = v;
+      if (cudaMemsetAsync(w, 0, sizeof(int), st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return NBODY_ECUDA;
+      }
+    }
   }
   return status;
+}
+
+int nbody_last_plan(void* cuda_stream, int64_t* out, int len) {
+  using namespace nbody;
+  if (out == nullptr && len > 0) return NBODY_EINVAL;
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != NBODY_OK) return rc;
+  Plan p;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_scratch.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(cuda_stream)));
+    if (it == g_scratch.end() || !it->second.has_last) return NBODY_EINVAL;
+    p = it->second.last;
+  }
+  write_plan(p, out, len);
+  return NBODY_OK;
 }
 
 int nbody_plan(int64_t n, int path, int split, int64_t* out, int len) {
@@ -1126,11 +1315,7 @@ int nbody_plan(int64_t n, int path, int split, int64_t* out, int len) {
   if ((rc = nbody::current_device(&dev)) != NBODY_OK) return rc;
   nbody::Plan p;
   if ((rc = nbody::make_plan(n > 0 ? n : 1, path, split, dev, &p)) != NBODY_OK) return rc;
-  const int64_t v[] = {p.path,  p.grid,  p.threads, p.block,
-                       p.tj,    p.ntiles, p.units,  p.second_pass ? 1 : 0,
-                       nbody::launches_accel(p), nbody::launches_step1(p), p.sms};
-  const int nv = static_cast<int>(sizeof(v) / sizeof(v[0]));
-  for (int k = 0; k < len && k < nv; ++k) out[k] = v[k];
+  nbody::write_plan(p, out, len);
   return NBODY_OK;
 }
 
@@ -1205,9 +1390,10 @@ void nbody_release(void) {
       continue;
     }
     cudaDeviceSynchronize();
-    for (nbody::Buf* b : {&kv.second.pos_alt, &kv.second.partial, &kv.second.act,
-                          &kv.second.react, &kv.second.pair_acc}) {
-      if (b->p != nullptr) cudaFree(b->p);
+    nbody::Scratch& s = kv.second;
+    for (nbody::Buf* b : {&s.status, &s.pos_alt, &s.partial, &s.act, &s.react, &s.pair_acc,
+                          &s.check[0], &s.check[1], &s.check[2], &s.check[3]}) {
+      if (b->p != nullptr) cudaFree(b->p);  // stream-ordered blocks; the device is idle
       b->p = nullptr;
       b->bytes = 0;
     }
@@ -1217,62 +1403,18 @@ void nbody_release(void) {
   cudaGetLastError();
 }
 
+int nbody_selftest_timeout_enqueue(int timeout_ms, void* cuda_stream) {
+  return nbody::selftest_enqueue(timeout_ms, static_cast<cudaStream_t>(cuda_stream), 3);
+}
+
 int nbody_selftest_timeout(int timeout_ms, void* cuda_stream) {
   using namespace nbody;
-  if (timeout_ms <= 0) return NBODY_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  int rc = NBODY_OK, dev = 0;
-  if ((rc = current_device(&dev)) != NBODY_OK) return rc;
-  DeviceInfo d;
-  if ((rc = device_info(dev, &d)) != NBODY_OK) return rc;  // sets the kernels' attributes
-  const uint64_t limit = static_cast<uint64_t>(timeout_ms) * 1000000ull;
-
-  // One CTA of each tile-copying kernel whose first copy is never issued:
-  // the smallest one-sided tiled kernel over one i-block, and the default
-  // pair kernel over two i-blocks (zero bodies; only the wait matters).
-  constexpr int kCfg = kTiledSmall;  // smallest tiled kernel (4 KB tiles)
-  const TiledConfig& tc = kTiled[kCfg];
-  const PairConfig& pc = kPairs[0];
-  const long long n1 = static_cast<long long>(tc.ki) * tc.nt;
-  const long long pb = static_cast<long long>(pc.ki) * pc.nt;
-  const long long n2 = 2 * pb;
-  const long long nt2 = ceil_div(n2, pc.tj);
-  const long long units2 = pair_units_before(2, nt2, pb / pc.tj);
-  const size_t sizes[] = {static_cast<size_t>(n2) * sizeof(float4),  // positions (both)
-                          static_cast<size_t>(n2) * sizeof(float4),  // accel / action
-                          static_cast<size_t>(2 * pb) * sizeof(float4),
-                          static_cast<size_t>(units2 * pc.tj) * sizeof(float4)};
-  float4* buf[4] = {nullptr, nullptr, nullptr, nullptr};
-  auto free_all = [&]() {
-    for (float4*& b : buf) {
-      cudaFree(b);
-      b = nullptr;
-    }
-  };
-  for (int k = 0; k < 4; ++k)
-    if (cudaMalloc(&buf[k], sizes[k]) != cudaSuccess) {
-      cudaGetLastError();
-      free_all();
-      return NBODY_ENOMEM;
-    }
-  cudaMemsetAsync(buf[0], 0, sizes[0], st);
-
-  TiledArgs a{buf[0], static_cast<int>(n1), 1.0f, ceil_div(n1, tc.tj), ceil_div(n1, tc.tj), 1,
-              nullptr, limit, 0};
-  const Epilogue epi = make_epilogue(buf[0], buf[1], nullptr, nullptr, 0.f, 0.f, kRows4, n1);
-  set_caps(n2, 2 * pb, units2 * pc.tj, 0, st);
-  tc.kernel<<<1, tc.nt, 0, st>>>(a, epi);
-  int rc1 = launch_status();
-  const int s1 = nbody_sync(cuda_stream);
-  if (rc1 == NBODY_OK) rc1 = s1;
-
-  PairArgs pa{buf[0], static_cast<int>(n2), 1.0f, nt2, 2, 0, units2, 1, buf[1], buf[2], buf[3],
-              limit, 0};
-  pc.kernel<<<1, pc.nt, pc.smem(), st>>>(pa);
-  int rc2 = launch_status();
-  const int s2 = nbody_sync(cuda_stream);
-  if (rc2 == NBODY_OK) rc2 = s2;
-  free_all();
+  // each kernel on its own, so that each must report the expired wait
+  int rc1 = selftest_enqueue(timeout_ms, st, 1);
+  if (rc1 == NBODY_OK) rc1 = nbody_sync(cuda_stream);
+  int rc2 = selftest_enqueue(timeout_ms, st, 2);
+  if (rc2 == NBODY_OK) rc2 = nbody_sync(cuda_stream);
   if (rc1 != NBODY_ETIMEOUT) return rc1;
   return rc2;
 }

@@ -56,16 +56,13 @@
 
 namespace nbody {
 
-// Device-side status word: NBODY_OK or NBODY_ETIMEOUT (read and cleared by
-// nbody_sync on the host).  This header is compiled into one translation unit.
-__device__ int g_status = 0;
-
 // Index checks of the checked build (compiled with NBODY_BOUNDS_CHECK): each
 // computed index into a scratch or output array is tested against the
-// capacity the host allocated (g_caps, set before the launches); a failed
-// check records NBODY_EBOUNDS (the first error wins) and the access is
-// skipped.  In the release build NBODY_IN_BOUNDS is the constant true, so
-// every guarded access compiles exactly as unguarded.
+// capacity the host allocated for that call (passed in the launch's Ctl); a
+// failed check records NBODY_EBOUNDS in the calling stream's status word
+// (the first error wins) and the access is skipped.  In the release build
+// NBODY_IN_BOUNDS is the constant true, so every guarded access compiles
+// exactly as unguarded.
 enum CapSlot : int {
   kCapRows = 0,   // rows of pos/accel/vel/pos_next/ndc/rgba and of per-body scratch
   kCapPartial,    // float4 rows of `partial`
@@ -73,16 +70,27 @@ enum CapSlot : int {
   kCapNeighbors,  // ints of the neighbour list
   kNumCaps
 };
+
+// What every launch carries besides its data: the status word of the stream
+// it runs on (NBODY_OK until a kernel records a failure; nbody_sync on that
+// stream reads and clears it), and in the checked build the capacities of
+// the call's arrays.
+struct Ctl {
+  int* status;
 #ifdef NBODY_BOUNDS_CHECK
-__device__ long long g_caps[kNumCaps];
-__device__ __noinline__ bool index_in_bounds(long long idx, int slot) {
-  if (idx >= 0 && idx < g_caps[slot]) return true;
-  atomicCAS(&g_status, 0, static_cast<int>(NBODY_EBOUNDS));
+  long long caps[kNumCaps];
+#endif
+};
+
+#ifdef NBODY_BOUNDS_CHECK
+__device__ __noinline__ bool index_in_bounds(const Ctl& c, long long idx, int slot) {
+  if (idx >= 0 && idx < c.caps[slot]) return true;
+  atomicCAS(c.status, 0, static_cast<int>(NBODY_EBOUNDS));
   return false;
 }
-#define NBODY_IN_BOUNDS(idx, slot) index_in_bounds((idx), (slot))
+#define NBODY_IN_BOUNDS(ctl, idx, slot) index_in_bounds((ctl), (idx), (slot))
 #else
-#define NBODY_IN_BOUNDS(idx, slot) true
+#define NBODY_IN_BOUNDS(ctl, idx, slot) true
 #endif
 
 // ---------------------------------------------------------------------------
@@ -256,6 +264,7 @@ struct Epilogue {
   float dt;           // drift coefficient on v
   int layout;         // VecLayout of accel and vel
   long long n;        // bodies (block stride of kBlocks3)
+  Ctl ctl;
 };
 
 __device__ __forceinline__ void store_vec3(float* base, int layout, long long n, long long i, float x,
@@ -289,7 +298,7 @@ __device__ __forceinline__ float4 load_vec3(const float* base, int layout, long 
 // schedule of the inner loop (up to 2.5% in a measured sweep).
 __device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
                                          float az) {
-  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
+  if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return;
   store_vec3(e.accel, e.layout, e.n, i, ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
     float4 v = load_vec3(e.vel, e.layout, e.n, i);
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
           const float fz = h ? az[p].y : az[p].x;
           if (whole)
             finish_body(e, i, fx, fy, fz);
-          else if (NBODY_IN_BOUNDS(slot + local, kCapPartial))
+          else if (NBODY_IN_BOUNDS(e.ctl, slot + local, kCapPartial))
             a.partial[slot + local] = make_float4(fx, fy, fz, 0.f);
         }
       }
@@ -563,7 +572,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
   }
 
   if (timed_out && tid == 0) {
-    atomicExch(&g_status, static_cast<int>(NBODY_ETIMEOUT));
+    atomicExch(e.ctl.status, static_cast<int>(NBODY_ETIMEOUT));
     // The copy of unit k may still be landing in shared memory: give it a
     // bounded wait before the CTA (and its shared memory) goes away.
     if (k != a.withhold)
@@ -596,7 +605,8 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
     // the block's segment is CTA c's first segment unless c started earlier
     const int side = unit_begin(a.units, a.grid, c) >= u0 ? 0 : 1;
     const long long at = (c * 2 + side) * a.block + local;
-    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 p =
+        NBODY_IN_BOUNDS(e.ctl, at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -647,6 +657,7 @@ struct PairArgs {
   float4* react;      // [units][TJ] reaction sums of this launch's units (local index)
   uint64_t timeout_ns;
   long long withhold;  // failure-detection check only (see TiledArgs)
+  Ctl ctl;
 };
 
 // One source (duplicated pairs X, Y, Z, M) against two targets (negated
@@ -1058,7 +1069,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             sy += red[w][1][j];
             sz += red[w][2][j];
           }
-          if (NBODY_IN_BOUNDS((u - a.u_base) * TJ + j, kCapReact))
+          if (NBODY_IN_BOUNDS(a.ctl, (u - a.u_base) * TJ + j, kCapReact))
             a.react[(u - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
         }
       }
@@ -1098,9 +1109,9 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
           }
           const float4 v = make_float4(h ? sx2.y : sx2.x, h ? sy2.y : sy2.x,
                                        h ? sz2.y : sz2.x, 0.f);
-          if (whole && NBODY_IN_BOUNDS(i, kCapRows))
+          if (whole && NBODY_IN_BOUNDS(a.ctl, i, kCapRows))
             a.act[i] = v;
-          else if (!whole && NBODY_IN_BOUNDS(slot + local, kCapPartial))
+          else if (!whole && NBODY_IN_BOUNDS(a.ctl, slot + local, kCapPartial))
             a.partial[slot + local] = v;
         }
       }
@@ -1112,7 +1123,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   }
 
   if (timed_out && tid == 0) {
-    atomicExch(&g_status, static_cast<int>(NBODY_ETIMEOUT));
+    atomicExch(a.ctl.status, static_cast<int>(NBODY_ETIMEOUT));
     if (k != a.withhold)
       (void)mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
   }
@@ -1141,6 +1152,7 @@ struct PairFinishArgs {
   long long units;   // its units
   long long grid;    // its CTAs
   long long I0, I1;  // its i-blocks (all of them for finish_pairs)
+  Ctl ctl;
 };
 
 // Action sum of body i of block I, whose units all belong to the launch
@@ -1153,7 +1165,7 @@ __device__ __forceinline__ float3 pair_action(const PairFinishArgs& a, long long
   const long long c0 = unit_owner(a.units, a.grid, u0);
   const long long c1 = unit_owner(a.units, a.grid, u1);
   if (c0 == c1) {
-    const float4 v = NBODY_IN_BOUNDS(i, kCapRows) ? a.act[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 v = NBODY_IN_BOUNDS(a.ctl, i, kCapRows) ? a.act[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     return make_float3(v.x, v.y, v.z);
   }
   float sx = 0.f, sy = 0.f, sz = 0.f;
@@ -1161,7 +1173,8 @@ __device__ __forceinline__ float3 pair_action(const PairFinishArgs& a, long long
   for (long long cc = c0; cc <= c1; ++cc) {
     const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
     const long long at = (cc * 2 + side) * a.block + local;
-    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 p =
+        NBODY_IN_BOUNDS(a.ctl, at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -1176,7 +1189,7 @@ __device__ __forceinline__ void pair_reactions(const PairFinishArgs& a, long lon
                                                float& sz) {
   for (long long J = a.I0; J < J1; ++J) {
     const long long u = pair_units_before(J, a.ntiles, tb) + t - tb * J - a.u_base;
-    const float4 r = NBODY_IN_BOUNDS(u * a.tj + j, kCapReact) ? a.react[u * a.tj + j]
+    const float4 r = NBODY_IN_BOUNDS(a.ctl, u * a.tj + j, kCapReact) ? a.react[u * a.tj + j]
                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += r.x;
     sy += r.y;
@@ -1205,7 +1218,7 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
   if (I < a.I1) s = pair_action(a, i, I, tb);
   const long long t = i / a.tj;
   pair_reactions(a, t, i - t * a.tj, min(I, a.I1), tb, s.x, s.y, s.z);
-  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
+  if (!NBODY_IN_BOUNDS(a.ctl, i, kCapRows)) return;
   if (first) {
     acc[i] = make_float4(s.x, s.y, s.z, 0.f);
   } else {
@@ -1217,7 +1230,7 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
 __global__ void finish_accumulated(const float4* acc, int n, const Epilogue e) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  if (!NBODY_IN_BOUNDS(i, kCapRows)) return;
+  if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return;
   const float4 v = acc[i];
   finish_body(e, i, v.x, v.y, v.z);
 }
@@ -1307,7 +1320,7 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
       if (a.slices == 1)
         finish_body(e, i, sx, sy, sz);
       else
-        if (NBODY_IN_BOUNDS(static_cast<long long>(blockIdx.y) * a.n + i, kCapPartial))
+        if (NBODY_IN_BOUNDS(e.ctl, static_cast<long long>(blockIdx.y) * a.n + i, kCapPartial))
           a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
     }
   }
@@ -1321,7 +1334,8 @@ __global__ void finish_slices(const float4* __restrict__ partial, int n, int sli
   float sx = 0.f, sy = 0.f, sz = 0.f;
   for (int s = 0; s < slices; ++s) {
     const long long at = static_cast<long long>(s) * n + i;
-    const float4 p = NBODY_IN_BOUNDS(at, kCapPartial) ? partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 p =
+        NBODY_IN_BOUNDS(e.ctl, at, kCapPartial) ? partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
     sx += p.x;
     sy += p.y;
     sz += p.z;
@@ -1342,6 +1356,7 @@ struct RenderArgs {
   float3 scale;      // 2 / (max_c - (-max_c)) per component
   float min_w;
   float inv_range;   // 1 / (max_w - min_w)
+  Ctl ctl;           // checked build: rows capacity (not used by the release kernel)
 };
 
 // Vertex shader: p_c = 2 (c - (-max_c)) / (max_c - (-max_c)) - 1 and
@@ -1379,6 +1394,7 @@ struct NeighborArgs {
   int* nn;              // out: neighbours per target
   int* nl;              // out: nl[k * n + i], ascending, -1 past the count
   long long ntiles;
+  Ctl ctl;
 };
 
 // All pairs in the page's single precision, every operation rounded
@@ -1464,7 +1480,7 @@ __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
               if ((h ? d2[u][p].y : d2[u][p].x) < c2 && j != i) {
                 int& c = cnt[2 * p + h];
                 if (c < a.max_neighbors)
-                  if (NBODY_IN_BOUNDS(static_cast<long long>(c) * a.n + i, kCapNeighbors))
+                  if (NBODY_IN_BOUNDS(a.ctl, static_cast<long long>(c) * a.n + i, kCapNeighbors))
                     a.nl[static_cast<long long>(c) * a.n + i] = static_cast<int>(j);
                 ++c;
               }
@@ -1480,7 +1496,7 @@ __global__ void __launch_bounds__(NT) neighbors_2d(const NeighborArgs a) {
     if (i < a.n) {
       a.nn[i] = cnt[k];
       for (int q = cnt[k]; q < a.max_neighbors; ++q)
-        if (NBODY_IN_BOUNDS(static_cast<long long>(q) * a.n + i, kCapNeighbors))
+        if (NBODY_IN_BOUNDS(a.ctl, static_cast<long long>(q) * a.n + i, kCapNeighbors))
           a.nl[static_cast<long long>(q) * a.n + i] = -1;
     }
   }

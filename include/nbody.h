@@ -28,18 +28,21 @@
  * Pointers are DEVICE pointers on the calling thread's current CUDA device
  * (cudaMalloc / cudaMallocAsync / managed memory); host pointers are
  * rejected with NBODY_EINVAL.  The caller owns every array it passes.  The
- * library owns only its cached scratch (the ping-pong positions of a
- * multi-step call, the split-j partial sums and the pair path's action and
- * reaction sums), allocated on first use per (device, stream) and freed by
- * nbody_release().
+ * library owns only what it keeps per (device, stream): a status word and
+ * its cached scratch (the ping-pong positions of a multi-step call, the
+ * split-j partial sums and the pair path's action and reaction sums).  Both
+ * come from stream-ordered allocation (cudaMallocAsync on the call's stream)
+ * on the stream's first use and when a larger call needs more, and are
+ * freed by nbody_release().
  *
  * Execution is asynchronous: a call validates its arguments, enqueues its
  * kernels on the stream and returns.  NBODY_OK means "enqueued"; a device
- * side failure (a bounded wait that expired) is reported by nbody_sync().
- * Results are bitwise deterministic for a given (n, path, split, device
- * model, library build): every sum runs in a fixed order and no atomics
- * take part in any reduction.  Calls on different streams use different
- * scratch and may run concurrently; the caller orders calls that share a
+ * side failure (a bounded wait that expired) is recorded in the stream's
+ * status word and reported by nbody_sync() on that stream.  Results are
+ * bitwise deterministic for a given (n, path, split, device model, library
+ * build): every sum runs in a fixed order and no atomics take part in any
+ * reduction.  Calls on different streams use different scratch and status
+ * words and may run concurrently; the caller orders calls that share a
  * stream, as usual.
  *
  * Errors (every entry point returns one of these codes):
@@ -110,13 +113,14 @@ typedef enum nbody_path {
        of the FP32 work of the one-sided paths.  The reactions on a tile's
        sources are summed over the CTA's targets in fixed order and stored
        per (i-block, tile) unit; the second pass adds them to the action in
-       block order.  Scratch: about n^2 / 448 bytes of reaction sums (2.5 GB
-       at n = 2^20); where that exceeds 4 GiB (or NBODY_PAIRS_MAX_BYTES) the
-       pass runs in chunks of consecutive i-blocks whose sums fit, each
-       chunk's sums folded into a per-body accumulator (16 B per body) before
-       the next chunk (two more launches per chunk, one at the end).  AUTO
-       takes this path from n = 16384 on, and falls back to
-       NBODY_PATH_SPLIT's plan if its scratch cannot be allocated. */
+       block order.  Scratch: about 8 n^2 / B bytes of reaction sums for B
+       targets per i-block (2.1 to 2.5 GB at n = 2^20); where that exceeds
+       1 GiB (or NBODY_PAIRS_MAX_BYTES) the pass runs in chunks of
+       consecutive i-blocks whose sums fit, each chunk's sums folded into a
+       per-body accumulator (16 B per body) before the next chunk (two more
+       launches per chunk, one at the end).  AUTO takes this path from
+       n = 16384 on, and falls back to NBODY_PATH_SPLIT's plan if its
+       scratch cannot be allocated; nbody_last_plan tells which ran. */
     NBODY_PATH_PAIRS = 4
 } nbody_path;
 
@@ -253,11 +257,26 @@ int nbody_leapfrog_step_layout(float *pos_mass, float *vel, float *accel,
                                int layout, void *cuda_stream);
 
 /*
- * Wait for the stream, then report and clear the device-side status of
- * this device: NBODY_OK, NBODY_ETIMEOUT, or NBODY_ECUDA if the stream
- * reported a CUDA error.
+ * Wait for the stream, then report and clear its status word: NBODY_OK,
+ * NBODY_ETIMEOUT (or NBODY_EBOUNDS in the checked build) if a kernel this
+ * library enqueued on that stream recorded a failure since the last
+ * nbody_sync on it, or NBODY_ECUDA if the stream reported a CUDA error.
+ * Failures of kernels on other streams are not reported here.  The status
+ * of nbody_accel_noalloc, whose calls share one status word per device, is
+ * reported on the stream of its last call.  Call it with the stream's
+ * device current.
  */
 int nbody_sync(void *cuda_stream);
+
+/*
+ * The plan of the last force pass this library enqueued on the stream (the
+ * fields of nbody_plan), which differs from nbody_plan's answer where AUTO
+ * chose the pair path and its scratch could not be allocated: the call then
+ * ran NBODY_PATH_SPLIT's one-sided plan.  Returns NBODY_EINVAL if no force
+ * pass has run on the stream (since nbody_release).  Needs the stream's
+ * device current.
+ */
+int nbody_last_plan(void *cuda_stream, int64_t *out, int len);
 
 /*
  * Largest n that nbody_accel_noalloc accepts.
@@ -269,28 +288,28 @@ int nbody_sync(void *cuda_stream);
  * this entry point exists for callers of this library).
  *
  * Some callers cannot allocate GPU memory at the point where they need the
- * accelerations: code running inside a region where the CUDA allocator is
- * off limits (for example while a stream is being captured), hosts that
- * hand every byte of device memory to their own pool and forbid other
- * allocations, and real-time or certified loops that ban allocation after
- * start-up because cudaMalloc may block or synchronise.  This call computes
- * the same accelerations as nbody_accel_on_stream, with the same argument
- * rules, but keeps its working memory (the split-j partial sums) in one
- * fixed array that the library holds on every GPU that loads it, until the
- * process exits: 6 MiB of device memory.  It
- * calls no allocation routine of CUDA, PyTorch or the C/C++ runtime.
+ * accelerations: hosts that hand every byte of device memory to their own
+ * pool and forbid other allocations, and real-time or certified loops that
+ * ban allocation after start-up because cudaMalloc may block or synchronise
+ * the device.  This call computes the same accelerations as
+ * nbody_accel_on_stream, with the same argument rules, but keeps its
+ * working memory (the split-j partial sums, and a status word for its
+ * bounded waits) in fixed arrays that the library holds on every GPU that
+ * loads it, until the process exits: 6 MiB of device memory.  It calls no
+ * allocation routine of CUDA, PyTorch or the C/C++ runtime.
  *
  *   n must be <= NBODY_NOALLOC_MAX_N; larger n returns NBODY_EINVAL and
  *   enqueues nothing.  All other arguments as for nbody_accel_on_stream.
  *
- * The first call on a device looks up that device's copy of the array
+ * The first call on a device looks up that device's copy of the arrays
  * (cudaGetSymbolAddress) with the device current; make that first call
- * before any stream capture.  All calls on a device share the one array,
- * which keeps whatever the last call left in it; every call writes each
- * slot it reads before reading it, so nothing needs clearing.
- * Two calls whose kernels overlap on the same GPU (for example on two
- * streams without ordering between them) race on the array and give wrong
- * results; order them (same stream, or an event).
+ * before any stream capture.  All calls on a device share the arrays, which
+ * keep whatever the last call left in them; every call writes each slot it
+ * reads before reading it, so nothing needs clearing.  Two calls whose
+ * kernels overlap on the same GPU (for example on two streams without
+ * ordering between them) race on the arrays and give wrong results; order
+ * them (same stream, or an event).  nbody_sync on the stream of the last
+ * call reports an expired wait of these calls.
  */
 int nbody_accel_noalloc(const float *pos_mass, float *accel, int64_t n,
                         float eps2, void *cuda_stream);
@@ -308,6 +327,9 @@ int nbody_accel_noalloc(const float *pos_mass, float *accel, int64_t n,
  *       2 per chunk + 1)
  *   [9] kernel launches of one nbody_leapfrog_step call with steps = 1
  *  [10] streaming multiprocessors on the device
+ *  [11] bytes of reaction sums the pair path keeps (0 on the other paths)
+ *  [12] chunks of i-blocks the pair pass runs in (1 on the other paths)
+ * This is the plan before any scratch is allocated; see nbody_last_plan.
  * Returns NBODY_OK, NBODY_EINVAL or NBODY_ECUDA.
  */
 int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
@@ -353,12 +375,20 @@ void nbody_release(void);
 /*
  * Failure-detection check: runs the one-sided tiled kernel and the pair
  * kernel, each on a tiny private problem with its first tile copy
- * deliberately never issued and a wait limit of `timeout_ms`, waiting for
- * the stream after each.  A correct build returns NBODY_ETIMEOUT (both
- * kernels gave up and returned; the context stays usable); otherwise the
- * first other status.  Allocates and frees its own small buffers.
+ * deliberately never issued and a wait limit of `timeout_ms`, calling
+ * nbody_sync on the stream after each.  A correct build returns
+ * NBODY_ETIMEOUT (both kernels gave up and returned; the context stays
+ * usable); otherwise the first other status.  Its buffers are the stream's
+ * scratch.
  */
 int nbody_selftest_timeout(int timeout_ms, void *cuda_stream);
+
+/*
+ * The same two kernels enqueued on the stream without waiting: their
+ * expired waits stay in that stream's status word until nbody_sync on it
+ * (NBODY_ETIMEOUT once both have run).  Returns NBODY_OK when enqueued.
+ */
+int nbody_selftest_timeout_enqueue(int timeout_ms, void *cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -220,3 +220,39 @@ def test_binding_rejects_tensors_before_any_cuda_call():
         nb.neighbors_2d(torch.zeros(8), torch.zeros(8), 0.5, 4)
     with pytest.raises(ValueError):
         nb.accel_layout(good_shape, torch.zeros(24), 0.1, nb.ROWS3)
+
+
+def _table(L, which, row):
+    out = (ctypes.c_int64 * 6)()
+    rc = L.nbody_table(which, row, out, 6)
+    return rc, list(out)
+
+
+def test_release_table_holds_only_the_planned_kernels(L):
+    """The release build compiles the rows its plans choose between: four
+    one-sided tiled shapes (two large-n tiles, the no-allocation shape, the
+    small-n shape) and six pair-symmetric shapes (targets per thread, threads,
+    tile, running sums in shared memory, reaction scheme); with the warp
+    kernel that is 11 force kernels."""
+    rc, row = _table(L, 0, 0)
+    assert rc == nb.OK and row[0] == 4
+    tiled = [tuple(_table(L, 0, r)[1][1:5]) for r in range(4)]
+    assert tiled == [(10, 256, 512, 0), (10, 256, 256, 0), (4, 128, 128, 0), (2, 128, 64, 0)]
+    rc, row = _table(L, 1, 0)
+    assert rc == nb.OK and row[0] == 6
+    pairs = [tuple(_table(L, 1, r)[1][1:6]) for r in range(6)]
+    assert pairs == [(16, 256, 512, 1, 3), (14, 256, 512, 0, 3), (12, 256, 512, 1, 3),
+                     (10, 256, 512, 1, 4), (8, 256, 512, 1, 4), (8, 256, 256, 0, 4)]
+    assert 4 + 6 + 1 <= 12
+    for which, row in ((0, 4), (1, 6), (0, -1), (2, 0)):
+        assert _table(L, which, row)[0] == nb.EINVAL
+    assert L.nbody_table(0, 0, None, 0) == nb.OK
+    assert L.nbody_table(0, 0, None, 3) == nb.EINVAL
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the behaviour without a usable device")
+def test_status_queries_without_a_device(L):
+    out = (ctypes.c_int64 * 13)()
+    assert L.nbody_last_plan(S, out, 13) in (nb.ECUDA, nb.EINVAL)
+    assert L.nbody_last_plan(S, None, 13) == nb.EINVAL
+    assert L.nbody_selftest_timeout_enqueue(0, S) == nb.EINVAL

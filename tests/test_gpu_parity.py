@@ -262,15 +262,16 @@ def test_plan_pairs_path(monkeypatch):
         assert p["bodies_per_cta"] == block and p["tile"] == tj, (n, cost, p)
         assert p["units"] == pair_units(n, block, tj)
         assert p["grid"] == min(p["units"], p["sms"])
-        chunks = pair_chunks(n, block, 4 << 30, tj)
+        chunks = pair_chunks(n, block, 1 << 30, tj)
         assert p["launches_accel"] == (2 if chunks == 1 else 2 * chunks + 1)
+        assert p["chunks"] == chunks and p["react_bytes"] <= 1 << 30
     if nb.plan(32768)["sms"] == 152:
         assert nb.plan(1048576)["bodies_per_cta"] == 3584
     # 4M bodies need ~39 GB of reaction rows: the pass runs in chunks of
-    # i-blocks whose rows fit 4 GiB, one accumulation pass per chunk
+    # i-blocks whose rows fit 1 GiB, one accumulation pass per chunk
     p = nb.plan(4194304)
     assert p["path"] == nb.PATH_PAIRS
-    assert p["launches_accel"] == 2 * pair_chunks(4194304, p["bodies_per_cta"], 4 << 30,
+    assert p["launches_accel"] == 2 * pair_chunks(4194304, p["bodies_per_cta"], 1 << 30,
                                                   p["tile"]) + 1
     monkeypatch.setenv("NBODY_PAIRS_MAX_BYTES", "1000")
     p = nb.plan(65537)
@@ -421,6 +422,85 @@ def test_bounded_wait_times_out_and_context_survives():
     a = gpu_accel(pm.pos_mass, pm.eps2)
     assert rel_err(a, oracle.accel(pm.pos_mass, pm.eps2)) <= ACC_TOL
     assert torch.cuda.is_available()
+
+
+def test_status_is_per_stream():
+    """An expired wait on one stream is reported by nbody_sync on that stream
+    only: a clean call on a second stream syncs clean, the first stream's
+    sync returns ETIMEOUT once, and both streams keep working."""
+    import torch
+    import all_pairs_body_gb300 as nb
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    w = W.cube_sweep(4097)
+    with torch.cuda.stream(sb):
+        pm = torch.from_numpy(w.pos_mass).cuda()
+    torch.cuda.synchronize()
+    assert nb.selftest_timeout_enqueue(50, stream=sa) == nb.OK
+    out = nb.accel(pm, w.eps2, stream=sb)
+    torch.cuda.synchronize()  # both streams' kernels have finished
+    assert nb.lib().nbody_sync(nb._stream(sb)) == nb.OK
+    assert nb.lib().nbody_sync(nb._stream(sa)) == nb.ETIMEOUT
+    assert nb.lib().nbody_sync(nb._stream(sa)) == nb.OK  # read and cleared
+    assert rel_err(out.cpu().numpy(), oracle.accel(w.pos_mass, w.eps2)) <= ACC_TOL
+    again = nb.accel(pm, w.eps2, stream=sa)
+    nb.sync(sa)
+    assert torch.equal(again, out)
+
+
+def test_pair_scratch_failure_falls_back_visibly(monkeypatch):
+    """Where the automatic plan's pair path cannot get its reaction rows the
+    call runs the one-sided plan instead, and nbody_last_plan says so."""
+    import torch
+    import all_pairs_body_gb300 as nb
+    nb.release()
+    w = W.cube_sweep(20000)
+    pm = torch.from_numpy(w.pos_mass).cuda()
+    ref = oracle.accel(w.pos_mass, w.eps2)
+    assert nb.plan(w.n)["path"] == nb.PATH_PAIRS
+    out = nb.accel(pm, w.eps2)
+    nb.sync()
+    assert nb.last_plan()["path"] == nb.PATH_PAIRS
+    nb.release()
+    monkeypatch.setenv("NBODY_FAULT_ALLOC", "pairs")
+    out2 = nb.accel(pm, w.eps2)
+    nb.sync()
+    assert nb.plan(w.n)["path"] == nb.PATH_PAIRS  # the plan before allocation
+    last = nb.last_plan()
+    assert last["path"] == nb.PATH_SPLIT and last["react_bytes"] == 0
+    for got in (out, out2):
+        assert rel_err(got.cpu().numpy(), ref) <= ACC_TOL
+    monkeypatch.delenv("NBODY_FAULT_ALLOC")
+    nb.release()
+    with pytest.raises(nb.NBodyError):
+        nb.last_plan()  # nothing ran since the release
+
+
+@pytest.mark.parametrize("n", [9000, 20000])
+def test_pair_and_one_sided_terms_agree_bitwise(n):
+    """Every path forms the term m_j (q q) q r of a pair the same way, and the
+    pair kernel's reaction -m_i q^3 r is the exact negative of the term the
+    one-sided kernels form from the other body's side.  With only two massive
+    bodies (in different i-blocks) every acceleration is one term, or the sum
+    of two, whatever the order of the additions, so all paths must agree bit
+    for bit."""
+    pm = W.random_bodies(n, 7100 + n)
+    pm[:, 3] = 0.0
+    pm[5, 3] = 0.7
+    pm[n - 3, 3] = 1.3
+    ref = oracle.accel(pm, 1e-3)
+    outs = {name: gpu_accel(pm, 1e-3, path, split) for name, path, split in
+            (("pairs", 4, 0), ("split", 2, 0), ("split3", 2, 3), ("tiled", 1, 0), ("warp", 3, 0),
+             ("warp5", 3, 5))}
+    assert rel_err(outs["pairs"], ref) <= ACC_TOL
+    for name, a in outs.items():
+        assert np.array_equal(a, outs["pairs"]), name
+
+
+@pytest.mark.parametrize("n", [16384, 65537, 262144, 1048576, 4194304, 16777216])
+def test_default_pair_scratch_is_at_most_1_gib(n):
+    import all_pairs_body_gb300 as nb
+    p = nb.plan(n)
+    assert p["path"] == nb.PATH_PAIRS and 0 < p["react_bytes"] <= 1 << 30
 
 
 # ---------------------------------------------------------------------------
@@ -619,6 +699,39 @@ def test_layouts_match_rows4(layout, n):
     wanta = ra if layout == 0 else _to_layout(ra, layout)
     assert np.array_equal(tv.cpu().numpy(), wantv) and np.array_equal(ta.cpu().numpy(), wanta)
 
+
+def _from_layout(a, layout):
+    """(n, 3) rows of a velocity or acceleration array in `layout`."""
+    a = np.asarray(a, dtype=np.float64)
+    return a[:, :3] if layout != 2 else a.T
+
+
+_LAYOUT_REF = {}
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("n", [3000, 40000, 200000])  # warp kernel, pair path, pair path
+def test_layout_steps_match_oracle(layout, n):
+    """Three leapfrog steps with velocities and accelerations as float3 rows or
+    x/y/z blocks, against the FP64 oracle at the trajectory tolerances."""
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = W.random_bodies(n, 8000 + n)
+    v = W.random_velocities(n, 8000 + n)
+    if n not in _LAYOUT_REF:
+        _LAYOUT_REF[n] = oracle.leapfrog(pm, v, 1e-3, 1e-3, 3)
+    rp, rv, ra = _LAYOUT_REF[n]
+    tp = torch.from_numpy(pm).cuda()
+    tv = torch.from_numpy(_to_layout(v, layout)).cuda()
+    ta = torch.full_like(tv, float("nan"))
+    nb.leapfrog_step_layout(tp, tv, ta, 1e-3, 1e-3, 3, layout)
+    nb.sync()
+    got_p = tp.cpu().numpy()
+    assert np.array_equal(got_p[:, 3], pm[:, 3]), "masses must not change"
+    assert rel_err(got_p, rp) <= POS_TOL
+    assert rel_err(_from_layout(tv.cpu().numpy(), layout), rv) <= VEL_TOL
+    assert rel_err(_from_layout(ta.cpu().numpy(), layout), ra) <= ACC_TOL
+    assert displacement_err(got_p, rp, pm, 3) <= POS_TOL
 
 
 # ---------------------------------------------------------------------------
