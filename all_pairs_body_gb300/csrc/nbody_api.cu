@@ -25,8 +25,6 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per tile copy: only a fault gets near it
 constexpr int kFinishThreads = 256;
-constexpr int kWarpKW = 4;  // targets per CTA of the small-n kernel (sweep: 4 beats 6-16)
-constexpr int kWarpNW = 4;
 // Forced one-sided TILED/SPLIT passes use the smallest tiled blocks up to this
 // n, the large shapes above it (latency sweep over n).
 constexpr long long kWarpMaxN = 24576;
@@ -184,6 +182,32 @@ const PairConfig kPairs[] = {
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
 
+using WarpKernel = void (*)(const WarpArgs, const Epilogue);
+
+struct WarpConfig {
+  int kw, nw, u;  // targets per CTA, warps per CTA, sources loaded ahead per thread
+  WarpKernel kernel;
+};
+
+// Shapes of the small-n warp kernel.  The release row: 6 targets per CTA,
+// 4 warps, 8 sources loaded ahead per thread; it matched or beat the other
+// shapes at every n from 1000 to 16384 in a sweep of per-call time (4.7
+// against 6.0 us at n = 1000 for the loop without loads ahead).  The tuning
+// build appends the others.
+const WarpConfig kWarps[] = {
+    {6, 4, 8, force_warp<6, 4, 8>},
+#ifdef NBODY_TUNING_TABLE
+    {4, 4, 0, force_warp<4, 4, 0>},   {4, 4, 4, force_warp<4, 4, 4>},
+    {4, 4, 8, force_warp<4, 4, 8>},   {8, 4, 4, force_warp<8, 4, 4>},
+    {8, 4, 8, force_warp<8, 4, 8>},   {8, 4, 16, force_warp<8, 4, 16>},
+    {16, 4, 8, force_warp<16, 4, 8>}, {8, 8, 8, force_warp<8, 8, 8>},
+    {4, 8, 8, force_warp<4, 8, 8>},   {12, 4, 8, force_warp<12, 4, 8>},
+    {8, 2, 8, force_warp<8, 2, 8>},
+#endif
+};
+constexpr int kNumWarps = sizeof(kWarps) / sizeof(kWarps[0]);
+
+
 // The pair path keeps one reaction row of TJ float4 per unit; all of them
 // come to about 16 N^2 / (2 B) bytes for B targets per i-block (2.5 GB at
 // N = 2^20 and B = 3584).  Where they exceed this many bytes the pass runs
@@ -250,9 +274,7 @@ struct Profile {
 };
 Profile g_prof;
 
-void count_launches(int k) {
-  if (g_prof.enabled.load(std::memory_order_relaxed)) g_prof.kernel_launches += k;
-}
+void count_launches(int k) { g_prof.kernel_launches.fetch_add(k, std::memory_order_relaxed); }
 
 // Record an event on `st` (profiling only); returns nullptr when disabled.
 cudaEvent_t prof_event(cudaStream_t st) {
@@ -434,10 +456,18 @@ void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) 
   p->second_pass = streamk_needs_second_pass(p->units, p->grid, p->ntiles);
 }
 
+// The warp kernel's shape: NBODY_WARP_CONFIG forces a row, else row 0.
+int warp_config() {
+  const long long forced = env_int("NBODY_WARP_CONFIG", -1);
+  return forced >= 0 && forced < kNumWarps ? static_cast<int>(forced) : 0;
+}
+
 void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
-  p->threads = kWarpNW * 32;
-  p->block = kWarpKW;
-  p->nblocks = ceil_div(n, kWarpKW);
+  p->cfg = warp_config();
+  const WarpConfig& wc = kWarps[p->cfg];
+  p->threads = wc.nw * 32;
+  p->block = wc.kw;
+  p->nblocks = ceil_div(n, wc.kw);
   // one slice by default: the single launch beats any split at every n the
   // warp kernel is chosen for (measured); split > 0 forces S slices
   long long s = split > 0 ? split : 1;
@@ -801,7 +831,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
     cudaEvent_t e0 = prof_event(st);
-    force_warp<kWarpKW, kWarpNW><<<grid, p.threads, 0, st>>>(a, epi);
+    kWarps[p.cfg].kernel<<<grid, p.threads, 0, st>>>(a, epi);
     cudaEvent_t e1 = prof_event(st);
     record_force(e0, e1);
     count_launches(1 + (p.second_pass ? 1 : 0));
@@ -1332,6 +1362,11 @@ int nbody_table(int which, int row, int64_t* out, int len) {
     if (row < 0 || row >= kNumPairs) return NBODY_EINVAL;
     const PairConfig& c = kPairs[row];
     const int64_t w[] = {kNumPairs, c.ki, c.nt, c.tj, c.acc, c.rot};
+    std::copy(w, w + 6, v);
+  } else if (which == 2) {
+    if (row < 0 || row >= kNumWarps) return NBODY_EINVAL;
+    const WarpConfig& c = kWarps[row];
+    const int64_t w[] = {kNumWarps, c.kw, c.nw * 32, c.u, 0, 0};
     std::copy(w, w + 6, v);
   } else {
     return NBODY_EINVAL;

@@ -32,9 +32,10 @@
 //   accumulate_pairs, finish_accumulated
 //                       the same in chunks of i-blocks where the reaction
 //                       sums of all units would not fit the scratch.
-//   force_warp<KW,NW>   small-n kernel: a CTA owns KW targets; its NW*32
-//                       threads stride over one j slice; warp shuffles then
-//                       shared memory (fixed order) combine the threads.
+//   force_warp<KW,NW,U> small-n kernel: a CTA owns KW targets; its NW*32
+//                       threads stride over one j slice, loading U sources
+//                       ahead; warp shuffles then shared memory (fixed
+//                       order) combine the threads.
 //   finish_slices       second pass for the warp kernel: sums S slices in order.
 //   render_points       the point shaders of "CUDA N-Body Simulation" §4.3 as a
 //                       kernel: normalised device coordinates and mass colour
@@ -1248,7 +1249,12 @@ struct WarpArgs {
   float4* partial;     // [S][n] when S > 1
 };
 
-template <int KW, int NW>
+// U = 0: the thread's sources are loaded one loop iteration at a time.
+// U > 0: in chunks of U, the next chunk's loads issued before the current
+// chunk's arithmetic (software pipelining across the L2 latency); the last
+// chunk is padded with zero-mass sources at the origin, which add exactly
+// nothing.
+template <int KW, int NW, int U = 0>
 __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Epilogue e) {
   static_assert(KW % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KW / 2;
@@ -1273,15 +1279,46 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
     nz[p] = make_float2(-q0.z, -q1.z);
     ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
   }
+  if constexpr (U == 0) {
 #pragma unroll 2
-  for (long long j = j_begin + tid; j < j_end; j += NTH) {
-    const float4 b = a.pos[j];
-    const float2 X = make_float2(b.x, b.x);
-    const float2 Y = make_float2(b.y, b.y);
-    const float2 Z = make_float2(b.z, b.z);
-    const float2 M = make_float2(b.w, b.w);
+    for (long long j = j_begin + tid; j < j_end; j += NTH) {
+      const float4 b = a.pos[j];
+      const float2 X = make_float2(b.x, b.x);
+      const float2 Y = make_float2(b.y, b.y);
+      const float2 Z = make_float2(b.z, b.z);
+      const float2 M = make_float2(b.w, b.w);
 #pragma unroll
-    for (int p = 0; p < P; ++p) interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, ax[p], ay[p], az[p]);
+      for (int p = 0; p < P; ++p) interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, ax[p], ay[p], az[p]);
+    }
+  } else {
+    // this thread's sources: j_begin + tid + k NTH for k < cnt
+    const long long first = j_begin + tid;
+    const int cnt = first < j_end ? static_cast<int>((j_end - first + NTH - 1) / NTH) : 0;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 cur[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) cur[u] = u < cnt ? a.pos[first + static_cast<long long>(u) * NTH] : zero;
+    for (int c = 0; c < cnt; c += U) {
+      float4 nxt[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int k = c + U + u;
+        nxt[u] = k < cnt ? a.pos[first + static_cast<long long>(k) * NTH] : zero;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float4 b = cur[u];
+        const float2 X = make_float2(b.x, b.x);
+        const float2 Y = make_float2(b.y, b.y);
+        const float2 Z = make_float2(b.z, b.z);
+        const float2 M = make_float2(b.w, b.w);
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+          interact2(X, Y, Z, M, nx[p], ny[p], nz[p], e2, ax[p], ay[p], az[p]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+    }
   }
 
   // Combine the 32 lanes with a butterfly of shuffles (every lane ends with

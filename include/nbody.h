@@ -336,16 +336,19 @@ int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
 
 /*
  * Rows of this build's kernel tables (for tests and tuning sweeps; the
- * NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG environment variables select a row
- * by its index).  which = 0: the one-sided tiled kernel, 1: the
- * pair-symmetric kernel.  out[0..len) receives, as far as len allows:
- *   [0] rows in the table   [1] target bodies per thread   [2] threads per CTA
- *   [3] sources per tile    [4] tiled: 1 for the mixed rsqrt/logarithmic
- *                               loop; pairs: 1 for running sums in shared
- *                               memory
+ * NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG / NBODY_WARP_CONFIG environment
+ * variables select a row by its index).  which = 0: the one-sided tiled
+ * kernel, 1: the pair-symmetric kernel, 2: the small-n warp kernel.
+ * out[0..len) receives, as far as len allows:
+ *   [0] rows in the table
+ *   [1] target bodies per thread (warp kernel: per CTA)
+ *   [2] threads per CTA
+ *   [3] sources per tile (warp kernel: sources each thread loads ahead)
+ *   [4] tiled: 1 for the mixed rsqrt/logarithmic loop; pairs: 1 for running
+ *       sums in shared memory; warp kernel: 0
  *   [5] pairs: the reaction scheme (0 warp butterfly over batches, 1 and 2
  *       lane rotation with one or two groups, 3 and 4 the same with loads one
- *       step ahead, scalar carries and duplicated groups); tiled: 0.
+ *       step ahead, scalar carries and duplicated groups); others: 0.
  * The release build holds only the rows its plans use; the tuning build
  * (compiled with NBODY_TUNING_TABLE) appends the others.  Needs no device.
  * Returns NBODY_OK or NBODY_EINVAL (unknown table or row).
@@ -353,14 +356,15 @@ int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
 int nbody_table(int which, int row, int64_t *out, int len);
 
 /*
- * Measurement hooks.  While enabled (nonzero), every force-kernel launch is
- * bracketed by a pair of CUDA events recorded on its own stream, and every
- * kernel launch of the library is counted.  nbody_profile_read waits for the
- * recorded events and returns, since the last read (or the enable), the
- * summed force-kernel time in milliseconds, the number of force-kernel
- * launches and the number of all kernel launches; then it starts a new
- * interval.  Any output pointer may be NULL.  Not thread-safe with
- * concurrent calls on other host threads.
+ * Measurement hooks.  Every kernel launch of the library is counted.  While
+ * enabled (nonzero), every force-kernel launch is also bracketed by a pair
+ * of CUDA events recorded on its own stream (which costs host time per
+ * launch: time calls with profiling off, and the force kernels in a
+ * separate profiled run).  nbody_profile_read waits for the recorded events
+ * and returns, since the last read, the summed force-kernel time in
+ * milliseconds, the number of force-kernel launches and the number of all
+ * kernel launches; then it starts a new interval.  Any output pointer may
+ * be NULL.  Not thread-safe with concurrent calls on other host threads.
  */
 int nbody_profile_enable(int enable);
 int nbody_profile_read(double *force_ms, int64_t *force_launches,

@@ -231,9 +231,9 @@ def _table(L, which, row):
 def test_release_table_holds_only_the_planned_kernels(L):
     """The release build compiles the rows its plans choose between: four
     one-sided tiled shapes (two large-n tiles, the no-allocation shape, the
-    small-n shape) and six pair-symmetric shapes (targets per thread, threads,
-    tile, running sums in shared memory, reaction scheme); with the warp
-    kernel that is 11 force kernels."""
+    small-n shape), six pair-symmetric shapes (targets per thread, threads,
+    tile, running sums in shared memory, reaction scheme) and one warp-kernel
+    shape: 11 force kernels."""
     rc, row = _table(L, 0, 0)
     assert rc == nb.OK and row[0] == 4
     tiled = [tuple(_table(L, 0, r)[1][1:5]) for r in range(4)]
@@ -244,7 +244,9 @@ def test_release_table_holds_only_the_planned_kernels(L):
     assert pairs == [(16, 256, 512, 1, 3), (14, 256, 512, 0, 3), (12, 256, 512, 1, 3),
                      (10, 256, 512, 1, 4), (8, 256, 512, 1, 4), (8, 256, 256, 0, 4)]
     assert 4 + 6 + 1 <= 12
-    for which, row in ((0, 4), (1, 6), (0, -1), (2, 0)):
+    rc, row = _table(L, 2, 0)
+    assert rc == nb.OK and row[:4] == [1, 6, 128, 8]  # the warp kernel: 6 targets, 8 loaded ahead
+    for which, row in ((0, 4), (1, 6), (2, 1), (0, -1), (3, 0)):
         assert _table(L, which, row)[0] == nb.EINVAL
     assert L.nbody_table(0, 0, None, 0) == nb.OK
     assert L.nbody_table(0, 0, None, 3) == nb.EINVAL

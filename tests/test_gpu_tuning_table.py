@@ -5,9 +5,11 @@ The tuning build (compiled with NBODY_TUNING_TABLE) appends every other shape
 and reaction scheme that was measured while choosing them: the one-sided
 tiled kernel with other tiles, unrolls and the mixed rsqrt/logarithmic inner
 loop, and the pair-symmetric kernel with the warp-butterfly reduction and
-the plain lane rotation.  NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG select a
-row by index; these tests route the binding through that build and hold each
-row to the same tolerances as the release paths.
+the plain lane rotation, and the small-n warp kernel with other target
+counts and load-ahead depths.  NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG /
+NBODY_WARP_CONFIG select a row by index; these tests route the binding
+through that build and hold each row to the same tolerances as the release
+paths.
 """
 import numpy as np
 import pytest
@@ -21,8 +23,10 @@ pytestmark = pytest.mark.gpu
 # rows of the tuning build's tables (the release rows come first)
 N_TILED_ROWS = 22
 N_PAIR_ROWS = 81
+N_WARP_ROWS = 12
 N_TILED_RELEASE = 4
 N_PAIR_RELEASE = 6
+N_WARP_RELEASE = 1
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -39,6 +43,7 @@ def tuning_lib():
     try:
         assert nb.table_row(0, 0)["rows"] == N_TILED_ROWS
         assert nb.table_row(1, 0)["rows"] == N_PAIR_ROWS
+        assert nb.table_row(2, 0)["rows"] == N_WARP_ROWS
         yield nb._lib
     finally:
         nb.release()
@@ -50,7 +55,7 @@ def test_release_rows_lead_the_tuning_tables():
     index means the same kernel in both builds."""
     import all_pairs_body_gb300 as nb
     release = nb.load(nb.LIB_PATH)
-    for which, count in ((0, N_TILED_RELEASE), (1, N_PAIR_RELEASE)):
+    for which, count in ((0, N_TILED_RELEASE), (1, N_PAIR_RELEASE), (2, N_WARP_RELEASE)):
         for r in range(count):
             out = (nb.ctypes.c_int64 * 6)()
             assert release.nbody_table(which, r, out, 6) == nb.OK
@@ -69,6 +74,22 @@ def test_every_pair_variant(cfg, monkeypatch):
     v = W.random_velocities(9000, 78)
     p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, 3, path=4)
     rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 3)
+    assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
+
+
+@pytest.mark.parametrize("cfg", range(N_WARP_ROWS))
+@pytest.mark.parametrize("n", [1000, 4097, 9000])
+def test_every_warp_variant(cfg, n, monkeypatch):
+    monkeypatch.setenv("NBODY_WARP_CONFIG", str(cfg))
+    pm = W.random_bodies(n, 79 + n)
+    a = gpu_accel(pm, 1e-3, path=3)
+    assert np.all(a[:, 3] == 0.0)
+    assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL
+    a5 = gpu_accel(pm, 1e-3, path=3, split=5)  # five j slices and the second pass
+    assert rel_err(a5, oracle.accel(pm, 1e-3)) <= ACC_TOL
+    v = W.random_velocities(n, 79 + n)
+    p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, 2, path=3)
+    rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, 2)
     assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL and rel_err(p, rp) <= POS_TOL
 
 
