@@ -22,6 +22,9 @@ LIB_CHECKED = os.path.join(HERE, "libnbody_gb300_checked.so")
 # kernel shape and scheme measured while choosing the release rows, reachable
 # through NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG; for tests and sweeps.
 LIB_TUNING = os.path.join(HERE, "libnbody_gb300_tuning.so")
+# The FP32-pipe calibration program (a standalone binary, not part of the
+# library): python -m all_pairs_body_gb300.build --probe builds and runs it.
+PROBE = os.path.join(HERE, "fp32_pipe_probe")
 SOURCES = ["nbody_api.cu"]
 DEPS = SOURCES + ["nbody_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -55,6 +58,24 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return out
 
 
+def build_probe(force: bool = False) -> str:
+    """Compile the FP32-pipe calibration program (fp32_pipe_probe.cu)."""
+    src = os.path.join(CSRC, "fp32_pipe_probe.cu")
+    deps = [src, os.path.join(CSRC, "nbody_kernels.cuh"), os.path.join(INCLUDE, "nbody.h")]
+    if not force and os.path.exists(PROBE):
+        t = os.path.getmtime(PROBE)
+        if all(os.path.getmtime(d) <= t for d in deps):
+            return PROBE
+    tmp = PROBE + f".tmp{os.getpid()}"
+    cmd = ([nvcc()] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-ftz=true", "-I", INCLUDE,
+                              "-I", CSRC, "-o", tmp, src])
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, PROBE)
+    return PROBE
+
+
 if __name__ == "__main__":
+    if "--probe" in sys.argv:
+        sys.exit(subprocess.run([build_probe()]).returncode)
     extra = ["-Xptxas", "-v"] if "-v" in sys.argv else None
     print(build(force=True, verbose=True, extra=extra))

@@ -9,7 +9,8 @@ N^2 body-body interactions per step.
 
     value    = interactions of all ranks / max-over-ranks device time,
                in billions of interactions per second (CUDA events on the
-               launching stream; L2 flushed by a 256 MiB write between steps)
+               launching stream; L2 flushed by a 512 MiB write between steps,
+               which also keeps the host ahead of the device at small N)
     e2e      = the same metric with host (pinned) buffers: each step copies
                positions and velocities in, runs the step and copies
                positions, velocities and accelerations back
@@ -46,7 +47,9 @@ FP32_OPS_PER_INTERACTION = 12  # 3 FADD + 3 FFMA (|r|^2+eps2) + 3 FMUL (m q^3) +
 # + 2 FMUL (both mass factors) + 6 FFMA (action and reaction) = 16
 FP32_OPS_PER_INTERACTION_PAIRS = 8
 FP32_LANES_PER_SM = 128  # per clock: 4 SM sub-partitions x 32 FP32 lanes
-FLUSH_BYTES = 256 << 20  # > 129 MB L2
+# > 129 MB L2; 512 MiB takes ~80 us of device time, longer than the host needs
+# to issue the next flush, event and call, so a small step's time is its own
+FLUSH_BYTES = 512 << 20
 PROFILE_SUMMARIES = {  # force kernel -> committed ncu summary of one launch
     "force_tiled": os.path.join(ROOT, "profiles", "force_tiled_ball-lognormal-1048576.md"),
     "force_pairs": os.path.join(ROOT, "profiles", "force_pairs_ball-lognormal-1048576.md"),
@@ -83,6 +86,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--tuning", action="store_true",
+                    help="load the tuning build (every measured kernel shape, selected with "
+                         "NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG / NBODY_WARP_CONFIG) instead of "
+                         "the release library")
     return ap.parse_args(argv)
 
 
@@ -303,7 +310,7 @@ def workload_config(w, mode: str, world: int) -> dict:
     return {
         "workload": f"{w.name}: N={w.n} bodies, eps2={w.eps2:g}, seed {w.seed}; each step is {what}",
         "n_bodies": w.n,
-        "l2": "flushed between timed steps (256 MiB write); sources 16N bytes",
+        "l2": "flushed between timed steps (512 MiB write); sources 16N bytes",
         "parallelism": "replicas" if world > 1 else "single GPU",
     }
 
@@ -325,6 +332,9 @@ def run_ours(args):
     dist = init_dist(world, True)
     __graft_entry__.build()
     import all_pairs_body_gb300 as nb
+    if args.tuning:
+        from all_pairs_body_gb300 import build as nbuild
+        nb._lib = nb.load(nbuild.build(tuning=True))
 
     w = workloads.by_name(args.workload)
     n = w.n
@@ -510,6 +520,7 @@ def run_ours(args):
         "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "parity": parity,
         "plan": plan, "layout": args.layout, "path": args.path, "impl": "ours",
+        "library": "tuning" if args.tuning else "release",
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -648,7 +659,7 @@ def run_neighbors(args):
         "config": {"workload": f"{p.name}: N={p.n} uniform 2-D points, 0.4 per unit area, "
                                f"cutoff {p.cutoff}, {p.max_neighbors} list slots; each step "
                                "tests all N^2 ordered pairs",
-                   "n_points": p.n, "l2": "flushed between timed steps (256 MiB write)",
+                   "n_points": p.n, "l2": "flushed between timed steps (512 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "alu", "achieved": value / world, "peak": peak, "unit": "Gpairs/s",
                      "frac": value / world / peak, "traffic": None,
