@@ -33,7 +33,7 @@ EXPORTS = ("nbody_accel", "nbody_accel_on_stream", "nbody_accel_with",
            "nbody_profile_read", "nbody_accel_noalloc", "nbody_leapfrog_kdk_on_stream",
            "nbody_leapfrog_kdk_with", "nbody_render_points", "nbody_neighbors_2d",
            "nbody_accel_layout", "nbody_leapfrog_step_layout", "nbody_table",
-           "nbody_last_plan", "nbody_selftest_timeout_enqueue")
+           "nbody_last_plan", "nbody_selftest_timeout_enqueue", "nbody_phase_read")
 ROWS4, ROWS3, BLOCKS3 = 0, 1, 2
 NOALLOC_MAX_N = 65536
 
@@ -76,6 +76,7 @@ def load(path: str) -> ctypes.CDLL:
         "nbody_selftest_timeout": [i32, p],
         "nbody_selftest_timeout_enqueue": [i32, p],
         "nbody_last_plan": [p, ctypes.POINTER(i64), i32],
+        "nbody_phase_read": [ctypes.POINTER(i64), i32],
         "nbody_table": [i32, i32, ctypes.POINTER(i64), i32],
         "nbody_profile_enable": [i32],
         "nbody_profile_read": [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
@@ -285,6 +286,17 @@ def last_plan(stream=None) -> dict:
     out = (ctypes.c_int64 * len(PLAN_FIELDS))()
     _check(lib().nbody_last_plan(_stream(stream), out, len(PLAN_FIELDS)), "nbody_last_plan")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+PHASES = ("wait", "expand", "own_tiles", "cross_tiles", "reduce", "fold", "other")
+
+
+def phase_read() -> dict:
+    """SM cycles the pair kernel's warps spent in each phase since the last read
+    (the profiling build only; others raise NBodyError(EINVAL))."""
+    out = (ctypes.c_int64 * len(PHASES))()
+    _check(lib().nbody_phase_read(out, len(PHASES)), "nbody_phase_read")
+    return dict(zip(PHASES, (int(v) for v in out)))
 
 
 def release() -> None:

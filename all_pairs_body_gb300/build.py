@@ -22,6 +22,9 @@ LIB_CHECKED = os.path.join(HERE, "libnbody_gb300_checked.so")
 # kernel shape and scheme measured while choosing the release rows, reachable
 # through NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG; for tests and sweeps.
 LIB_TUNING = os.path.join(HERE, "libnbody_gb300_tuning.so")
+# The profiling build (NBODY_PHASE_CLOCKS): the release library with clock64
+# stamps around the phases of the pair kernel's tiles (nbody_phase_read).
+LIB_PHASES = os.path.join(HERE, "libnbody_gb300_phases.so")
 # The FP32-pipe calibration program (a standalone binary, not part of the
 # library): python -m all_pairs_body_gb300.build --probe builds and runs it.
 PROBE = os.path.join(HERE, "fp32_pipe_probe")
@@ -38,17 +41,18 @@ def nvcc() -> str:
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
-          checked: bool = False, tuning: bool = False) -> str:
-    if checked and tuning:
-        raise ValueError("the checked and the tuning builds are separate libraries")
-    out = LIB_CHECKED if checked else (LIB_TUNING if tuning else LIB)
+          checked: bool = False, tuning: bool = False, phases: bool = False) -> str:
+    if checked + tuning + phases > 1:
+        raise ValueError("the checked, tuning and phase-clock builds are separate libraries")
+    out = LIB_CHECKED if checked else (LIB_TUNING if tuning else (LIB_PHASES if phases else LIB))
     deps = [os.path.join(CSRC, s) for s in DEPS] + [os.path.join(INCLUDE, "nbody.h")]
     if not force and os.path.exists(out):
         t = os.path.getmtime(out)
         if all(os.path.getmtime(d) <= t for d in deps):
             return out
     tmp = out + f".tmp{os.getpid()}"
-    flags = ["-DNBODY_BOUNDS_CHECK"] if checked else (["-DNBODY_TUNING_TABLE"] if tuning else [])
+    flags = (["-DNBODY_BOUNDS_CHECK"] if checked else
+             ["-DNBODY_TUNING_TABLE"] if tuning else ["-DNBODY_PHASE_CLOCKS"] if phases else [])
     cmd = ([nvcc()] + ARCH + NVCC_FLAGS + flags + ["-I", INCLUDE, "-I", CSRC] + list(extra or [])
            + ["-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcudart"])
     if verbose:

@@ -1375,6 +1375,28 @@ int nbody_table(int which, int row, int64_t* out, int len) {
   return NBODY_OK;
 }
 
+int nbody_phase_read(int64_t* out, int len) {
+#ifdef NBODY_PHASE_CLOCKS
+  if (out == nullptr && len > 0) return NBODY_EINVAL;
+  unsigned long long v[nbody::kNumPhases] = {};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(v, nbody::g_phase_cycles, sizeof(v)) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  const unsigned long long zero[nbody::kNumPhases] = {};
+  if (cudaMemcpyToSymbol(nbody::g_phase_cycles, zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return NBODY_ECUDA;
+  }
+  for (int k = 0; k < len && k < nbody::kNumPhases; ++k) out[k] = static_cast<int64_t>(v[k]);
+  return NBODY_OK;
+#else
+  (void)out, (void)len;
+  return NBODY_EINVAL;  // a build without phase clocks
+#endif
+}
+
 int nbody_profile_enable(int enable) {
   nbody::g_prof.enabled = enable != 0;
   return NBODY_OK;

@@ -94,6 +94,42 @@ __device__ __noinline__ bool index_in_bounds(const Ctl& c, long long idx, int sl
 #define NBODY_IN_BOUNDS(ctl, idx, slot) true
 #endif
 
+// Phase clocks of the profiling build (compiled with NBODY_PHASE_CLOCKS): the
+// pair kernel's warps add the SM cycles they spend in each phase of a tile
+// to these counters (lane 0 of every warp, at the end of the launch), read
+// and cleared by nbody_phase_read.  The release build has no stamps.
+enum PairPhase : int {
+  kPhaseWait = 0,   // the tile copy's mbarrier wait and the first CTA barrier
+  kPhaseExpand,     // issuing the next copy, the expansion, the second barrier
+  kPhaseOwn,        // the arithmetic of a tile of the block itself (one-sided loop)
+  kPhaseCross,      // the arithmetic of a tile past the block (rotation, reaction rows)
+  kPhaseReduce,     // the third barrier, the warps' reaction sums and the row's store
+  kPhaseFold,       // folding the per-tile sums into the running sums
+  kPhaseOther,      // the rest: target loads, segment epilogues, set-up
+  kNumPhases
+};
+#ifdef NBODY_PHASE_CLOCKS
+__device__ unsigned long long g_phase_cycles[kNumPhases];
+#define NBODY_PHASE_DECL long long ph_[kNumPhases] = {}, ph_t_ = clock64()
+#define NBODY_PHASE(q)                    \
+  do {                                    \
+    const long long ph_now_ = clock64();  \
+    ph_[(q)] += ph_now_ - ph_t_;          \
+    ph_t_ = ph_now_;                      \
+  } while (0)
+#define NBODY_PHASE_FLUSH()                                                           \
+  do {                                                                              \
+    NBODY_PHASE(kPhaseOther);                                                       \
+    if ((threadIdx.x & 31) == 0)                                                    \
+      for (int q_ = 0; q_ < kNumPhases; ++q_)                                       \
+        atomicAdd(&g_phase_cycles[q_], static_cast<unsigned long long>(ph_[q_]));   \
+  } while (0)
+#else
+#define NBODY_PHASE_DECL
+#define NBODY_PHASE(q)
+#define NBODY_PHASE_FLUSH()
+#endif
+
 // ---------------------------------------------------------------------------
 // small PTX wrappers
 // ---------------------------------------------------------------------------
@@ -835,6 +871,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   float2 nx[P], ny[P], nz[P], nm[P], ax[P], ay[P], az[P];
   long long k = 0, I = I0, t = t0;
   bool timed_out = false;
+  NBODY_PHASE_DECL;
 
   while (k < count) {
     const long long blk = I;
@@ -862,6 +899,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
 
     for (; t < te; ++t, ++k) {
       const int s = static_cast<int>(k & 1);
+      NBODY_PHASE(kPhaseOther);
       const bool ok = mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
       // As in force_tiled, and: every thread is done with the previous tile's
       // reaction sums in shared memory before they are rewritten.
@@ -869,6 +907,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
         timed_out = true;
         break;
       }
+      NBODY_PHASE(kPhaseWait);
       if (tid == 0 && k + 1 < count) issue_next(k + 1);
       if constexpr (kDup)
         expand_tile_dup(raw + s * TJ, tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ);
@@ -877,6 +916,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
       else
         (void)expand_tile(raw + s * TJ, tile, TJ, NT, tid, static_cast<long long>(a.n) - t * TJ, 0);
       __syncthreads();
+      NBODY_PHASE(kPhaseExpand);
 
       float2 tx[P], ty[P], tz[P];
 #pragma unroll
@@ -910,6 +950,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
                         make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
           }
         }
+        NBODY_PHASE(kPhaseOwn);
       } else {
         if constexpr (ROT == 3 || ROT == 4) {
           constexpr unsigned kAll = 0xffffffffu;
@@ -1059,6 +1100,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
             }
           }
         }
+        NBODY_PHASE(kPhaseCross);
         __syncthreads();
         // the unit's reaction partial: the NW warps' sums in warp order
         const long long u = u_lo + k;
@@ -1073,6 +1115,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
           if (NBODY_IN_BOUNDS(a.ctl, (u - a.u_base) * TJ + j, kCapReact))
             a.react[(u - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
         }
+        NBODY_PHASE(kPhaseReduce);
       }
 #pragma unroll
       for (int p = 0; p < P; ++p) {
@@ -1086,6 +1129,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
           az[p] = __fadd2_rn(az[p], tz[p]);
         }
       }
+      NBODY_PHASE(kPhaseFold);
     }
     if (timed_out) break;
 
@@ -1123,6 +1167,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
     }
   }
 
+  NBODY_PHASE_FLUSH();
   if (timed_out && tid == 0) {
     atomicExch(a.ctl.status, static_cast<int>(NBODY_ETIMEOUT));
     if (k != a.withhold)

@@ -86,6 +86,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--phases", action="store_true",
+                    help="load the profiling build (clock64 stamps around the phases of the "
+                         "pair kernel's tiles) and add the cycle split to the line; its timings "
+                         "are not the release library's")
     ap.add_argument("--tuning", action="store_true",
                     help="load the tuning build (every measured kernel shape, selected with "
                          "NBODY_TILED_CONFIG / NBODY_PAIRS_CONFIG / NBODY_WARP_CONFIG) instead of "
@@ -332,9 +336,9 @@ def run_ours(args):
     dist = init_dist(world, True)
     __graft_entry__.build()
     import all_pairs_body_gb300 as nb
-    if args.tuning:
+    if args.tuning or args.phases:
         from all_pairs_body_gb300 import build as nbuild
-        nb._lib = nb.load(nbuild.build(tuning=True))
+        nb._lib = nb.load(nbuild.build(tuning=args.tuning, phases=args.phases))
 
     w = workloads.by_name(args.workload)
     n = w.n
@@ -386,6 +390,8 @@ def run_ours(args):
 
     sampler = ClockSampler(gpu_selector(local)).start()
     nb.profile_read()  # starts a new count of kernel launches
+    if args.phases:
+        nb.phase_read()  # starts a new count of phase cycles
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(dist)
@@ -414,6 +420,14 @@ def run_ours(args):
     nb.sync()
     force_ms, force_launches, _ = nb.profile_read()
     nb.profile_enable(False)
+    phases = None
+    if args.phases:
+        cyc = nb.phase_read()
+        total_cyc = sum(cyc.values())
+        phases = {"cycles": cyc,
+                  "share": {k: (v / total_cyc if total_cyc else None) for k, v in cyc.items()},
+                  "what": "SM cycles of the pair kernel's warps per phase of a tile, summed over "
+                          "the timed and the profiled steps (clock64 stamps, profiling build)"}
     if args.mode == "render":
         if rank == 0:
             print(json.dumps(render_line(args, w, world, total_s, launches, clocks)), flush=True)
@@ -520,8 +534,10 @@ def run_ours(args):
         "gflops_20": value * FLOP_PER_INTERACTION, "roofline": roof, "cpu_baseline": cpu,
         "e2e": e2e, "gpu_launches": launches, "clocks": clocks, "parity": parity,
         "plan": plan, "layout": args.layout, "path": args.path, "impl": "ours",
-        "library": "tuning" if args.tuning else "release",
+        "library": "tuning" if args.tuning else ("phase clocks" if args.phases else "release"),
     }
+    if phases is not None:
+        line["phases"] = phases
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -370,6 +370,22 @@ int nbody_profile_enable(int enable);
 int nbody_profile_read(double *force_ms, int64_t *force_launches,
                        int64_t *kernel_launches);
 
+/*
+ * Phase clocks of the pair-symmetric kernel, in the profiling build only
+ * (compiled with NBODY_PHASE_CLOCKS; build(phases=True)): waits for the
+ * device, then returns and clears the SM cycles its warps spent, summed over
+ * every warp of every launch since the last read, in out[0..len):
+ *   [0] the tile copy's wait and the first CTA barrier
+ *   [1] issuing the next copy, expanding the tile, the second barrier
+ *   [2] the arithmetic of tiles of a CTA's own i-block
+ *   [3] the arithmetic of the other tiles (the lane rotation and reaction rows)
+ *   [4] the third barrier, the warps' reaction sums and the row's store
+ *   [5] folding the per-tile sums into the running sums
+ *   [6] everything else (target loads, segment epilogues, set-up)
+ * Other builds return NBODY_EINVAL.
+ */
+int nbody_phase_read(int64_t *out, int len);
+
 /* Text of a status code (static storage; never NULL). */
 const char *nbody_strerror(int status);
 

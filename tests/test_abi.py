@@ -258,3 +258,10 @@ def test_status_queries_without_a_device(L):
     assert L.nbody_last_plan(S, out, 13) in (nb.ECUDA, nb.EINVAL)
     assert L.nbody_last_plan(S, None, 13) == nb.EINVAL
     assert L.nbody_selftest_timeout_enqueue(0, S) == nb.EINVAL
+
+
+def test_phase_clocks_only_in_the_profiling_build(L):
+    """The release library has no phase stamps: nbody_phase_read says so
+    without touching a device."""
+    out = (ctypes.c_int64 * 7)()
+    assert L.nbody_phase_read(out, 7) == nb.EINVAL
