@@ -178,6 +178,11 @@ const PairConfig kPairs[] = {
     {20, 256, 512, force_pairs<20, 256, 512, 32, 4, 1, 3>, 1, 3},
     {12, 256, 512, force_pairs<12, 256, 512, 32, 4, 1, 4>, 1, 4},
     {14, 256, 512, force_pairs<14, 256, 512, 32, 4, 1, 4>, 1, 4},
+    {14, 256, 512, force_pairs_pipe<14, 256, 512, 4>, 0, 5},
+    {14, 256, 512, force_pairs_pipe<14, 256, 512, 8>, 0, 5},
+    {16, 256, 512, force_pairs_pipe<16, 256, 512, 4>, 0, 5},
+    {16, 256, 512, force_pairs_pipe<16, 256, 512, 8>, 0, 5},
+    {12, 256, 512, force_pairs_pipe<12, 256, 512, 4>, 0, 5},
 #endif
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);

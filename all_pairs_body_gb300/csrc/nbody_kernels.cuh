@@ -762,9 +762,12 @@ __device__ __forceinline__ float3 reduce_scatter(float (&vx)[NB], float (&vy)[NB
 // ring of the caller's source rows (the TMA targets), then the per-warp
 // reaction sums of a tile, and with ACC = 1 the targets' running action sums.
 __host__ __device__ constexpr size_t pair_reduce_smem(int ki, int nt, int tj, int acc, int rot) {
-  return (rot >= 3 ? static_cast<size_t>(2) * tj * sizeof(float4) : 0) +
-         static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float) +
-         (acc ? static_cast<size_t>(3) * ki * nt * sizeof(float) : 0);
+  // rot 5 (force_pairs_pipe): the ring, two expanded tiles and two sets of reaction rows
+  return rot == 5 ? static_cast<size_t>(10) * tj * sizeof(float4) +
+                        static_cast<size_t>(2) * (nt / 32) * 3 * tj * sizeof(float)
+                  : (rot >= 3 ? static_cast<size_t>(2) * tj * sizeof(float4) : 0) +
+                        static_cast<size_t>(nt / 32) * 3 * tj * sizeof(float) +
+                        (acc ? static_cast<size_t>(3) * ki * nt * sizeof(float) : 0);
 }
 
 // ACC = 0: the running action sums of a segment live in registers beside the
@@ -1172,6 +1175,274 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
     atomicExch(a.ctl.status, static_cast<int>(NBODY_ETIMEOUT));
     if (k != a.withhold)
       (void)mbar_wait_bounded(bar_of(k), static_cast<uint32_t>((k >> 1) & 1), a.timeout_ns);
+  }
+}
+
+// The pair kernel with one CTA barrier per tile (reaction scheme 3, running
+// sums in registers).  The expanded tile and the warps' reaction rows are
+// double-buffered: while the warps rotate tile k's sources over buffer k & 1,
+// nothing else touches it; after its rotation each thread, before the tile's
+// only barrier, (1) adds the warps' reaction rows of tile k - 1 (buffer
+// (k - 1) & 1, complete since the previous barrier) and stores the unit's
+// row, and (2) waits for the copy of tile k + 1 and expands it into buffer
+// (k + 1) & 1 (last read by tile k - 1's rotation).  The barrier then
+// publishes tile k + 1 and frees the rows of tile k - 1; the copy of tile
+// k + 3 is issued into the ring stage tile k + 1 has left.  Sums and their
+// order are those of force_pairs with the same scheme.
+template <int KI, int NT, int TJ, int UNRB>
+__global__ void __launch_bounds__(NT, 1) force_pairs_pipe(const PairArgs a) {
+  static_assert(KI % 2 == 0, "targets are processed in packed pairs");
+  static_assert((KI * NT) % TJ == 0 && TJ % 32 == 0, "tiles tile an i-block; groups tile a tile");
+  constexpr int P = KI / 2;
+  constexpr int NW = NT / 32;
+  constexpr long long B = static_cast<long long>(KI) * NT;
+  constexpr long long TB = B / TJ;
+
+  extern __shared__ __align__(128) float4 pipe_smem[];
+  float4* const raw = pipe_smem;             // [2][TJ]: the caller's rows (TMA targets)
+  float4* const tiles = pipe_smem + 2 * TJ;  // [2][4 TJ]: expanded, duplicated groups
+  float* const rows = reinterpret_cast<float*>(pipe_smem + 10 * TJ);  // [2][NW][3][TJ]
+  __shared__ __align__(8) unsigned long long bar[2];
+  auto red = [&](int buf, int w, int comp) { return rows + ((buf * NW + w) * 3 + comp) * TJ; };
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const long long c = blockIdx.x;
+  const long long u_lo = a.u_base + unit_begin(a.units, a.grid, c);  // global unit index
+  const long long count = unit_begin(a.units, a.grid, c + 1) - unit_begin(a.units, a.grid, c);
+  const uint32_t bar0 = smem_u32(&bar[0]);
+  const uint32_t raw0 = smem_u32(raw);
+  constexpr uint32_t kRawStride = TJ * sizeof(float4);
+  auto bar_of = [&](long long k) { return bar0 + static_cast<uint32_t>(k & 1) * 8u; };
+  auto raw_of = [&](long long k) { return raw0 + static_cast<uint32_t>(k & 1) * kRawStride; };
+  auto parity_of = [](long long k) { return static_cast<uint32_t>((k >> 1) & 1); };
+
+  long long I0 = 0;  // block of the CTA's first unit
+  {
+    long long lo = 0, hi = a.nblocks - 1;
+    while (lo < hi) {
+      const long long mid = (lo + hi + 1) / 2;
+      if (pair_units_before(mid, a.ntiles, TB) <= u_lo)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    I0 = lo;
+  }
+  const long long t0 = TB * I0 + (u_lo - pair_units_before(I0, a.ntiles, TB));
+
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8u, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (count <= 0) return;
+
+  // thread 0 issues the copies in unit order with its own cursor
+  long long iss_I = I0, iss_t = t0, issued = 0;  // units issued so far
+  auto issue_next = [&]() {
+    const long long k = issued++;
+    if (k != a.withhold) {
+      const long long j0 = iss_t * TJ;
+      const uint32_t bytes =
+          static_cast<uint32_t>(min(static_cast<long long>(TJ), a.n - j0)) * 16u;
+      mbar_arrive_expect_tx(bar_of(k), bytes);
+      bulk_copy_g2s(raw_of(k), a.pos + j0, bytes, bar_of(k));
+    }
+    if (++iss_t == a.ntiles) {
+      ++iss_I;
+      iss_t = TB * iss_I;
+    }
+  };
+  if (tid == 0) {
+    issue_next();
+    if (count > 1) issue_next();
+  }
+
+  const float2 e2 = make_float2(a.eps2, a.eps2);
+  float2 nx[P], ny[P], nz[P], nm[P], ax[P], ay[P], az[P];
+  bool timed_out = false;
+  long long k = 0, I = I0, t = t0;
+
+  // tile 0 into buffer 0
+  {
+    const bool ok = mbar_wait_bounded(bar_of(0), 0, a.timeout_ns);
+    if (!__syncthreads_and(ok)) {
+      timed_out = true;
+    } else {
+      expand_tile_dup(raw, tiles, TJ, NT, tid, static_cast<long long>(a.n) - t0 * TJ);
+      __syncthreads();
+      if (tid == 0 && count > 2) issue_next();  // into the stage tile 0 has left
+    }
+  }
+
+  long long blk = -1, seg_tb = 0;  // the current segment's block and first tile
+  bool seg_first = true;
+  long long pending = -1;          // unit whose reaction rows wait to be added (-1: none)
+  while (!timed_out) {
+    if (I != blk) {  // a new segment: this block's targets
+      blk = I;
+      seg_tb = t;
+      seg_first = (k == 0);
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const long long i0 = blk * B + (2 * p) * NT + tid;
+        const long long i1 = i0 + NT;
+        const float4 q0 = a.pos[min(i0, static_cast<long long>(a.n - 1))];
+        const float4 q1 = a.pos[min(i1, static_cast<long long>(a.n - 1))];
+        nx[p] = make_float2(-q0.x, -q1.x);
+        ny[p] = make_float2(-q0.y, -q1.y);
+        nz[p] = make_float2(-q0.z, -q1.z);
+        nm[p] = make_float2(i0 < a.n ? -q0.w : 0.f, i1 < a.n ? -q1.w : 0.f);
+        ax[p] = ay[p] = az[p] = make_float2(0.f, 0.f);
+      }
+    }
+    const int b = static_cast<int>(k & 1);
+    const float4* src = tiles + b * 4 * TJ;
+    float2 tx[P], ty[P], tz[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) tx[p] = ty[p] = tz[p] = make_float2(0.f, 0.f);
+    const bool cross = !(t < TB * (blk + 1));
+    if (!cross) {
+      // a tile of the block itself: both sides of each pair, as in force_tiled
+      for (int g = 0; g < TJ; g += 32) {
+#pragma unroll 2
+        for (int j = 0; j < 32; ++j) {
+          const float4 lo = src[2 * g + j];
+          const float4 hi = src[2 * TJ + 2 * g + j];
+#pragma unroll
+          for (int p = 0; p < P; ++p)
+            interact2(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w), make_float2(hi.x, hi.y),
+                      make_float2(hi.z, hi.w), nx[p], ny[p], nz[p], e2, tx[p], ty[p], tz[p]);
+        }
+      }
+    } else {
+      constexpr unsigned kAll = 0xffffffffu;
+      const int from = (lane + 1) & 31;
+      float* const rx_row = red(b, warp, 0);
+      float* const ry_row = red(b, warp, 1);
+      float* const rz_row = red(b, warp, 2);
+      for (int g = 0; g < TJ; g += 32) {
+        const float4* lo0 = src + 2 * g + lane;
+        const float4* hi0 = src + 2 * TJ + 2 * g + lane;
+        float4 clo = lo0[0], chi = hi0[0];
+        float bxs = 0.f, bys = 0.f, bzs = 0.f;
+#pragma unroll UNRB
+        for (int st = 0; st < 32; ++st) {
+          const float4 lo = clo;
+          const float4 hi = chi;
+          if (st + 1 < 32) {  // the next step's source, one step ahead
+            clo = lo0[st + 1];
+            chi = hi0[st + 1];
+          }
+          bxs = __shfl_sync(kAll, bxs, from);
+          bys = __shfl_sync(kAll, bys, from);
+          bzs = __shfl_sync(kAll, bzs, from);
+          float2 bx = make_float2(bxs, 0.f), by = make_float2(bys, 0.f), bz = make_float2(bzs, 0.f);
+#pragma unroll
+          for (int p = 0; p < P; ++p)
+            interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                           make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p], nz[p],
+                           nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+          bxs = bx.x + bx.y;
+          bys = by.x + by.y;
+          bzs = bz.x + bz.y;
+        }
+        const int jj = g + ((lane + 31) & 31);
+        rx_row[jj] = bxs;
+        ry_row[jj] = bys;
+        rz_row[jj] = bzs;
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      ax[p] = __fadd2_rn(ax[p], tx[p]);
+      ay[p] = __fadd2_rn(ay[p], ty[p]);
+      az[p] = __fadd2_rn(az[p], tz[p]);
+    }
+
+    // the unit after this one
+    long long nI = I, nt = t + 1;
+    if (nt == a.ntiles) {
+      ++nI;
+      nt = TB * nI;
+    }
+    const bool last = (k + 1 == count);
+    if (last || nI != I) {  // the segment ends with this unit: its action sums
+      const bool whole = (seg_tb == TB * blk && t + 1 == a.ntiles);
+      const long long slot = (c * 2 + (seg_first ? 0 : 1)) * B;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const long long local = (2 * p + h) * NT + tid;
+          const long long i = blk * B + local;
+          if (i < a.n) {
+            const float4 v = make_float4(h ? ax[p].y : ax[p].x, h ? ay[p].y : ay[p].x,
+                                         h ? az[p].y : az[p].x, 0.f);
+            if (whole && NBODY_IN_BOUNDS(a.ctl, i, kCapRows))
+              a.act[i] = v;
+            else if (!whole && NBODY_IN_BOUNDS(a.ctl, slot + local, kCapPartial))
+              a.partial[slot + local] = v;
+          }
+        }
+      }
+    }
+
+    // before the barrier: the previous cross tile's reaction row, then tile k + 1
+    if (pending >= 0) {
+      const int pb = b ^ 1;
+      for (int j = tid; j < TJ; j += NT) {
+        float sx = 0.f, sy = 0.f, sz = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          sx += red(pb, w, 0)[j];
+          sy += red(pb, w, 1)[j];
+          sz += red(pb, w, 2)[j];
+        }
+        if (NBODY_IN_BOUNDS(a.ctl, (pending - a.u_base) * TJ + j, kCapReact))
+          a.react[(pending - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
+      }
+    }
+    pending = cross ? u_lo + k : -1;
+    if (last) break;
+    bool ok = mbar_wait_bounded(bar_of(k + 1), parity_of(k + 1), a.timeout_ns);
+    if (ok)
+      expand_tile_dup(raw + ((k + 1) & 1) * TJ, tiles + ((k + 1) & 1) * 4 * TJ, TJ, NT, tid,
+                      static_cast<long long>(a.n) - nt * TJ);
+    if (!__syncthreads_and(ok)) {
+      timed_out = true;
+      ++k;  // the unit whose wait expired
+      break;
+    }
+    if (tid == 0 && issued < count) issue_next();  // tile k + 3, into the stage k + 1 has left
+    ++k;
+    I = nI;
+    t = nt;
+  }
+
+  if (!timed_out && pending >= 0) {
+    __syncthreads();  // every warp's rows of the last tile are written
+    const int pb = static_cast<int>(k & 1);
+    for (int j = tid; j < TJ; j += NT) {
+      float sx = 0.f, sy = 0.f, sz = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        sx += red(pb, w, 0)[j];
+        sy += red(pb, w, 1)[j];
+        sz += red(pb, w, 2)[j];
+      }
+      if (NBODY_IN_BOUNDS(a.ctl, (pending - a.u_base) * TJ + j, kCapReact))
+        a.react[(pending - a.u_base) * TJ + j] = make_float4(sx, sy, sz, 0.f);
+    }
+  }
+  if (timed_out && tid == 0) {
+    atomicExch(a.ctl.status, static_cast<int>(NBODY_ETIMEOUT));
+    // copies issued and not consumed may still be landing: a bounded wait for each
+    for (long long q = k; q < issued; ++q)
+      if (q != a.withhold) (void)mbar_wait_bounded(bar_of(q), parity_of(q), a.timeout_ns);
   }
 }
 
