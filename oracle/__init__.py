@@ -44,6 +44,8 @@ class Oracle:
         lib.oracle_leapfrog.restype = i32
         lib.oracle_leapfrog_kdk.argtypes = [p, p, p, i64, d, d, i32, i32]
         lib.oracle_leapfrog_kdk.restype = i32
+        lib.oracle_step_sampled.argtypes = [p, p, i64, d, d, p, i64, p, p, p, i32]
+        lib.oracle_step_sampled.restype = i32
         lib.oracle_render_points.argtypes = [p, i64, d, d, d, d, d, p, p]
         lib.oracle_render_points.restype = i32
         lib.oracle_neighbors_2d.argtypes = [p, p, i64, ctypes.c_float, i32, p, i64, p, p, i32]
@@ -97,6 +99,27 @@ class Oracle:
             raise ValueError("oracle_leapfrog: bad argument")
         return pm, v, acc
 
+
+    def step_sampled(self, pos_mass, vel, eps2: float, dt: float, idx, threads: int = 0):
+        """One half-kick + drift step for the bodies ``idx`` only (their rows of
+        ``leapfrog(..., steps=1)``): returns ``(pos_mass (k,4), vel (k,3), acc (k,3))``
+        in float64."""
+        pm = _bodies64(pos_mass)
+        n = pm.shape[0]
+        v = np.ascontiguousarray(np.asarray(vel, dtype=np.float64)[:, :3])
+        if v.shape[0] != n:
+            raise ValueError("vel must have one row per body")
+        idx_arr = np.ascontiguousarray(idx, dtype=np.int64)
+        m = idx_arr.shape[0]
+        pos_out = np.empty((m, 4), dtype=np.float64)
+        vel_out = np.empty((m, 3), dtype=np.float64)
+        acc_out = np.empty((m, 3), dtype=np.float64)
+        rc = self.lib.oracle_step_sampled(_ptr(pm), _ptr(v), n, float(eps2), float(dt),
+                                          _ptr(idx_arr), m, _ptr(pos_out), _ptr(vel_out),
+                                          _ptr(acc_out), int(threads))
+        if rc < 0:
+            raise ValueError("oracle_step_sampled: bad argument")
+        return pos_out, vel_out, acc_out
 
     def leapfrog_kdk(self, pos_mass, vel, eps2: float, dt: float, steps: int,
                      threads: int = 0):
@@ -179,6 +202,10 @@ def leapfrog(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int = 0
 
 def leapfrog_kdk(pos_mass, vel, eps2: float, dt: float, steps: int, threads: int = 0):
     return default().leapfrog_kdk(pos_mass, vel, eps2, dt, steps, threads)
+
+
+def step_sampled(pos_mass, vel, eps2: float, dt: float, idx, threads: int = 0):
+    return default().step_sampled(pos_mass, vel, eps2, dt, idx, threads)
 
 
 def render_points(pos_mass, max_xyz, min_w: float, max_w: float):

@@ -134,6 +134,36 @@ int oracle_leapfrog(double *pos_mass, double *vel, double *acc, int64_t n,
 }
 
 /*
+ * One step of oracle_leapfrog for the bodies idx[0..m) only ("CUDA N-Body
+ * Simulation" §1.3): a_i = A_i(x(t)) over all n sources, then
+ *     v_i <- v_i + (dt/2) a_i,   x_i <- x_i + dt v_i.
+ * A body's step needs only its own acceleration, so each row equals the
+ * full step's.  pos_mass: n rows (x, y, z, m), vel: n rows (vx, vy, vz);
+ * pos_out m rows (x, y, z, m), vel_out and acc_out m rows of 3.  Returns
+ * the threads used, or -1 on a bad argument.
+ */
+int oracle_step_sampled(const double *pos_mass, const double *vel, int64_t n, double eps2,
+                        double dt, const int64_t *idx, int64_t m, double *pos_out,
+                        double *vel_out, double *acc_out, int threads)
+{
+    if (n < 0 || m < 0 || (m > 0 && (idx == NULL || pos_mass == NULL || vel == NULL ||
+                                     pos_out == NULL || vel_out == NULL || acc_out == NULL)))
+        return -1;
+    const int nt = oracle_accel(pos_mass, n, eps2, idx, m, acc_out, threads);
+    if (nt < 0)
+        return -1;
+    for (int64_t k = 0; k < m; ++k) {
+        const int64_t i = idx[k];
+        for (int c = 0; c < 3; ++c) {
+            vel_out[3 * k + c] = vel[3 * i + c] + 0.5 * dt * acc_out[3 * k + c];
+            pos_out[4 * k + c] = pos_mass[4 * i + c] + dt * vel_out[3 * k + c];
+        }
+        pos_out[4 * k + 3] = pos_mass[4 * i + 3];
+    }
+    return nt;
+}
+
+/*
  * `steps` kick-drift-kick leapfrog steps in place, the closed form of the
  * staggered leapfrog named in "CUDA N-Body Simulation" §1.3:
  *   a = A(x(t))                       (once, before the first step)

@@ -576,7 +576,24 @@ ACCEL_PINS = [
     pin_bruteforce_fsum,
     pin_sampled_rows_match_full,
 ]
+def pin_step_sampled_rows_match_full(o):
+    """The sampled step's rows are the full one-step leapfrog's rows, bit for
+    bit, in any order and with repeats; masses are carried unchanged."""
+    rng = np.random.default_rng(11)
+    pm = np.zeros((150, 4))
+    pm[:, :3] = rng.normal(size=(150, 3))
+    pm[:, 3] = rng.uniform(0.1, 2.0, size=150)
+    v = rng.normal(size=(150, 3))
+    fp, fv, fa = o.leapfrog(pm, v, 1e-2, 0.01, 1)
+    idx = np.array([149, 3, 3, 0, 77])
+    sp, sv, sa = o.step_sampled(pm, v, 1e-2, 0.01, idx)
+    assert np.array_equal(sp, fp[idx]) and np.array_equal(sv, fv[idx])
+    assert np.array_equal(sa, fa[idx])
+    assert np.array_equal(sp[:, 3], pm[idx, 3])
+
+
 LEAPFROG_PINS = [
+    pin_step_sampled_rows_match_full,
     pin_leapfrog_zero_steps,
     pin_leapfrog_single_body_drift,
     pin_leapfrog_two_body_by_hand,

@@ -117,6 +117,15 @@ MUTANTS = {
                       "pos_mass[4 * i + 3] = pos_mass[4 * i + 3] + dt * vel[3 * i];\n"
                       "            for (int c = 0; c < 3; ++c) {\n                vel[3 * i + c]")],
     "sample_index_ignored": [("const int64_t i = idx ? idx[k] : k;", "const int64_t i = k;")],
+    "sampled_step_full_kick": [("vel[3 * i + c] + 0.5 * dt * acc_out[3 * k + c];",
+                                "vel[3 * i + c] + dt * acc_out[3 * k + c];")],
+    "sampled_step_drift_with_old_velocity": [
+        ("pos_mass[4 * i + c] + dt * vel_out[3 * k + c];",
+         "pos_mass[4 * i + c] + dt * vel[3 * i + c];")],
+    "sampled_step_mass_not_copied": [("pos_out[4 * k + 3] = pos_mass[4 * i + 3];",
+                                      "pos_out[4 * k + 3] = 0.0;")],
+    "sampled_step_row_not_indexed": [("        const int64_t i = idx[k];\n        for (int c = 0; c < 3; ++c) {\n            vel_out",
+                                      "        const int64_t i = k;\n        for (int c = 0; c < 3; ++c) {\n            vel_out")],
 }
 
 
