@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import workloads as W
-from parity import (ACC_TOL, POS_TOL, VEL_TOL, displacement_err, gpu_accel, gpu_leapfrog,
+from parity import (ACC_TOL, EPS32, POS_TOL, VEL_TOL, displacement_err, gpu_accel, gpu_leapfrog,
                     rel_err)
 
 pytestmark = pytest.mark.gpu
@@ -71,6 +71,37 @@ def test_uniform_cube_1024_step():
     assert rel_err(p, rp) <= POS_TOL
     # from rest: v_1 = (dt/2) a_0 exactly in the oracle's arithmetic
     assert rel_err(v, 0.5 * w.dt * ra) <= VEL_TOL
+
+
+@pytest.mark.parametrize("name,moving", [("ball-lognormal-1048576", False),
+                                         ("ball-lognormal-1048576", True),
+                                         ("cube-sweep-4194304", True)])
+def test_full_size_step_sampled(name, moving):
+    """One leapfrog step at the full sizes, through the default plan (the pair
+    kernel in chunks of reaction rows, the chunked accumulation and the fused
+    half-kick and drift), checked on the workload's 4096 sampled bodies against
+    the oracle's step of those rows.  The bodies start at rest, as the benchmark
+    runs them, or with seeded velocities so that the drift moves them."""
+    import all_pairs_body_gb300 as nb
+    w = W.by_name(name)
+    v0 = W.random_velocities(w.n, 4100) if moving else w.vel
+    p, v, a = gpu_leapfrog(w.pos_mass, v0, w.eps2, w.dt, 1)
+    plan = nb.last_plan()
+    assert plan["path"] == nb.PATH_PAIRS and plan["chunks"] > 1
+    rp, rv, ra = oracle.step_sampled(w.pos_mass, v0, w.eps2, w.dt, w.sample)
+    s = w.sample
+    assert rel_err(a[s], ra) <= ACC_TOL
+    assert rel_err(v[s], rv) <= VEL_TOL
+    assert rel_err(p[s], rp) <= POS_TOL
+    assert displacement_err(p[s], rp, w.pos_mass[s], 1) <= 1e-3
+    # the kick alone: v - v0 = (dt/2) a, beyond one float32 ulp of |v|
+    dv = v[s, :3].astype(np.float64) - v0[s, :3]
+    dv_ref = rv - v0[s, :3]
+    floor = EPS32 * np.sqrt(3.0) * np.linalg.norm(rv, axis=1)
+    excess = np.maximum(np.linalg.norm(dv - dv_ref, axis=1) - floor, 0.0)
+    assert excess.max() <= 1e-3 * np.sqrt(np.mean(np.sum(dv_ref * dv_ref, axis=1)))
+    assert np.array_equal(p[:, 3], w.pos_mass[:, 3]), "masses changed"
+    assert np.array_equal(v[:, 3], v0[:, 3]), "vel.w changed"
 
 
 @pytest.mark.parametrize("name", ["plummer-16384", "two-plummer-131072"])
