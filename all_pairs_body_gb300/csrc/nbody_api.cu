@@ -256,8 +256,10 @@ struct Buf {
 // word, the scratch of its calls, and the plan of the last force pass it
 // enqueued there (nbody_last_plan).
 struct Scratch {
-  Buf status;      // int: NBODY_OK until a kernel on this stream records a failure
-  Buf pos_alt, partial;
+  Buf status;      // int4: [0] NBODY_OK until a kernel on this stream records a
+                   // failure; [1] the warp kernel's grid counter (copy-back)
+  Buf pos_alt;     // end-of-step positions of a one-kernel pass (see step_impl)
+  Buf partial;
   Buf act, react;  // pair path: whole-block action sums, per-unit reaction sums
   Buf pair_acc;    // pair path in chunks: per-body running sums
   Buf check[4];    // nbody_selftest_timeout_enqueue: its private problem
@@ -653,6 +655,21 @@ Scratch& scratch_of(int dev, cudaStream_t st) {
   return g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
 }
 
+// Largest n whose one-kernel warp pass copies its drifted positions back in
+// its last CTA; above it a copy before the pass costs less than one CTA's
+// serial copy.
+#ifndef NBODY_COPY_BACK_MAX_N
+#define NBODY_COPY_BACK_MAX_N 4096
+#endif
+constexpr long long kCopyBackMaxN = NBODY_COPY_BACK_MAX_N;
+
+// True when every acceleration of a pass is completed by a later kernel than
+// the ones that read the positions (the pair path's finishing passes, the
+// warp path's slice sum): that kernel may drift the positions in place.
+bool drift_in_place(const Plan& p) {
+  return p.path == NBODY_PATH_PAIRS || (p.path == NBODY_PATH_WARP && p.second_pass);
+}
+
 int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapfrog,
                 Scratch** out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -673,7 +690,8 @@ int get_scratch(int dev, cudaStream_t st, const Plan& p, long long n, bool leapf
   } else if (p.second_pass) {
     rc = ensure(s.partial, static_cast<size_t>(p.slices) * n * sizeof(float4), st);
   }
-  if (rc == NBODY_OK && leapfrog) rc = ensure(s.pos_alt, static_cast<size_t>(n) * sizeof(float4), st);
+  if (rc == NBODY_OK && leapfrog && !drift_in_place(p))
+    rc = ensure(s.pos_alt, static_cast<size_t>(n) * sizeof(float4), st);
   *out = &s;
   return rc;
 }
@@ -778,10 +796,30 @@ int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st
   return rc;
 }
 
+// Launches a second-pass kernel right behind the force kernel on `st` with
+// programmatic stream serialization: its launch overlaps the force kernel's
+// tail, and the kernel itself waits for the force kernel's completion before
+// touching memory (wait_for_prior_grid).
+template <typename... KArgs, typename... Args>
+void launch_second_pass(void (*kernel)(KArgs...), long long blocks, cudaStream_t st,
+                        Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kFinishThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, args...);  // an error stays for launch_status()
+}
+
 // One force pass (plus its second pass): sources and targets `pos`, finished
 // through `epi`, with the stream's status word and the scratch of `s`.
 void launch_force(const Plan& p, const float4* pos, long long n, float eps2, const Scratch& s,
-                  const Epilogue& epi_in, cudaStream_t st) {
+                  const Epilogue& epi_in, cudaStream_t st, float4* copy_to = nullptr) {
   float4* partial = static_cast<float4*>(s.partial.p);
   const Ctl ctl = make_ctl(static_cast<int*>(s.status.p), n, float4_rows(s.partial.p, s.partial.bytes),
                            float4_rows(s.react.p, s.react.bytes), 0);
@@ -813,8 +851,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
       PairFinishArgs f{act,      partial, react, static_cast<int>(n), p.block, p.tj,
                        p.ntiles, u_base,  units, grid,                0,       p.nblocks,
                        ctl};
-      finish_pairs<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0, st>>>(
-          f, epi);
+      launch_second_pass(finish_pairs, ceil_div(n, kFinishThreads), st, f, epi);
       return;
     }
     float4* acc = static_cast<float4*>(s.pair_acc.p);
@@ -825,15 +862,20 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
                        p.ntiles, u_base,  units, grid,                I0,      I1,
                        ctl};
       const long long bodies = n - I0 * p.block;
-      accumulate_pairs<<<static_cast<unsigned>(ceil_div(bodies, kFinishThreads)), kFinishThreads,
-                         0, st>>>(f, acc, k == 0 ? 1 : 0);
+      launch_second_pass(accumulate_pairs, ceil_div(bodies, kFinishThreads), st, f, acc,
+                         k == 0 ? 1 : 0);
     }
-    finish_accumulated<<<static_cast<unsigned>(ceil_div(n, kFinishThreads)), kFinishThreads, 0,
-                         st>>>(acc, static_cast<int>(n), epi);
+    launch_second_pass(finish_accumulated, ceil_div(n, kFinishThreads), st,
+                       static_cast<const float4*>(acc), static_cast<int>(n), epi);
     return;
   }
   if (p.path == NBODY_PATH_WARP) {
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
+    if (copy_to != nullptr) {  // one kernel (no second pass): see step_impl
+      a.copy_from = epi.pos_next;
+      a.copy_to = copy_to;
+      a.done = reinterpret_cast<unsigned*>(s.status.p) + 1;
+    }
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
     cudaEvent_t e0 = prof_event(st);
     kWarps[p.cfg].kernel<<<grid, p.threads, 0, st>>>(a, epi);
@@ -842,8 +884,8 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     count_launches(1 + (p.second_pass ? 1 : 0));
     if (p.second_pass) {
       const long long blocks = ceil_div(n, kFinishThreads);
-      finish_slices<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(
-          partial, static_cast<int>(n), p.slices, epi);
+      launch_second_pass(finish_slices, blocks, st, static_cast<const float4*>(partial),
+                         static_cast<int>(n), p.slices, epi);
     }
     return;
   }
@@ -856,7 +898,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
   if (p.second_pass) {
     StreamkFinishArgs f{partial, static_cast<int>(n), p.block, p.ntiles, p.units, p.grid};
     const long long blocks = ceil_div(n, kFinishThreads);
-    finish_streamk<<<static_cast<unsigned>(blocks), kFinishThreads, 0, st>>>(f, epi);
+    launch_second_pass(finish_streamk, blocks, st, f, epi);
   }
 }
 
@@ -892,9 +934,13 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
 //                 and drifts, passes 1..steps-1 kick by a full dt (closing
 //                 half kick of one step fused with the opening half kick of
 //                 the next) and drift, the last pass half-kicks only.
-// Within a pass every acceleration uses the start-of-pass positions; the new
-// positions go to the other buffer of a ping-pong pair, and an odd number of
-// drifts starts from a copy so that the result lands in the caller's buffer.
+// Within a pass every acceleration uses the start-of-pass positions.  Where a
+// later kernel than the position readers completes every acceleration (the
+// pair path, the warp path with slices) it drifts the caller's positions in
+// place.  Otherwise the new positions go to the other buffer of a ping-pong
+// pair: on the one-kernel warp path the last CTA of an odd-numbered final
+// pass copies them back; on the one-sided paths an odd number of drifts
+// starts from a copy so that the result lands in the caller's buffer.
 int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
               int steps, int path, int split, int layout, bool kdk, cudaStream_t st) {
   int rc = check_scalars(n, eps2, path, split);
@@ -920,10 +966,13 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
   if ((rc = plan_with_scratch(n, path, split, dev, st, true, &p, &s)) != NBODY_OK) return rc;
 
   float4* user = reinterpret_cast<float4*>(pos_mass);
-  float4* alt = static_cast<float4*>(s->pos_alt.p);
+  const bool in_place = drift_in_place(p);
+  const bool copy_back = p.path == NBODY_PATH_WARP && !p.second_pass && n <= kCopyBackMaxN;
+  float4* alt = in_place ? user : static_cast<float4*>(s->pos_alt.p);
   float4* cur = user;
   float4* nxt = alt;
-  if (steps & 1) {  // an odd number of drifts then ends in the caller's buffer
+  if ((steps & 1) && !in_place && !copy_back) {
+    // an odd number of drifts then ends in the caller's buffer
     if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
       cudaGetLastError();
       return NBODY_ECUDA;
@@ -934,8 +983,12 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
   for (int k = 0; k < steps; ++k) {
     const float kick = (kdk && k > 0) ? dt : 0.5f * dt;
     const Epilogue epi = make_epilogue(cur, accel, vel, nxt, kick, dt, layout, n);
-    launch_force(p, cur, n, eps2, *s, epi, st);
-    std::swap(cur, nxt);
+    const bool back = copy_back && k == steps - 1 && nxt != user;
+    launch_force(p, cur, n, eps2, *s, epi, st, back ? user : nullptr);
+    if (back)
+      cur = user;
+    else
+      std::swap(cur, nxt);
   }
   if (kdk) {
     const Epilogue last = make_epilogue(cur, accel, vel, nullptr, 0.5f * dt, dt, layout, n);

@@ -292,6 +292,20 @@ __device__ __forceinline__ void interact2_lg(float2 X, float2 Y, float2 Z, float
 // Simulation" §3.5 compares the float4 and float3 forms).
 enum VecLayout : int { kRows4 = 0, kRows3 = 1, kBlocks3 = 2 };
 
+// Programmatic dependent launch.  A force kernel lets the launch of the
+// kernel queued after it (its second pass, launched with programmatic stream
+// serialization) begin once all of its CTAs are running, so that launch
+// overlaps the force kernel's tail; the second pass waits, before its first
+// memory access, until the force kernel has completed and its writes are
+// visible.  Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_for_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 struct Epilogue {
   const float4* pos;  // start-of-step positions (x, y, z, m)
   float* accel;       // out: accelerations in `layout`
@@ -333,23 +347,45 @@ __device__ __forceinline__ float4 load_vec3(const float* base, int layout, long 
 // Kept out of line (and taken by value): it runs once per body and segment,
 // and inlining it into the force kernel perturbs the register allocation and
 // schedule of the inner loop (up to 2.5% in a measured sweep).
-__device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
-                                         float az) {
+// The body's velocity and position as the epilogue needs them (zeros where
+// it needs none); the second-pass kernels load them before their sums, so
+// that these loads overlap the sums' loads.
+struct BodyState {
+  float4 v, x;
+};
+
+__device__ __forceinline__ BodyState load_body(const Epilogue& e, long long i) {
+  BodyState b{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return b;
+  if (e.vel != nullptr) {
+    b.v = load_vec3(e.vel, e.layout, e.n, i);
+    if (e.pos_next != nullptr) b.x = e.pos[i];
+  }
+  return b;
+}
+
+__device__ __forceinline__ void finish_loaded(const Epilogue& e, long long i, float ax, float ay,
+                                              float az, BodyState b) {
   if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return;
   store_vec3(e.accel, e.layout, e.n, i, ax, ay, az, 0.0f);
   if (e.vel != nullptr) {
-    float4 v = load_vec3(e.vel, e.layout, e.n, i);
+    float4 v = b.v;
     v.x = fmaf(e.kick, ax, v.x);
     v.y = fmaf(e.kick, ay, v.y);
     v.z = fmaf(e.kick, az, v.z);
     store_vec3(e.vel, e.layout, e.n, i, v.x, v.y, v.z, v.w);
     if (e.pos_next == nullptr) return;
-    float4 x = e.pos[i];
+    float4 x = b.x;
     x.x = fmaf(e.dt, v.x, x.x);
     x.y = fmaf(e.dt, v.y, x.y);
     x.z = fmaf(e.dt, v.z, x.z);
     e.pos_next[i] = x;
   }
+}
+
+__device__ __noinline__ void finish_body(const Epilogue e, long long i, float ax, float ay,
+                                         float az) {
+  finish_loaded(e, i, ax, ay, az, load_body(e, i));
 }
 
 // ---------------------------------------------------------------------------
@@ -450,6 +486,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
   __shared__ __align__(8) unsigned long long bar[2];
 
   const int tid = threadIdx.x;
+  allow_dependent_launch();
   const long long c = blockIdx.x;
   const long long u_lo = unit_begin(a.units, a.grid, c);
   const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
@@ -629,6 +666,7 @@ struct StreamkFinishArgs {
 };
 
 __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
+  wait_for_prior_grid();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
   const long long blk = i / a.block;
@@ -637,18 +675,34 @@ __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
   const long long c1 = unit_owner(a.units, a.grid, u0 + a.ntiles - 1);
   if (c0 == c1) return;
   const long long local = i - blk * a.block;
+  const BodyState b = load_body(e, i);
   float sx = 0.f, sy = 0.f, sz = 0.f;
-  for (long long c = c0; c <= c1; ++c) {
-    // the block's segment is CTA c's first segment unless c started earlier
-    const int side = unit_begin(a.units, a.grid, c) >= u0 ? 0 : 1;
-    const long long at = (c * 2 + side) * a.block + local;
-    const float4 p =
-        NBODY_IN_BOUNDS(e.ctl, at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
-    sx += p.x;
-    sy += p.y;
-    sz += p.z;
+  // The block's segment is CTA cc's first segment, except for CTA c0 when it
+  // started before the block (every later CTA starts inside it).
+  const int side0 = unit_begin(a.units, a.grid, c0) >= u0 ? 0 : 1;
+  constexpr int D = 8;  // partials loaded eight CTAs at a time, added in CTA order
+  for (long long c = c0; c <= c1; c += D) {
+    float4 p[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const long long cc = c + d;
+      p[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (cc <= c1) {
+        const int side = cc == c0 ? side0 : 0;
+        const long long at = (cc * 2 + side) * a.block + local;
+        if (NBODY_IN_BOUNDS(e.ctl, at, kCapPartial)) p[d] = a.partial[at];
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (c + d <= c1) {
+        sx += p[d].x;
+        sy += p[d].y;
+        sz += p[d].z;
+      }
+    }
   }
-  finish_body(e, i, sx, sy, sz);
+  finish_loaded(e, i, sx, sy, sz, b);
 }
 
 // ---------------------------------------------------------------------------
@@ -819,6 +873,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
   auto acc_at = [&](int c, int p) -> float2& { return acc_s[(c * P + p) * NT + threadIdx.x]; };
 
   const int tid = threadIdx.x;
+  allow_dependent_launch();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -1487,54 +1542,96 @@ __device__ __forceinline__ float3 pair_action(const PairFinishArgs& a, long long
   }
   float sx = 0.f, sy = 0.f, sz = 0.f;
   const long long local = i - I * a.block;
-  for (long long cc = c0; cc <= c1; ++cc) {
-    const int side = unit_begin(a.units, a.grid, cc) >= u0 ? 0 : 1;
-    const long long at = (cc * 2 + side) * a.block + local;
-    const float4 p =
-        NBODY_IN_BOUNDS(a.ctl, at, kCapPartial) ? a.partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
-    sx += p.x;
-    sy += p.y;
-    sz += p.z;
+  // The block's segment is CTA cc's first segment, except for CTA c0 when it
+  // started before the block (every later CTA starts inside it).
+  const int side0 = unit_begin(a.units, a.grid, c0) >= u0 ? 0 : 1;
+  constexpr int D = 8;  // partials loaded eight CTAs at a time, added in CTA order
+  for (long long c = c0; c <= c1; c += D) {
+    float4 p[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const long long cc = c + d;
+      p[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (cc <= c1) {
+        const int side = cc == c0 ? side0 : 0;
+        const long long at = (cc * 2 + side) * a.block + local;
+        if (NBODY_IN_BOUNDS(a.ctl, at, kCapPartial)) p[d] = a.partial[at];
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (c + d <= c1) {
+        sx += p[d].x;
+        sy += p[d].y;
+        sz += p[d].z;
+      }
+    }
   }
   return make_float3(sx, sy, sz);
 }
 
 // Adds to (sx, sy, sz) the reactions on body i (tile t, row j) from the
-// launch's blocks J in [a.I0, J1), in block order.
+// launch's blocks J in [a.I0, J1), in block order.  The rows are loaded
+// eight blocks at a time before they are added (in the same order), so that
+// a body waits for one memory latency per eight blocks, not per block.
 __device__ __forceinline__ void pair_reactions(const PairFinishArgs& a, long long t, long long j,
                                                long long J1, long long tb, float& sx, float& sy,
                                                float& sz) {
-  for (long long J = a.I0; J < J1; ++J) {
-    const long long u = pair_units_before(J, a.ntiles, tb) + t - tb * J - a.u_base;
-    const float4 r = NBODY_IN_BOUNDS(a.ctl, u * a.tj + j, kCapReact) ? a.react[u * a.tj + j]
-                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-    sx += r.x;
-    sy += r.y;
-    sz += r.z;
+  constexpr int D = 8;
+  for (long long J0 = a.I0; J0 < J1; J0 += D) {
+    float4 r[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const long long J = J0 + d;
+      r[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (J < J1) {
+        const long long at = (pair_units_before(J, a.ntiles, tb) + t - tb * J - a.u_base) * a.tj + j;
+        if (NBODY_IN_BOUNDS(a.ctl, at, kCapReact)) r[d] = a.react[at];
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (J0 + d < J1) {
+        sx += r[d].x;
+        sy += r[d].y;
+        sz += r[d].z;
+      }
+    }
   }
 }
 
+// Body i's block I and tile t, and block / tile (32-bit: n < 2^31).
+struct BodyBlock {
+  long long I, t, j, tb;
+};
+
+__device__ __forceinline__ BodyBlock body_block(const PairFinishArgs& a, long long i) {
+  const int ii = static_cast<int>(i);
+  const int B = static_cast<int>(a.block), TJ = static_cast<int>(a.tj);
+  const int t = ii / TJ;
+  return BodyBlock{ii / B, t, ii - t * TJ, B / TJ};
+}
+
 __global__ void finish_pairs(const PairFinishArgs a, const Epilogue e) {
+  wait_for_prior_grid();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
-  const long long tb = a.block / a.tj;
-  const long long I = i / a.block;
-  float3 s = pair_action(a, i, I, tb);
-  const long long t = i / a.tj;
-  pair_reactions(a, t, i - t * a.tj, I, tb, s.x, s.y, s.z);
-  finish_body(e, i, s.x, s.y, s.z);
+  const BodyState b = load_body(e, i);
+  const BodyBlock k = body_block(a, i);
+  float3 s = pair_action(a, i, k.I, k.tb);
+  pair_reactions(a, k.t, k.j, k.I, k.tb, s.x, s.y, s.z);
+  finish_loaded(e, i, s.x, s.y, s.z, b);
 }
 
 __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first) {
+  wait_for_prior_grid();
   const long long i = a.I0 * a.block + static_cast<long long>(blockIdx.x) * blockDim.x +
                       threadIdx.x;
   if (i >= a.n) return;
-  const long long tb = a.block / a.tj;
-  const long long I = i / a.block;
+  const BodyBlock k = body_block(a, i);
   float3 s = make_float3(0.f, 0.f, 0.f);
-  if (I < a.I1) s = pair_action(a, i, I, tb);
-  const long long t = i / a.tj;
-  pair_reactions(a, t, i - t * a.tj, min(I, a.I1), tb, s.x, s.y, s.z);
+  if (k.I < a.I1) s = pair_action(a, i, k.I, k.tb);
+  pair_reactions(a, k.t, k.j, min(k.I, a.I1), k.tb, s.x, s.y, s.z);
   if (!NBODY_IN_BOUNDS(a.ctl, i, kCapRows)) return;
   if (first) {
     acc[i] = make_float4(s.x, s.y, s.z, 0.f);
@@ -1545,11 +1642,13 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
 }
 
 __global__ void finish_accumulated(const float4* acc, int n, const Epilogue e) {
+  wait_for_prior_grid();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return;
+  const BodyState b = load_body(e, i);
   const float4 v = acc[i];
-  finish_body(e, i, v.x, v.y, v.z);
+  finish_loaded(e, i, v.x, v.y, v.z, b);
 }
 
 // ---------------------------------------------------------------------------
@@ -1563,6 +1662,13 @@ struct WarpArgs {
   int slices;          // S: j slices (gridDim.y)
   long long slice_len; // sources per slice
   float4* partial;     // [S][n] when S > 1
+  // S = 1 only: when copy_to is set, the last CTA to finish copies the n
+  // end-of-step positions from copy_from (the epilogue's pos_next) into
+  // copy_to (the buffer `pos` this pass reads); `done` is a grid counter,
+  // 0 at launch and reset to 0 by that CTA.
+  const float4* copy_from = nullptr;
+  float4* copy_to = nullptr;
+  unsigned* done = nullptr;
 };
 
 // U = 0: the thread's sources are loaded one loop iteration at a time.
@@ -1578,6 +1684,7 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
   __shared__ float red[NW][3 * KW];
 
   const int tid = threadIdx.x;
+  allow_dependent_launch();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long i_base = static_cast<long long>(blockIdx.x) * KW;
@@ -1677,23 +1784,67 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
           a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
     }
   }
+  if (a.copy_to != nullptr) {
+    // A one-kernel step cannot drift in place: another CTA may still read a
+    // body's start-of-step position as a source.  Every CTA's reads of
+    // `pos` are consumed before it counts itself done, so the last one to
+    // count may overwrite them (a grid-wide "last block" hand-off; no CTA
+    // waits for another).
+    __shared__ bool last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(a.done, 1u) == gridDim.x * gridDim.y - 1u;
+    __syncthreads();
+    if (last) {
+      // eight loads in flight per thread before their stores: the copy is
+      // bound by L2 latency, not bandwidth
+      constexpr int D = 8;
+      __threadfence();
+      for (long long base = tid; base < a.n; base += D * NTH) {
+        float4 r[D];
+#pragma unroll
+        for (int u = 0; u < D; ++u) {
+          const long long i = base + static_cast<long long>(u) * NTH;
+          if (i < a.n) r[u] = __ldcg(a.copy_from + i);
+        }
+#pragma unroll
+        for (int u = 0; u < D; ++u) {
+          const long long i = base + static_cast<long long>(u) * NTH;
+          if (i < a.n && NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) a.copy_to[i] = r[u];
+        }
+      }
+      if (tid == 0) *a.done = 0u;
+    }
+  }
 }
 
 // Second pass of the warp kernel: a_i = sum over slices s = 0..S-1 in order.
 __global__ void finish_slices(const float4* __restrict__ partial, int n, int slices,
                               const Epilogue e) {
+  wait_for_prior_grid();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
+  const BodyState b = load_body(e, i);
   float sx = 0.f, sy = 0.f, sz = 0.f;
-  for (int s = 0; s < slices; ++s) {
-    const long long at = static_cast<long long>(s) * n + i;
-    const float4 p =
-        NBODY_IN_BOUNDS(e.ctl, at, kCapPartial) ? partial[at] : make_float4(0.f, 0.f, 0.f, 0.f);
-    sx += p.x;
-    sy += p.y;
-    sz += p.z;
+  constexpr int D = 8;  // slices loaded before they are added, in order
+  for (int s0 = 0; s0 < slices; s0 += D) {
+    float4 p[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const long long at = static_cast<long long>(s0 + d) * n + i;
+      p[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + d < slices && NBODY_IN_BOUNDS(e.ctl, at, kCapPartial)) p[d] = partial[at];
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (s0 + d < slices) {
+        sx += p[d].x;
+        sy += p[d].y;
+        sz += p[d].z;
+      }
+    }
   }
-  finish_body(e, i, sx, sy, sz);
+  finish_loaded(e, i, sx, sy, sz, b);
 }
 
 // ---------------------------------------------------------------------------

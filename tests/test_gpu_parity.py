@@ -211,6 +211,42 @@ def test_steps_compose(n):
     assert np.array_equal(p10, p46) and np.array_equal(v10, v46) and np.array_equal(a10, a46)
 
 
+# (n, path, split): the one-kernel warp pass (the last CTA copies the drifted
+# positions back), the warp pass with slices and the pair path (drift in
+# place in the finishing kernel), the one-sided paths (ping-pong from a copy)
+DRIFT_CASES = [(1024, 0, 0, "warp", 0), (4097, 3, 1, "warp", 0), (3000, 3, 5, "warp", 1),
+               (20000, 4, 0, "pairs", 1), (20000, 1, 0, "tiled", 0), (20000, 2, 3, "tiled", 1)]
+
+
+@pytest.mark.parametrize("n,path,split,kind,second", DRIFT_CASES)
+def test_drift_buffers_by_path(n, path, split, kind, second):
+    """One, two and three steps per call on every way the new positions reach
+    the caller's buffer, against the oracle; three one-step calls give the
+    bits of one three-step call; the kick-drift-kick form the same."""
+    import all_pairs_body_gb300 as nb
+    pm = W.random_bodies(n, 8100 + n)
+    v = W.random_velocities(n, 8100 + n)
+    for steps in (1, 2, 3):
+        p, vv, a = gpu_leapfrog(pm, v, 1e-3, 1e-3, steps, path, split)
+        plan = nb.last_plan()
+        assert plan["path"] == {"warp": nb.PATH_WARP, "pairs": nb.PATH_PAIRS}.get(
+            kind, plan["path"]) and plan["second_pass"] == second
+        rp, rv, ra = oracle.leapfrog(pm, v, 1e-3, 1e-3, steps)
+        assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL
+        assert rel_err(p, rp) <= POS_TOL
+        assert displacement_err(p, rp, pm, steps) <= 1e-3
+        assert np.array_equal(p[:, 3], pm[:, 3]) and np.array_equal(vv[:, 3], v[:, 3])
+    p1, v1, a1 = pm, v, None
+    for _ in range(3):
+        p1, v1, a1 = gpu_leapfrog(p1, v1, 1e-3, 1e-3, 1, path, split)
+    assert np.array_equal(p1, p) and np.array_equal(v1, vv) and np.array_equal(a1, a)
+    for steps in (1, 3):
+        p, vv, a = gpu_kdk(pm, v, 1e-3, 1e-3, steps, path, split)
+        rp, rv, ra = oracle.leapfrog_kdk(pm, v, 1e-3, 1e-3, steps)
+        assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL
+        assert displacement_err(p, rp, pm, steps) <= 1e-3
+
+
 def test_zero_steps_is_noop():
     pm = W.random_bodies(100, 2)
     v = W.random_velocities(100, 2)
@@ -792,12 +828,14 @@ def test_plain_entry_points_on_the_legacy_stream():
     assert rel_err(a.cpu().numpy(), ra) <= ACC_TOL and rel_err(pm.cpu().numpy(), rp) <= POS_TOL
 
 
-def test_concurrent_streams_use_separate_scratch():
-    """Two tiled multi-step calls in flight at once on two streams (each with
-    its own cached scratch) give the same bits as the same calls run alone."""
+@pytest.mark.parametrize("n", [4000, 40000])
+def test_concurrent_streams_use_separate_scratch(n):
+    """Two multi-step calls in flight at once on two streams (each with its
+    own cached scratch and grid counter) give the same bits as the same calls
+    run alone: the one-kernel warp pass and the pair path."""
     import torch
     import all_pairs_body_gb300 as nb
-    inputs = [(W.random_bodies(40000, s), W.random_velocities(40000, s)) for s in (51, 52)]
+    inputs = [(W.random_bodies(n, s), W.random_velocities(n, s)) for s in (51, 52)]
     alone = [gpu_leapfrog(pm, v, 1e-3, 1e-3, 3) for pm, v in inputs]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     bufs = []
