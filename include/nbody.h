@@ -29,8 +29,9 @@
  * (cudaMalloc / cudaMallocAsync / managed memory); host pointers are
  * rejected with NBODY_EINVAL.  The caller owns every array it passes.  The
  * library owns only what it keeps per (device, stream): a status word and
- * its cached scratch (the ping-pong positions of a multi-step call, the
- * split-j partial sums and the pair path's action and reaction sums).  Both
+ * its cached scratch (the second buffer of the positions where one kernel
+ * both reads and drifts them, the split-j partial sums and the pair path's
+ * action and reaction sums).  Both
  * come from stream-ordered allocation (cudaMallocAsync on the call's stream)
  * on the stream's first use and when a larger call needs more, and are
  * freed by nbody_release().
