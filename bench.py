@@ -83,6 +83,9 @@ def parse_args(argv=None):
                     help="velocity/acceleration layout for --mode step|accel (float4 rows, "
                          "float3 rows, or x/y/z blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other benchmark configurations measured after the "
+                         "default workload (the line's \"configs\")")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -324,6 +327,91 @@ def workload_config(w, mode: str, world: int) -> dict:
 # ---------------------------------------------------------------------------
 
 
+# The benchmark's other configurations, measured after the default workload in
+# the same process (rank 0 of a one-GPU run): (workload, mode, path, calls,
+# warm-up calls).  C1-C5 and the one-sided kernel at 2^20.
+OTHER_CONFIGS = (
+    ("uniform-cube-1024", "accel", "auto", 200, 10),
+    ("uniform-cube-1024", "step", "auto", 200, 10),
+    ("plummer-16384", "step", "auto", 50, 5),
+    ("two-plummer-131072", "step", "auto", 10, 3),
+    ("cube-sweep-1000", "accel", "auto", 200, 10),
+    ("cube-sweep-4097", "accel", "auto", 200, 10),
+    ("cube-sweep-65537", "accel", "auto", 10, 3),
+    ("cube-sweep-500000", "accel", "auto", 5, 2),
+    ("cube-sweep-4194304", "accel", "auto", 1, 1),
+    ("ball-lognormal-1048576", "step", "split", 3, 1),
+)
+
+
+def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[dict]:
+    """Per-call device time of each OTHER_CONFIGS entry, timed like the main
+    line (CUDA events around each call, the L2 flushed before it), and its
+    force kernel alone from a second, profiled run of the same calls."""
+    import workloads
+    paths = {"auto": nb.PATH_AUTO, "split": nb.PATH_SPLIT}
+    out = []
+    for name, mode, path_name, calls, warm in OTHER_CONFIGS:
+        w = workloads.by_name(name)
+        n, path = w.n, paths[path_name]
+        pm = torch.from_numpy(w.pos_mass).cuda()
+        vel = torch.from_numpy(w.vel).cuda()
+        acc = torch.empty_like(pm)
+
+        def call():
+            if mode == "step":
+                nb.leapfrog_step(pm, vel, acc, w.eps2, w.dt, 1, path=path)
+            else:
+                nb.accel(pm, w.eps2, out=acc, path=path)
+
+        for _ in range(warm):
+            call()
+        nb.sync()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(calls)]
+        nb.profile_read()
+        torch.cuda.synchronize()
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            call()
+            e.record(stream)
+        torch.cuda.synchronize()
+        nb.sync()
+        _, _, launches = nb.profile_read()
+        call_s = sum(s.elapsed_time(e) for s, e in ev) / 1e3 / calls
+        plan = nb.last_plan()
+        nb.profile_enable(True)
+        nb.profile_read()
+        for _ in range(calls):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        nb.sync()
+        force_ms, force_launches, _ = nb.profile_read()
+        nb.profile_enable(False)
+        passes = force_launches / max(plan["chunks"], 1) if force_launches else 0
+        force_s = force_ms / 1e3 / passes if passes else None
+        inter = float(n) * float(n)
+        kernel = {nb.PATH_WARP: "force_warp", nb.PATH_PAIRS: "force_pairs"}.get(plan["path"],
+                                                                             "force_tiled")
+        ops = FP32_OPS_PER_INTERACTION_PAIRS if kernel == "force_pairs" else FP32_OPS_PER_INTERACTION
+        r_one_sided = alu_peak_ginter(sms, f_max)
+        force_rate = inter / force_s / 1e9 if force_s else None
+        out.append({
+            "workload": name, "mode": mode, "path": path_name, "n": n, "calls": calls,
+            "us_per_call": 1e6 * call_s, "value": inter / call_s / 1e9, "unit": UNIT,
+            "kernel": kernel, "force_us_per_pass": 1e6 * force_s if force_s else None,
+            "call_over_force": call_s / force_s if force_s else None,
+            "force_frac_of_R": force_rate / r_one_sided if force_rate else None,
+            "force_frac_of_own_roofline": (force_rate / alu_peak_ginter(sms, f_max, ops)
+                                           if force_rate else None),
+            "kernels_per_call": launches / calls,
+        })
+        del pm, vel, acc
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -526,6 +614,17 @@ def run_ours(args):
         except Exception as exc:  # noqa: BLE001
             parity = {"error": f"{type(exc).__name__}: {exc}"}
 
+    configs = None
+    if (rank == 0 and world == 1 and not args.no_configs and args.workload == DEFAULT_WORKLOAD
+            and args.mode == "step" and path == nb.PATH_AUTO and not layout and not args.split
+            and not (args.tuning or args.phases)):
+        configs = {"what": "the other benchmark configurations and the one-sided kernel at 2^20, "
+                           "measured after the timed steps in this process: device time per "
+                           "call between CUDA events (L2 flushed before each call), the force "
+                           "kernel alone from a second, profiled run; R = the one-sided 12-op "
+                           "FP32 roofline at sm_max_mhz",
+                   "results": measure_configs(nb, torch, stream, flush, sms, f_max)}
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
@@ -536,6 +635,8 @@ def run_ours(args):
         "plan": plan, "layout": args.layout, "path": args.path, "impl": "ours",
         "library": "tuning" if args.tuning else ("phase clocks" if args.phases else "release"),
     }
+    if configs is not None:
+        line["configs"] = configs
     if phases is not None:
         line["phases"] = phases
     if rank == 0:
