@@ -341,7 +341,10 @@ OTHER_CONFIGS = (
     ("cube-sweep-500000", "accel", "auto", 5, 2),
     ("cube-sweep-4194304", "accel", "auto", 1, 1),
     ("ball-lognormal-1048576", "step", "split", 3, 1),
+    ("ball-lognormal-1048576", "kdk", "auto", 1, 1),
 )
+RENDER_CONFIG = ("ball-lognormal-16777216", 20, 3)  # point-shader kernel: workload, calls, warm-up
+NEIGHBOR_CONFIG = ("points2d-1048576", 3, 1)  # 2-D neighbour list
 
 
 def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[dict]:
@@ -361,6 +364,8 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
         def call():
             if mode == "step":
                 nb.leapfrog_step(pm, vel, acc, w.eps2, w.dt, 1, path=path)
+            elif mode == "kdk":
+                nb.leapfrog_kdk(pm, vel, acc, w.eps2, w.dt, 1, path=path)
             else:
                 nb.accel(pm, w.eps2, out=acc, path=path)
 
@@ -392,7 +397,8 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
         nb.profile_enable(False)
         passes = force_launches / max(plan["chunks"], 1) if force_launches else 0
         force_s = force_ms / 1e3 / passes if passes else None
-        inter = float(n) * float(n)
+        inter = float(n) * float(n)  # per force pass; a kick-drift-kick step takes two
+        per_call = 2.0 if mode == "kdk" else 1.0
         kernel = {nb.PATH_WARP: "force_warp", nb.PATH_PAIRS: "force_pairs"}.get(plan["path"],
                                                                              "force_tiled")
         ops = FP32_OPS_PER_INTERACTION_PAIRS if kernel == "force_pairs" else FP32_OPS_PER_INTERACTION
@@ -400,16 +406,75 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
         force_rate = inter / force_s / 1e9 if force_s else None
         out.append({
             "workload": name, "mode": mode, "path": path_name, "n": n, "calls": calls,
-            "us_per_call": 1e6 * call_s, "value": inter / call_s / 1e9, "unit": UNIT,
+            "us_per_call": 1e6 * call_s, "value": per_call * inter / call_s / 1e9, "unit": UNIT,
             "kernel": kernel, "force_us_per_pass": 1e6 * force_s if force_s else None,
-            "call_over_force": call_s / force_s if force_s else None,
+            "call_over_force": call_s / (per_call * force_s) if force_s else None,
             "force_frac_of_R": force_rate / r_one_sided if force_rate else None,
             "force_frac_of_own_roofline": (force_rate / alu_peak_ginter(sms, f_max, ops)
                                            if force_rate else None),
             "kernels_per_call": launches / calls,
         })
         del pm, vel, acc
+    out.append(measure_render(nb, torch, stream, flush))
+    out.append(measure_neighbors(nb, torch, stream, flush, sms, f_max))
     return out
+
+
+def timed_calls(torch, stream, flush, call, calls: int, warm: int) -> float:
+    """Mean device seconds per call, CUDA events around each, L2 flushed before it."""
+    for _ in range(warm):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(calls)]
+    torch.cuda.synchronize()
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return sum(s.elapsed_time(e) for s, e in ev) / 1e3 / calls
+
+
+def measure_render(nb, torch, stream, flush) -> dict:
+    """The point-shader kernel: 16 bytes read and 32 written per body."""
+    import workloads
+    name, calls, warm = RENDER_CONFIG
+    w = workloads.by_name(name)
+    pm = torch.from_numpy(w.pos_mass).cuda()
+    ndc = torch.empty_like(pm)
+    rgba = torch.empty_like(pm)
+    m_lo = float(w.pos_mass[:, 3].min())
+    m_hi = max(float(w.pos_mass[:, 3].max()), m_lo * (1 + 1e-6) + 1e-30)
+    s = timed_calls(torch, stream, flush,
+                    lambda: nb.render_points(pm, (1.0, 1.0, 1.0), m_lo, m_hi, ndc=ndc, rgba=rgba),
+                    calls, warm)
+    nb.sync()
+    gbs = 48.0 * w.n / s / 1e9
+    peak, src = measured_hbm_gbs()
+    return {"workload": name, "mode": "render", "n": w.n, "calls": calls,
+            "us_per_call": 1e6 * s, "value": gbs, "unit": "GB/s", "kernel": "render_points",
+            "frac_of_hbm": gbs / peak, "peak_basis": src}
+
+
+def measure_neighbors(nb, torch, stream, flush, sms: int, f_max: float) -> dict:
+    """The 2-D cutoff neighbour list: N^2 ordered pair tests per call."""
+    import workloads
+    name, calls, warm = NEIGHBOR_CONFIG
+    p = workloads.by_name(name)
+    x = torch.from_numpy(p.x).cuda()
+    y = torch.from_numpy(p.y).cuda()
+    nn = torch.empty(p.n, dtype=torch.int32, device="cuda")
+    nl = torch.empty((p.max_neighbors, p.n), dtype=torch.int32, device="cuda")
+    s = timed_calls(torch, stream, flush,
+                    lambda: nb.neighbors_2d(x, y, p.cutoff, p.max_neighbors, nn=nn, nl=nl),
+                    calls, warm)
+    nb.sync()
+    value = float(p.n) * float(p.n) / s / 1e9
+    peak = sms * f_max * 1e6 * FP32_LANES_PER_SM / NEIGHBOR_FP32_OPS / 1e9
+    return {"workload": name, "mode": "neighbors", "n": p.n, "calls": calls,
+            "us_per_call": 1e6 * s, "value": value, "unit": "Gpairs/s", "kernel": "neighbors_2d",
+            "frac_of_own_roofline": value / peak}
 
 
 def run_ours(args):
@@ -618,11 +683,12 @@ def run_ours(args):
     if (rank == 0 and world == 1 and not args.no_configs and args.workload == DEFAULT_WORKLOAD
             and args.mode == "step" and path == nb.PATH_AUTO and not layout and not args.split
             and not (args.tuning or args.phases)):
-        configs = {"what": "the other benchmark configurations and the one-sided kernel at 2^20, "
-                           "measured after the timed steps in this process: device time per "
-                           "call between CUDA events (L2 flushed before each call), the force "
-                           "kernel alone from a second, profiled run; R = the one-sided 12-op "
-                           "FP32 roofline at sm_max_mhz",
+        configs = {"what": "the other benchmark configurations, the one-sided kernel and the "
+                           "kick-drift-kick step at 2^20, the point-shader kernel at 2^24 and "
+                           "the 2-D neighbour list at 2^20, measured after the timed steps in "
+                           "this process: device time per call between CUDA events (L2 flushed "
+                           "before each call), the force kernel alone from a second, profiled "
+                           "run; R = the one-sided 12-op FP32 roofline at sm_max_mhz",
                    "results": measure_configs(nb, torch, stream, flush, sms, f_max)}
 
     line = {
