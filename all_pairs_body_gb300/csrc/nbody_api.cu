@@ -796,24 +796,33 @@ int plan_with_scratch(long long n, int path, int split, int dev, cudaStream_t st
   return rc;
 }
 
-// Launches a second-pass kernel right behind the force kernel on `st` with
-// programmatic stream serialization: its launch overlaps the force kernel's
-// tail, and the kernel itself waits for the force kernel's completion before
-// touching memory (wait_for_prior_grid).
+// Launches a force or second-pass kernel with programmatic stream
+// serialization: when the kernel before it on `st` is one of the library's
+// (which allow their dependents' launch as they start), this launch overlaps
+// that kernel's tail; the kernel itself waits for the one before it to
+// complete, with its writes visible, before it touches memory
+// (wait_for_prior_grid).  After any other stream work it starts as a plain
+// launch would.
 template <typename... KArgs, typename... Args>
-void launch_second_pass(void (*kernel)(KArgs...), long long blocks, cudaStream_t st,
-                        Args... args) {
+void launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem,
+                      cudaStream_t st, Args... args) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(kFinishThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, kernel, args...);  // an error stays for launch_status()
+}
+
+template <typename... KArgs, typename... Args>
+void launch_second_pass(void (*kernel)(KArgs...), long long blocks, cudaStream_t st,
+                        Args... args) {
+  launch_dependent(kernel, dim3(static_cast<unsigned>(blocks)), kFinishThreads, 0, st, args...);
 }
 
 // One force pass (plus its second pass): sources and targets `pos`, finished
@@ -840,7 +849,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
                  *units, *grid,               act,     partial,  react,        kWaitLimitNs,
                  -1,     ctl};
       cudaEvent_t e0 = prof_event(st);
-      pc.kernel<<<static_cast<unsigned>(*grid), p.threads, pc.smem(), st>>>(a);
+      launch_dependent(pc.kernel, dim3(static_cast<unsigned>(*grid)), p.threads, pc.smem(), st, a);
       cudaEvent_t e1 = prof_event(st);
       record_force(e0, e1);
     };
@@ -878,7 +887,7 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
     }
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
     cudaEvent_t e0 = prof_event(st);
-    kWarps[p.cfg].kernel<<<grid, p.threads, 0, st>>>(a, epi);
+    launch_dependent(kWarps[p.cfg].kernel, grid, p.threads, 0, st, a, epi);
     cudaEvent_t e1 = prof_event(st);
     record_force(e0, e1);
     count_launches(1 + (p.second_pass ? 1 : 0));
@@ -891,7 +900,8 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
   }
   TiledArgs a{pos, static_cast<int>(n), eps2, p.ntiles, p.units, p.grid, partial, kWaitLimitNs, -1};
   cudaEvent_t e0 = prof_event(st);
-  kTiled[p.cfg].kernel<<<static_cast<unsigned>(p.grid), p.threads, 0, st>>>(a, epi);
+  launch_dependent(kTiled[p.cfg].kernel, dim3(static_cast<unsigned>(p.grid)), p.threads, 0, st,
+                   a, epi);
   cudaEvent_t e1 = prof_event(st);
   record_force(e0, e1);
   count_launches(1 + (p.second_pass ? 1 : 0));

@@ -292,12 +292,14 @@ __device__ __forceinline__ void interact2_lg(float2 X, float2 Y, float2 Z, float
 // Simulation" §3.5 compares the float4 and float3 forms).
 enum VecLayout : int { kRows4 = 0, kRows3 = 1, kBlocks3 = 2 };
 
-// Programmatic dependent launch.  A force kernel lets the launch of the
-// kernel queued after it (its second pass, launched with programmatic stream
-// serialization) begin once all of its CTAs are running, so that launch
-// overlaps the force kernel's tail; the second pass waits, before its first
-// memory access, until the force kernel has completed and its writes are
-// visible.  Both are no-ops for kernels launched without the attribute.
+// Programmatic dependent launch.  Every force and second-pass kernel lets
+// the launch of the kernel queued after it (launched with programmatic
+// stream serialization) begin once all of its own CTAs are running, so that
+// launch overlaps this kernel's tail; and waits, before its first memory
+// access, until the kernel before it has completed and its writes are
+// visible.  The dependent's CTAs are placed only after every CTA of the
+// kernel before it has started, so they never hold back its CTAs.  Both are
+// no-ops for kernels launched without the attribute.
 __device__ __forceinline__ void allow_dependent_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -487,6 +489,7 @@ __global__ void __launch_bounds__(NT, MINB) force_tiled(const TiledArgs a, const
 
   const int tid = threadIdx.x;
   allow_dependent_launch();
+  wait_for_prior_grid();
   const long long c = blockIdx.x;
   const long long u_lo = unit_begin(a.units, a.grid, c);
   const long long count = unit_begin(a.units, a.grid, c + 1) - u_lo;
@@ -667,6 +670,7 @@ struct StreamkFinishArgs {
 
 __global__ void finish_streamk(const StreamkFinishArgs a, const Epilogue e) {
   wait_for_prior_grid();
+  allow_dependent_launch();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
   const long long blk = i / a.block;
@@ -874,6 +878,7 @@ __global__ void __launch_bounds__(NT, 1) force_pairs(const PairArgs a) {
 
   const int tid = threadIdx.x;
   allow_dependent_launch();
+  wait_for_prior_grid();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -1261,6 +1266,8 @@ __global__ void __launch_bounds__(NT, 1) force_pairs_pipe(const PairArgs a) {
   auto red = [&](int buf, int w, int comp) { return rows + ((buf * NW + w) * 3 + comp) * TJ; };
 
   const int tid = threadIdx.x;
+  allow_dependent_launch();
+  wait_for_prior_grid();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long c = blockIdx.x;
@@ -1614,6 +1621,7 @@ __device__ __forceinline__ BodyBlock body_block(const PairFinishArgs& a, long lo
 
 __global__ void finish_pairs(const PairFinishArgs a, const Epilogue e) {
   wait_for_prior_grid();
+  allow_dependent_launch();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
   const BodyState b = load_body(e, i);
@@ -1625,6 +1633,7 @@ __global__ void finish_pairs(const PairFinishArgs a, const Epilogue e) {
 
 __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first) {
   wait_for_prior_grid();
+  allow_dependent_launch();
   const long long i = a.I0 * a.block + static_cast<long long>(blockIdx.x) * blockDim.x +
                       threadIdx.x;
   if (i >= a.n) return;
@@ -1643,6 +1652,7 @@ __global__ void accumulate_pairs(const PairFinishArgs a, float4* acc, int first)
 
 __global__ void finish_accumulated(const float4* acc, int n, const Epilogue e) {
   wait_for_prior_grid();
+  allow_dependent_launch();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   if (!NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) return;
@@ -1685,6 +1695,7 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
 
   const int tid = threadIdx.x;
   allow_dependent_launch();
+  wait_for_prior_grid();
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const long long i_base = static_cast<long long>(blockIdx.x) * KW;
@@ -1822,6 +1833,7 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
 __global__ void finish_slices(const float4* __restrict__ partial, int n, int slices,
                               const Epilogue e) {
   wait_for_prior_grid();
+  allow_dependent_launch();
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const BodyState b = load_body(e, i);
