@@ -655,14 +655,6 @@ Scratch& scratch_of(int dev, cudaStream_t st) {
   return g_scratch[std::make_pair(dev, reinterpret_cast<uintptr_t>(st))];
 }
 
-// Largest n whose one-kernel warp pass copies its drifted positions back in
-// its last CTA; above it a copy before the pass costs less than one CTA's
-// serial copy.
-#ifndef NBODY_COPY_BACK_MAX_N
-#define NBODY_COPY_BACK_MAX_N 4096
-#endif
-constexpr long long kCopyBackMaxN = NBODY_COPY_BACK_MAX_N;
-
 // True when every acceleration of a pass is completed by a later kernel than
 // the ones that read the positions (the pair path's finishing passes, the
 // warp path's slice sum): that kernel may drift the positions in place.
@@ -828,7 +820,7 @@ void launch_second_pass(void (*kernel)(KArgs...), long long blocks, cudaStream_t
 // One force pass (plus its second pass): sources and targets `pos`, finished
 // through `epi`, with the stream's status word and the scratch of `s`.
 void launch_force(const Plan& p, const float4* pos, long long n, float eps2, const Scratch& s,
-                  const Epilogue& epi_in, cudaStream_t st, float4* copy_to = nullptr) {
+                  const Epilogue& epi_in, cudaStream_t st) {
   float4* partial = static_cast<float4*>(s.partial.p);
   const Ctl ctl = make_ctl(static_cast<int*>(s.status.p), n, float4_rows(s.partial.p, s.partial.bytes),
                            float4_rows(s.react.p, s.react.bytes), 0);
@@ -880,11 +872,6 @@ void launch_force(const Plan& p, const float4* pos, long long n, float eps2, con
   }
   if (p.path == NBODY_PATH_WARP) {
     WarpArgs a{pos, static_cast<int>(n), eps2, p.slices, p.slice_len, partial};
-    if (copy_to != nullptr) {  // one kernel (no second pass): see step_impl
-      a.copy_from = epi.pos_next;
-      a.copy_to = copy_to;
-      a.done = reinterpret_cast<unsigned*>(s.status.p) + 1;
-    }
     dim3 grid(static_cast<unsigned>(p.nblocks), static_cast<unsigned>(p.slices));
     cudaEvent_t e0 = prof_event(st);
     launch_dependent(kWarps[p.cfg].kernel, grid, p.threads, 0, st, a, epi);
@@ -948,9 +935,8 @@ int accel_impl(const float* pos_mass, float* accel, int64_t n, float eps2, int p
 // later kernel than the position readers completes every acceleration (the
 // pair path, the warp path with slices) it drifts the caller's positions in
 // place.  Otherwise the new positions go to the other buffer of a ping-pong
-// pair: on the one-kernel warp path the last CTA of an odd-numbered final
-// pass copies them back; on the one-sided paths an odd number of drifts
-// starts from a copy so that the result lands in the caller's buffer.
+// pair, and when an odd number of drifts leaves them there, copy_rows copies
+// them into the caller's buffer right behind the last drift.
 int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, float dt,
               int steps, int path, int split, int layout, bool kdk, cudaStream_t st) {
   int rc = check_scalars(n, eps2, path, split);
@@ -976,29 +962,21 @@ int step_impl(float* pos_mass, float* vel, float* accel, int64_t n, float eps2, 
   if ((rc = plan_with_scratch(n, path, split, dev, st, true, &p, &s)) != NBODY_OK) return rc;
 
   float4* user = reinterpret_cast<float4*>(pos_mass);
-  const bool in_place = drift_in_place(p);
-  const bool copy_back = p.path == NBODY_PATH_WARP && !p.second_pass && n <= kCopyBackMaxN;
-  float4* alt = in_place ? user : static_cast<float4*>(s->pos_alt.p);
+  float4* alt = drift_in_place(p) ? user : static_cast<float4*>(s->pos_alt.p);
   float4* cur = user;
   float4* nxt = alt;
-  if ((steps & 1) && !in_place && !copy_back) {
-    // an odd number of drifts then ends in the caller's buffer
-    if (cudaMemcpyAsync(alt, user, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) {
-      cudaGetLastError();
-      return NBODY_ECUDA;
-    }
-    cur = alt;
-    nxt = user;
-  }
   for (int k = 0; k < steps; ++k) {
     const float kick = (kdk && k > 0) ? dt : 0.5f * dt;
     const Epilogue epi = make_epilogue(cur, accel, vel, nxt, kick, dt, layout, n);
-    const bool back = copy_back && k == steps - 1 && nxt != user;
-    launch_force(p, cur, n, eps2, *s, epi, st, back ? user : nullptr);
-    if (back)
-      cur = user;
-    else
-      std::swap(cur, nxt);
+    launch_force(p, cur, n, eps2, *s, epi, st);
+    std::swap(cur, nxt);
+  }
+  if (cur != user) {  // an odd number of drifts into the other buffer
+    const long long blocks = std::min(ceil_div(n, kFinishThreads), static_cast<long long>(p.sms) * 8);
+    count_launches(1);
+    launch_second_pass(copy_rows, blocks, st, static_cast<const float4*>(cur), user,
+                       static_cast<long long>(n), make_ctl(static_cast<int*>(s->status.p), n, 0, 0, 0));
+    cur = user;
   }
   if (kdk) {
     const Epilogue last = make_epilogue(cur, accel, vel, nullptr, 0.5f * dt, dt, layout, n);

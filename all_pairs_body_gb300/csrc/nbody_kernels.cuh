@@ -1672,13 +1672,6 @@ struct WarpArgs {
   int slices;          // S: j slices (gridDim.y)
   long long slice_len; // sources per slice
   float4* partial;     // [S][n] when S > 1
-  // S = 1 only: when copy_to is set, the last CTA to finish copies the n
-  // end-of-step positions from copy_from (the epilogue's pos_next) into
-  // copy_to (the buffer `pos` this pass reads); `done` is a grid counter,
-  // 0 at launch and reset to 0 by that CTA.
-  const float4* copy_from = nullptr;
-  float4* copy_to = nullptr;
-  unsigned* done = nullptr;
 };
 
 // U = 0: the thread's sources are loaded one loop iteration at a time.
@@ -1795,38 +1788,6 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
           a.partial[static_cast<long long>(blockIdx.y) * a.n + i] = make_float4(sx, sy, sz, 0.f);
     }
   }
-  if (a.copy_to != nullptr) {
-    // A one-kernel step cannot drift in place: another CTA may still read a
-    // body's start-of-step position as a source.  Every CTA's reads of
-    // `pos` are consumed before it counts itself done, so the last one to
-    // count may overwrite them (a grid-wide "last block" hand-off; no CTA
-    // waits for another).
-    __shared__ bool last;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) last = atomicAdd(a.done, 1u) == gridDim.x * gridDim.y - 1u;
-    __syncthreads();
-    if (last) {
-      // eight loads in flight per thread before their stores: the copy is
-      // bound by L2 latency, not bandwidth
-      constexpr int D = 8;
-      __threadfence();
-      for (long long base = tid; base < a.n; base += D * NTH) {
-        float4 r[D];
-#pragma unroll
-        for (int u = 0; u < D; ++u) {
-          const long long i = base + static_cast<long long>(u) * NTH;
-          if (i < a.n) r[u] = __ldcg(a.copy_from + i);
-        }
-#pragma unroll
-        for (int u = 0; u < D; ++u) {
-          const long long i = base + static_cast<long long>(u) * NTH;
-          if (i < a.n && NBODY_IN_BOUNDS(e.ctl, i, kCapRows)) a.copy_to[i] = r[u];
-        }
-      }
-      if (tid == 0) *a.done = 0u;
-    }
-  }
 }
 
 // Second pass of the warp kernel: a_i = sum over slices s = 0..S-1 in order.
@@ -1857,6 +1818,21 @@ __global__ void finish_slices(const float4* __restrict__ partial, int n, int sli
     }
   }
   finish_loaded(e, i, sx, sy, sz, b);
+}
+
+// The end-of-step positions of a pass that drifted into the other buffer of
+// the ping-pong pair, copied into the caller's buffer once that pass has
+// completed (a one-kernel pass cannot drift in place: another CTA may still
+// read a position as a source).  Launched as a programmatic dependent of the
+// pass, so the copy starts as soon as it ends.
+__global__ void copy_rows(const float4* __restrict__ from, float4* __restrict__ to, long long n,
+                          Ctl ctl) {
+  wait_for_prior_grid();
+  allow_dependent_launch();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride)
+    if (NBODY_IN_BOUNDS(ctl, i, kCapRows)) to[i] = from[i];
 }
 
 // ---------------------------------------------------------------------------

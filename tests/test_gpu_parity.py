@@ -211,9 +211,10 @@ def test_steps_compose(n):
     assert np.array_equal(p10, p46) and np.array_equal(v10, v46) and np.array_equal(a10, a46)
 
 
-# (n, path, split): the one-kernel warp pass (the last CTA copies the drifted
-# positions back), the warp pass with slices and the pair path (drift in
-# place in the finishing kernel), the one-sided paths (ping-pong from a copy)
+# (n, path, split): the one-kernel warp pass and the one-sided paths
+# (ping-pong, and a copy into the caller's buffer after an odd number of
+# drifts), the warp pass with slices and the pair path (drift in place in the
+# finishing kernel)
 DRIFT_CASES = [(1024, 0, 0, "warp", 0), (4097, 3, 1, "warp", 0), (3000, 3, 5, "warp", 1),
                (20000, 4, 0, "pairs", 1), (20000, 1, 0, "tiled", 0), (20000, 2, 3, "tiled", 1)]
 
