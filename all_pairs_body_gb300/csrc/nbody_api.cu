@@ -256,8 +256,7 @@ struct Buf {
 // word, the scratch of its calls, and the plan of the last force pass it
 // enqueued there (nbody_last_plan).
 struct Scratch {
-  Buf status;      // int4: [0] NBODY_OK until a kernel on this stream records a
-                   // failure; [1] the warp kernel's grid counter (copy-back)
+  Buf status;      // int: NBODY_OK until a kernel on this stream records a failure
   Buf pos_alt;     // end-of-step positions of a one-kernel pass (see step_impl)
   Buf partial;
   Buf act, react;  // pair path: whole-block action sums, per-unit reaction sums

@@ -329,19 +329,21 @@ def workload_config(w, mode: str, world: int) -> dict:
 
 # The benchmark's other configurations, measured after the default workload in
 # the same process (rank 0 of a one-GPU run): (workload, mode, path, calls,
-# warm-up calls).  C1-C5 and the one-sided kernel at 2^20.
+# warm-up calls, steps per call).  C1 (an acceleration and a step), C2 and C3
+# (trajectories: 10 steps per call), C5 (accelerations), and at 2^20 the
+# one-sided kernel's step and the kick-drift-kick step.
 OTHER_CONFIGS = (
-    ("uniform-cube-1024", "accel", "auto", 200, 10),
-    ("uniform-cube-1024", "step", "auto", 200, 10),
-    ("plummer-16384", "step", "auto", 50, 5),
-    ("two-plummer-131072", "step", "auto", 10, 3),
-    ("cube-sweep-1000", "accel", "auto", 200, 10),
-    ("cube-sweep-4097", "accel", "auto", 200, 10),
-    ("cube-sweep-65537", "accel", "auto", 10, 3),
-    ("cube-sweep-500000", "accel", "auto", 5, 2),
-    ("cube-sweep-4194304", "accel", "auto", 1, 1),
-    ("ball-lognormal-1048576", "step", "split", 3, 1),
-    ("ball-lognormal-1048576", "kdk", "auto", 1, 1),
+    ("uniform-cube-1024", "accel", "auto", 200, 10, 1),
+    ("uniform-cube-1024", "step", "auto", 200, 10, 1),
+    ("plummer-16384", "step", "auto", 10, 2, 10),
+    ("two-plummer-131072", "step", "auto", 3, 1, 10),
+    ("cube-sweep-1000", "accel", "auto", 200, 10, 1),
+    ("cube-sweep-4097", "accel", "auto", 200, 10, 1),
+    ("cube-sweep-65537", "accel", "auto", 10, 3, 1),
+    ("cube-sweep-500000", "accel", "auto", 5, 2, 1),
+    ("cube-sweep-4194304", "accel", "auto", 1, 1, 1),
+    ("ball-lognormal-1048576", "step", "split", 3, 1, 1),
+    ("ball-lognormal-1048576", "kdk", "auto", 1, 1, 1),
 )
 RENDER_CONFIG = ("ball-lognormal-16777216", 20, 3)  # point-shader kernel: workload, calls, warm-up
 NEIGHBOR_CONFIG = ("points2d-1048576", 3, 1)  # 2-D neighbour list
@@ -354,7 +356,7 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
     import workloads
     paths = {"auto": nb.PATH_AUTO, "split": nb.PATH_SPLIT}
     out = []
-    for name, mode, path_name, calls, warm in OTHER_CONFIGS:
+    for name, mode, path_name, calls, warm, steps in OTHER_CONFIGS:
         w = workloads.by_name(name)
         n, path = w.n, paths[path_name]
         pm = torch.from_numpy(w.pos_mass).cuda()
@@ -363,9 +365,9 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
 
         def call():
             if mode == "step":
-                nb.leapfrog_step(pm, vel, acc, w.eps2, w.dt, 1, path=path)
+                nb.leapfrog_step(pm, vel, acc, w.eps2, w.dt, steps, path=path)
             elif mode == "kdk":
-                nb.leapfrog_kdk(pm, vel, acc, w.eps2, w.dt, 1, path=path)
+                nb.leapfrog_kdk(pm, vel, acc, w.eps2, w.dt, steps, path=path)
             else:
                 nb.accel(pm, w.eps2, out=acc, path=path)
 
@@ -398,7 +400,7 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
         passes = force_launches / max(plan["chunks"], 1) if force_launches else 0
         force_s = force_ms / 1e3 / passes if passes else None
         inter = float(n) * float(n)  # per force pass; a kick-drift-kick step takes two
-        per_call = 2.0 if mode == "kdk" else 1.0
+        per_call = float(steps) * (2.0 if mode == "kdk" else 1.0)  # force passes per call
         kernel = {nb.PATH_WARP: "force_warp", nb.PATH_PAIRS: "force_pairs"}.get(plan["path"],
                                                                              "force_tiled")
         ops = FP32_OPS_PER_INTERACTION_PAIRS if kernel == "force_pairs" else FP32_OPS_PER_INTERACTION
@@ -406,7 +408,9 @@ def measure_configs(nb, torch, stream, flush, sms: int, f_max: float) -> list[di
         force_rate = inter / force_s / 1e9 if force_s else None
         out.append({
             "workload": name, "mode": mode, "path": path_name, "n": n, "calls": calls,
-            "us_per_call": 1e6 * call_s, "value": per_call * inter / call_s / 1e9, "unit": UNIT,
+            "steps_per_call": steps, "us_per_call": 1e6 * call_s,
+            "us_per_step": 1e6 * call_s / steps if mode != "accel" else None,
+            "value": per_call * inter / call_s / 1e9, "unit": UNIT,
             "kernel": kernel, "force_us_per_pass": 1e6 * force_s if force_s else None,
             "call_over_force": call_s / (per_call * force_s) if force_s else None,
             "force_frac_of_R": force_rate / r_one_sided if force_rate else None,
