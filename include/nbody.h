@@ -44,7 +44,11 @@
  * build): every sum runs in a fixed order and no atomics take part in any
  * reduction.  Calls on different streams use different scratch and status
  * words and may run concurrently; the caller orders calls that share a
- * stream, as usual.
+ * stream, as usual.  Within a call, each kernel is launched as a
+ * programmatic dependent of the library kernel before it on the stream: its
+ * launch overlaps that kernel's last CTAs, and it waits for that kernel to
+ * complete before it touches memory.  Work the caller enqueues around a
+ * call is ordered as for any stream.
  *
  * Errors (every entry point returns one of these codes):
  *   NBODY_EINVAL    n < 0 or n > 2^31-1; eps2 not finite or <= 0; dt not
