@@ -47,8 +47,12 @@
  * stream, as usual.  Within a call, each kernel is launched as a
  * programmatic dependent of the library kernel before it on the stream: its
  * launch overlaps that kernel's last CTAs, and it waits for that kernel to
- * complete before it touches memory.  Work the caller enqueues around a
- * call is ordered as for any stream.
+ * complete before it touches memory.  The library's kernels allow their
+ * dependents' launch as they start, so a kernel of the caller's that is
+ * itself launched with programmatic stream serialization right after a call
+ * must wait for its prerequisite grid (cudaGridDependencySynchronize)
+ * before it reads the call's outputs; any other work enqueued after a call
+ * is ordered as for any stream.
  *
  * Errors (every entry point returns one of these codes):
  *   NBODY_EINVAL    n < 0 or n > 2^31-1; eps2 not finite or <= 0; dt not
