@@ -807,6 +807,39 @@ def test_layout_steps_match_oracle(layout, n):
 # ---------------------------------------------------------------------------
 
 
+@pytest.mark.parametrize("n", [1000, 3000, 20000])
+def test_caller_kernels_around_calls_are_ordered(n):
+    """The library's kernels are programmatic dependents of one another; the
+    caller's own kernels enqueued right before and after a call, with no host
+    synchronisation, still see the call's inputs and outputs in stream order:
+    a step on positions a torch kernel just shifted, then a torch kernel that
+    reads the step's outputs."""
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm0 = W.random_bodies(n, 9100 + n)
+    v0 = W.random_velocities(n, 9100 + n)
+    shift = np.array([0.25, -0.5, 0.125, 0.0], dtype=np.float32)
+    pm = torch.from_numpy(pm0).cuda()
+    v = torch.from_numpy(v0).cuda()
+    a = torch.empty_like(pm)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        pm.add_(torch.from_numpy(shift).cuda())  # a caller kernel before the call
+        nb.leapfrog_step(pm, v, a, 1e-3, 1e-3, 3)
+        doubled = a * 2.0  # a caller kernel after it
+    nb.sync()
+    p_ref, v_ref = pm0.copy(), v0.copy()
+    for _ in range(2):
+        p_ref[:, :3] += shift[:3]
+        p_ref, v_ref, a_ref = oracle.leapfrog(p_ref.astype(np.float32), v_ref.astype(np.float32),
+                                              1e-3, 1e-3, 3)
+        v_ref = np.concatenate([v_ref, v0[:, 3:4]], axis=1)
+    assert rel_err(pm.cpu().numpy(), p_ref) <= POS_TOL
+    assert rel_err(v.cpu().numpy(), v_ref) <= VEL_TOL
+    assert rel_err(doubled.cpu().numpy(), 2.0 * a_ref) <= ACC_TOL
+    assert np.array_equal(doubled.cpu().numpy(), 2.0 * a.cpu().numpy())
+
+
 def test_plain_entry_points_on_the_legacy_stream():
     import ctypes
     import torch
