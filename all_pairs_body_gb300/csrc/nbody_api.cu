@@ -183,6 +183,12 @@ const PairConfig kPairs[] = {
     {16, 256, 512, force_pairs_pipe<16, 256, 512, 4>, 0, 5},
     {16, 256, 512, force_pairs_pipe<16, 256, 512, 8>, 0, 5},
     {12, 256, 512, force_pairs_pipe<12, 256, 512, 4>, 0, 5},
+    // 128-thread CTAs, two per SM: one CTA's barriers and reaction sums can
+    // overlap the other's rotation loop
+    {16, 128, 512, force_pairs<16, 128, 512, 32, 8, 1, 3>, 1, 3},
+    {12, 128, 512, force_pairs<12, 128, 512, 32, 4, 1, 3>, 1, 3},
+    {14, 128, 256, force_pairs<14, 128, 256, 32, 4, 0, 3>, 0, 3},
+    {16, 128, 256, force_pairs<16, 128, 256, 32, 8, 1, 3>, 1, 3},
 #endif
 };
 constexpr int kNumPairs = sizeof(kPairs) / sizeof(kPairs[0]);
@@ -486,12 +492,13 @@ void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
 }
 
 // Pair shapes the plan chooses between (the release rows), with their speed
-// per interaction relative to the first, measured at n = 2^20 (force kernel
-// 264.9, 265.0, 272.0, 271.4, 277.0 and 275.6 ms per pass): more targets per
-// CTA are faster per interaction; smaller blocks and tiles cut the work into
-// more units, which wins when a CTA's share of units is small.
-constexpr LargeShape kPairShapes[] = {{0, 1.0},   {1, 0.9995}, {2, 0.974},
-                                      {3, 0.976}, {4, 0.956},  {5, 0.961}};
+// relative to the first: the model's work at n = 2^20 (the slowest CTA's
+// ceil(units / grid) units of B x TJ pairs) per measured second, force kernel
+// 265.35, 265.78, 272.55, 272.14, 277.52 and 275.72 ms per pass.  More
+// targets per CTA are faster per pair; smaller blocks and tiles cut the work
+// into more units, which wins when a CTA's share of units is small.
+constexpr LargeShape kPairShapes[] = {{0, 1.0},    {1, 0.9977}, {2, 0.9726},
+                                      {3, 0.9736}, {4, 0.9539}, {5, 0.9602}};
 
 long long pair_units_of(long long n, const PairConfig& pc) {
   const long long block = static_cast<long long>(pc.ki) * pc.nt;

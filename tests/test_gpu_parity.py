@@ -309,8 +309,8 @@ def pair_units(n, block, tj=512):
     return sum(nt - (block // tj) * i for i in range(nb_))
 
 
-PAIR_SHAPES = ((4096, 512, 1.0), (3584, 512, 0.9995), (3072, 512, 0.974), (2560, 512, 0.976),
-               (2048, 512, 0.956), (2048, 256, 0.961))  # targets per CTA, tile, speed
+PAIR_SHAPES = ((4096, 512, 1.0), (3584, 512, 0.9977), (3072, 512, 0.9726), (2560, 512, 0.9736),
+               (2048, 512, 0.9539), (2048, 256, 0.9602))  # targets per CTA, tile, speed
 
 
 def test_plan_pairs_path(monkeypatch):
@@ -334,7 +334,7 @@ def test_plan_pairs_path(monkeypatch):
         assert p["launches_accel"] == (2 if chunks == 1 else 2 * chunks + 1)
         assert p["chunks"] == chunks and p["react_bytes"] <= 1 << 30
     if nb.plan(32768)["sms"] == 152:
-        assert nb.plan(1048576)["bodies_per_cta"] == 3584
+        assert nb.plan(1048576)["bodies_per_cta"] == 4096
     # 4M bodies need ~39 GB of reaction rows: the pass runs in chunks of
     # i-blocks whose rows fit 1 GiB, one accumulation pass per chunk
     p = nb.plan(4194304)
