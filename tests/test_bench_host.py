@@ -72,6 +72,20 @@ def test_traffic_needs_matching_kernel(tmp_path, monkeypatch):
     assert bench.profiled_traffic(20, "force_warp") is None
 
 
+def test_other_configs_name_known_workloads():
+    """Every row of the default run's configs block names a workload the
+    generators know, in a mode the binding has, so the default run cannot
+    stop on a name after its timed steps."""
+    import workloads
+    for name, mode, path, calls, warm, steps in bench.OTHER_CONFIGS:
+        assert mode in ("accel", "step", "kdk") and path in ("auto", "split")
+        assert calls >= 1 and warm >= 1 and steps >= 1
+        assert workloads.by_name(name).n == int(name.rsplit("-", 1)[1])
+    for name in (bench.RENDER_CONFIG[0], bench.NEIGHBOR_CONFIG[0]):
+        assert name.rsplit("-", 1)[0] in ("ball-lognormal", "points2d")
+    assert workloads.by_name(bench.NEIGHBOR_CONFIG[0]).n == 1048576
+
+
 def test_pair_roofline_counts_eight_ops():
     one_sided = bench.alu_peak_ginter(152, 2070.0)
     assert one_sided == pytest.approx(152 * 2070e6 * 128 / 12 / 1e9)
