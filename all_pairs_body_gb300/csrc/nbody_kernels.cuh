@@ -37,6 +37,10 @@
 //                       ahead; warp shuffles then shared memory (fixed
 //                       order) combine the threads.
 //   finish_slices       second pass for the warp kernel: sums S slices in order.
+//   copy_rows           the positions an odd number of one-kernel drifts left
+//                       in the other buffer, into the caller's buffer.
+//   Every force and finishing kernel is a programmatic dependent of the
+//   kernel before it (allow_dependent_launch / wait_for_prior_grid).
 //   render_points       the point shaders of "CUDA N-Body Simulation" §4.3 as a
 //                       kernel: normalised device coordinates and mass colour
 //                       of every body into a device buffer (no graphics API).
