@@ -73,7 +73,10 @@ def test_checked_pair_chunks(n, cap, monkeypatch):
     assert rel_err(a, oracle.accel(pm, 1e-3)) <= ACC_TOL
 
 
-@pytest.mark.parametrize("path,split", [(0, 0), (2, 3), (4, 0)])
+# auto (the one-kernel warp pass and copy_rows), the one-sided paths (one
+# kernel, and stream-K with its second pass), the sliced warp pass and the pair
+# path (drift in place)
+@pytest.mark.parametrize("path,split", [(0, 0), (1, 0), (2, 3), (3, 5), (4, 0)])
 def test_checked_leapfrog_and_kdk(path, split):
     import torch
     import all_pairs_body_gb300 as nb
@@ -156,6 +159,14 @@ def _accel_call(path, split):
     return run
 
 
+def _step_call(path, split):
+    def run():
+        pm = W.random_bodies(9000, 9800)
+        v = W.random_velocities(9000, 9800)
+        return gpu_leapfrog(pm, v, 1e-3, 1e-3, 3, path, split)
+    return run
+
+
 def _neighbors_call():
     import torch
     import all_pairs_body_gb300 as nb
@@ -170,6 +181,8 @@ def _neighbors_call():
     ("partial", _accel_call(2, 3)),
     ("partial", _accel_call(3, 5)),
     ("react", _accel_call(4, 0)),
+    ("rows", _step_call(0, 0)),
+    ("rows", _step_call(4, 0)),
     ("neighbors", _neighbors_call),
 ])
 def test_shrunk_capacity_reports_ebounds(slot, call, monkeypatch):
