@@ -97,3 +97,23 @@ def test_unit_numbering_closed_form():
             for c in range(g):
                 span = range(unit_begin(total, g, c), unit_begin(total, g, c + 1))
                 assert all(owners[u] == c for u in span)
+
+
+@pytest.mark.parametrize("n,block,tj,grid", [
+    (20000, 2048, 256, 152), (16384, 2048, 256, 152), (1048576, 4096, 512, 152),
+    (1048576, 3584, 512, 152), (65537, 2048, 512, 152), (5000, 512, 128, 7)])
+def test_block_segments_of_sharing_ctas(n, block, tj, grid):
+    """The finishing passes read, for a block shared by CTAs c0..c1, the first
+    segment of every CTA after c0 and, of c0 itself, the first segment when c0
+    starts at the block's first unit, else its last: every CTA after c0 starts
+    inside the block."""
+    nblocks, ntiles, tb = -(-n // block), -(-n // tj), block // tj
+    units = units_before(nblocks, ntiles, tb)
+    grid = min(grid, units)
+    for I in range(nblocks):
+        u0 = units_before(I, ntiles, tb)
+        u1 = units_before(I + 1, ntiles, tb) - 1
+        c0, c1 = unit_owner(units, grid, u0), unit_owner(units, grid, u1)
+        assert unit_begin(units, grid, c0) <= u0 < unit_begin(units, grid, c0 + 1)
+        for cc in range(c0 + 1, c1 + 1):
+            assert u0 < unit_begin(units, grid, cc) <= u1
