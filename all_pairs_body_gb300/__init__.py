@@ -274,7 +274,8 @@ TABLE_FIELDS = ("rows", "targets_per_thread", "threads", "tile", "form_or_acc", 
 
 
 def table_row(which: int, row: int) -> dict:
-    """Shape of row ``row`` of this build's tiled (0) or pair (1) kernel table."""
+    """Shape of row ``row`` of this build's tiled (0), pair (1) or warp (2)
+    kernel table; the fields as ``nbody_table`` in nbody.h describes them."""
     out = (ctypes.c_int64 * len(TABLE_FIELDS))()
     _check(lib().nbody_table(int(which), int(row), out, len(TABLE_FIELDS)), "nbody_table")
     return dict(zip(TABLE_FIELDS, (int(v) for v in out)))

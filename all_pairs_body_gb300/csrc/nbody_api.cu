@@ -198,22 +198,28 @@ using WarpKernel = void (*)(const WarpArgs, const Epilogue);
 struct WarpConfig {
   int kw, nw, u;  // targets per CTA, warps per CTA, sources loaded ahead per thread
   WarpKernel kernel;
+  int rs = 0;  // lanes combined by a reduce-scatter (1) or a butterfly (0)
 };
 
 // Shapes of the small-n warp kernel.  The release row: 6 targets per CTA,
 // 4 warps, 8 sources loaded ahead per thread; it matched or beat the other
 // shapes at every n from 1000 to 16384 in a sweep of per-call time (4.7
-// against 6.0 us at n = 1000 for the loop without loads ahead).  The tuning
-// build appends the others.
+// against 6.0 us at n = 1000 for the loop without loads ahead), and its lanes
+// combine their sums by a reduce-scatter (1-6% faster per call than the
+// butterfly from n = 1024 to 12288).  The tuning build appends the others.
 const WarpConfig kWarps[] = {
-    {6, 4, 8, force_warp<6, 4, 8>},
+    {6, 4, 8, force_warp<6, 4, 8, 1>, 1},
 #ifdef NBODY_TUNING_TABLE
+    {6, 4, 8, force_warp<6, 4, 8, 0>},
     {4, 4, 0, force_warp<4, 4, 0>},   {4, 4, 4, force_warp<4, 4, 4>},
     {4, 4, 8, force_warp<4, 4, 8>},   {8, 4, 4, force_warp<8, 4, 4>},
     {8, 4, 8, force_warp<8, 4, 8>},   {8, 4, 16, force_warp<8, 4, 16>},
     {16, 4, 8, force_warp<16, 4, 8>}, {8, 8, 8, force_warp<8, 8, 8>},
     {4, 8, 8, force_warp<4, 8, 8>},   {12, 4, 8, force_warp<12, 4, 8>},
     {8, 2, 8, force_warp<8, 2, 8>},
+    // lanes combined by a reduce-scatter instead of a butterfly
+    {4, 4, 8, force_warp<4, 4, 8, 1>, 1},  {8, 4, 8, force_warp<8, 4, 8, 1>, 1},
+    {10, 4, 8, force_warp<10, 4, 8, 1>, 1},
 #endif
 };
 constexpr int kNumWarps = sizeof(kWarps) / sizeof(kWarps[0]);
@@ -1418,7 +1424,7 @@ int nbody_table(int which, int row, int64_t* out, int len) {
   } else if (which == 2) {
     if (row < 0 || row >= kNumWarps) return NBODY_EINVAL;
     const WarpConfig& c = kWarps[row];
-    const int64_t w[] = {kNumWarps, c.kw, c.nw * 32, c.u, 0, 0};
+    const int64_t w[] = {kNumWarps, c.kw, c.nw * 32, c.u, c.rs, 0};
     std::copy(w, w + 6, v);
   } else {
     return NBODY_EINVAL;

@@ -1678,12 +1678,31 @@ struct WarpArgs {
   float4* partial;     // [S][n] when S > 1
 };
 
+// One level of a reduce-scatter over the 32 lanes of a warp: of the first
+// 2H values, the lanes with bit H set keep the upper H, the others the lower
+// H, each adding its partner's copy of the half it keeps.  After the levels
+// H = 16, 8, 4, 2, 1, lane l holds in w[0] the warp's sum of value l, every
+// sum formed in the same fixed order.
+template <int H>
+__device__ __forceinline__ void reduce_scatter_level(float (&w)[32], int lane) {
+  const bool upper = (lane & H) != 0;
+#pragma unroll
+  for (int k = 0; k < H; ++k) {
+    const float send = upper ? w[k] : w[k + H];
+    const float keep = upper ? w[k + H] : w[k];
+    w[k] = keep + __shfl_xor_sync(0xffffffffu, send, H);
+  }
+}
+
 // U = 0: the thread's sources are loaded one loop iteration at a time.
 // U > 0: in chunks of U, the next chunk's loads issued before the current
 // chunk's arithmetic (software pipelining across the L2 latency); the last
 // chunk is padded with zero-mass sources at the origin, which add exactly
 // nothing.
-template <int KW, int NW, int U = 0>
+// RS = 0: the lanes combine their 3 KW sums by a butterfly of shuffles (every
+// lane ends with every sum); RS = 1: by a reduce-scatter (31 shuffles for up
+// to 32 sums instead of 5 per sum; lane l ends with sum l).
+template <int KW, int NW, int U = 0, int RS = 0>
 __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Epilogue e) {
   static_assert(KW % 2 == 0, "targets are processed in packed pairs");
   constexpr int P = KW / 2;
@@ -1752,27 +1771,49 @@ __global__ void __launch_bounds__(NW * 32) force_warp(const WarpArgs a, const Ep
     }
   }
 
-  // Combine the 32 lanes with a butterfly of shuffles (every lane ends with
-  // the same bits: each step adds the same two values), then the warps in
-  // ascending order through shared memory.
-  float v[3 * KW];
+  // Combine the 32 lanes (a butterfly of shuffles, every lane ending with the
+  // same bits; or a reduce-scatter), then the warps in ascending order
+  // through shared memory.  Sum 3 t + c is component c of target t.
+  if constexpr (RS == 0) {
+    float v[3 * KW];
 #pragma unroll
-  for (int p = 0; p < P; ++p) {
-    v[6 * p + 0] = ax[p].x;
-    v[6 * p + 1] = ay[p].x;
-    v[6 * p + 2] = az[p].x;
-    v[6 * p + 3] = ax[p].y;
-    v[6 * p + 4] = ay[p].y;
-    v[6 * p + 5] = az[p].y;
-  }
+    for (int p = 0; p < P; ++p) {
+      v[6 * p + 0] = ax[p].x;
+      v[6 * p + 1] = ay[p].x;
+      v[6 * p + 2] = az[p].x;
+      v[6 * p + 3] = ax[p].y;
+      v[6 * p + 4] = ay[p].y;
+      v[6 * p + 5] = az[p].y;
+    }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+    for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
-    for (int q = 0; q < 3 * KW; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
-  }
-  if (lane == 0) {
+      for (int q = 0; q < 3 * KW; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], off);
+    }
+    if (lane == 0) {
 #pragma unroll
-    for (int q = 0; q < 3 * KW; ++q) red[warp][q] = v[q];
+      for (int q = 0; q < 3 * KW; ++q) red[warp][q] = v[q];
+    }
+  } else {
+    static_assert(3 * KW <= 32, "one sum per lane");
+    float w[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) w[q] = 0.f;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      w[6 * p + 0] = ax[p].x;
+      w[6 * p + 1] = ay[p].x;
+      w[6 * p + 2] = az[p].x;
+      w[6 * p + 3] = ax[p].y;
+      w[6 * p + 4] = ay[p].y;
+      w[6 * p + 5] = az[p].y;
+    }
+    reduce_scatter_level<16>(w, lane);
+    reduce_scatter_level<8>(w, lane);
+    reduce_scatter_level<4>(w, lane);
+    reduce_scatter_level<2>(w, lane);
+    reduce_scatter_level<1>(w, lane);
+    if (lane < 3 * KW) red[warp][lane] = w[0];
   }
   __syncthreads();
   if (tid < KW) {

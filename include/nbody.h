@@ -354,7 +354,8 @@ int nbody_plan(int64_t n, int path, int split, int64_t *out, int len);
  *   [2] threads per CTA
  *   [3] sources per tile (warp kernel: sources each thread loads ahead)
  *   [4] tiled: 1 for the mixed rsqrt/logarithmic loop; pairs: 1 for running
- *       sums in shared memory; warp kernel: 0
+ *       sums in shared memory; warp kernel: 1 for lanes combined by a
+ *       reduce-scatter, 0 for a butterfly
  *   [5] pairs: the reaction scheme (0 warp butterfly over batches, 1 and 2
  *       lane rotation with one or two groups, 3 and 4 the same with loads one
  *       step ahead, scalar carries and duplicated groups); others: 0.

@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 # rows of the tuning build's tables (the release rows come first)
 N_TILED_ROWS = 22
 N_PAIR_ROWS = 90
-N_WARP_ROWS = 12
+N_WARP_ROWS = 16
 N_TILED_RELEASE = 4
 N_PAIR_RELEASE = 6
 N_WARP_RELEASE = 1
