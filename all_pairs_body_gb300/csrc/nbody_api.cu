@@ -201,14 +201,17 @@ struct WarpConfig {
   int rs = 0;  // lanes combined by a reduce-scatter (1) or a butterfly (0)
 };
 
-// Shapes of the small-n warp kernel.  The release row: 6 targets per CTA,
-// 4 warps, 8 sources loaded ahead per thread; it matched or beat the other
+// Shapes of the small-n warp kernel.  The release rows: 6 targets per CTA,
+// 4 warps, 8 sources loaded ahead per thread, which matched or beat the other
 // shapes at every n from 1000 to 16384 in a sweep of per-call time (4.7
-// against 6.0 us at n = 1000 for the loop without loads ahead), and its lanes
-// combine their sums by a reduce-scatter (1-6% faster per call than the
-// butterfly from n = 1024 to 12288).  The tuning build appends the others.
+// against 6.0 us at n = 1000 for the loop without loads ahead); and 8 targets
+// per CTA, taken up to kWarpSmallN bodies (6.7 against 7.2 us per call at
+// n = 1024, equal at 4097, slower above).  Both combine their lanes' sums by a
+// reduce-scatter (1-6% faster per call than the butterfly from n = 1024 to
+// 12288).  The tuning build appends the others.
 const WarpConfig kWarps[] = {
     {6, 4, 8, force_warp<6, 4, 8, 1>, 1},
+    {8, 4, 8, force_warp<8, 4, 8, 1>, 1},
 #ifdef NBODY_TUNING_TABLE
     {6, 4, 8, force_warp<6, 4, 8, 0>},
     {4, 4, 0, force_warp<4, 4, 0>},   {4, 4, 4, force_warp<4, 4, 4>},
@@ -218,8 +221,7 @@ const WarpConfig kWarps[] = {
     {4, 8, 8, force_warp<4, 8, 8>},   {12, 4, 8, force_warp<12, 4, 8>},
     {8, 2, 8, force_warp<8, 2, 8>},
     // lanes combined by a reduce-scatter instead of a butterfly
-    {4, 4, 8, force_warp<4, 4, 8, 1>, 1},  {8, 4, 8, force_warp<8, 4, 8, 1>, 1},
-    {10, 4, 8, force_warp<10, 4, 8, 1>, 1},
+    {4, 4, 8, force_warp<4, 4, 8, 1>, 1},  {10, 4, 8, force_warp<10, 4, 8, 1>, 1},
 #endif
 };
 constexpr int kNumWarps = sizeof(kWarps) / sizeof(kWarps[0]);
@@ -474,14 +476,19 @@ void plan_tiled(long long n, int path, int split, const DeviceInfo& d, Plan* p) 
   p->second_pass = streamk_needs_second_pass(p->units, p->grid, p->ntiles);
 }
 
-// The warp kernel's shape: NBODY_WARP_CONFIG forces a row, else row 0.
-int warp_config() {
+// Up to this many bodies the warp kernel takes its second release row.
+constexpr long long kWarpSmallN = 4096;
+
+// The warp kernel's shape: NBODY_WARP_CONFIG forces a row, else row 1 up to
+// kWarpSmallN bodies and row 0 above.
+int warp_config(long long n) {
   const long long forced = env_int("NBODY_WARP_CONFIG", -1);
-  return forced >= 0 && forced < kNumWarps ? static_cast<int>(forced) : 0;
+  if (forced >= 0 && forced < kNumWarps) return static_cast<int>(forced);
+  return n <= kWarpSmallN ? 1 : 0;
 }
 
 void plan_warp(long long n, int split, const DeviceInfo& d, Plan* p) {
-  p->cfg = warp_config();
+  p->cfg = warp_config(n);
   const WarpConfig& wc = kWarps[p->cfg];
   p->threads = wc.nw * 32;
   p->block = wc.kw;

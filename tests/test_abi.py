@@ -232,8 +232,9 @@ def test_release_table_holds_only_the_planned_kernels(L):
     """The release build compiles the rows its plans choose between: four
     one-sided tiled shapes (two large-n tiles, the no-allocation shape, the
     small-n shape), six pair-symmetric shapes (targets per thread, threads,
-    tile, running sums in shared memory, reaction scheme) and one warp-kernel
-    shape: 11 force kernels."""
+    tile, running sums in shared memory, reaction scheme) and two warp-kernel
+    shapes (targets per CTA, threads, sources loaded ahead, lanes combined by
+    a reduce-scatter): 12 force kernels."""
     rc, row = _table(L, 0, 0)
     assert rc == nb.OK and row[0] == 4
     tiled = [tuple(_table(L, 0, r)[1][1:5]) for r in range(4)]
@@ -243,10 +244,12 @@ def test_release_table_holds_only_the_planned_kernels(L):
     pairs = [tuple(_table(L, 1, r)[1][1:6]) for r in range(6)]
     assert pairs == [(16, 256, 512, 1, 3), (14, 256, 512, 0, 3), (12, 256, 512, 1, 3),
                      (10, 256, 512, 1, 4), (8, 256, 512, 1, 4), (8, 256, 256, 0, 4)]
-    assert 4 + 6 + 1 <= 12
+    assert 4 + 6 + 2 <= 12
     rc, row = _table(L, 2, 0)
-    assert rc == nb.OK and row[:4] == [1, 6, 128, 8]  # the warp kernel: 6 targets, 8 loaded ahead
-    for which, row in ((0, 4), (1, 6), (2, 1), (0, -1), (3, 0)):
+    assert rc == nb.OK and row[0] == 2
+    warps = [tuple(_table(L, 2, r)[1][1:5]) for r in range(2)]
+    assert warps == [(6, 128, 8, 1), (8, 128, 8, 1)]
+    for which, row in ((0, 4), (1, 6), (2, 2), (0, -1), (3, 0)):
         assert _table(L, which, row)[0] == nb.EINVAL
     assert L.nbody_table(0, 0, None, 0) == nb.OK
     assert L.nbody_table(0, 0, None, 3) == nb.EINVAL

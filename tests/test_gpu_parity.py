@@ -277,6 +277,11 @@ def test_plan_is_consistent():
         assert p["launches_accel"] >= 1
     p = nb.plan(1048576, path=nb.PATH_TILED)
     assert p["second_pass"] == 0 and p["grid"] * p["bodies_per_cta"] >= 1048576
+    # the warp kernel: 8 targets per CTA up to 4096 bodies, 6 above
+    for n, kw in ((1000, 8), (4096, 8), (4097, 6), (16383, 6)):
+        p = nb.plan(n)
+        assert p["path"] == nb.PATH_WARP and p["bodies_per_cta"] == kw, (n, p)
+        assert p["grid"] == -(-n // kw) and p["second_pass"] == 0
 
 
 def test_plan_shape_follows_streamk_model():

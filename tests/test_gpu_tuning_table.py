@@ -26,7 +26,7 @@ N_PAIR_ROWS = 90
 N_WARP_ROWS = 16
 N_TILED_RELEASE = 4
 N_PAIR_RELEASE = 6
-N_WARP_RELEASE = 1
+N_WARP_RELEASE = 2
 
 
 @pytest.fixture(scope="module", autouse=True)
