@@ -808,6 +808,60 @@ def test_layout_steps_match_oracle(layout, n):
 
 
 # ---------------------------------------------------------------------------
+# seeded random configurations
+# ---------------------------------------------------------------------------
+
+
+def _random_cases(count, seed):
+    """Seeded draws over the call space: n log-uniform in [1, 60000], the
+    entry point (accelerations, steps, kick-drift-kick steps, steps with
+    float3 or block velocity layouts), the forced path and split, 1-4 steps
+    and eps2 in {1e-2, 1e-3, 1e-4}."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for k in range(count):
+        n = int(round(float(np.exp(rng.uniform(0.0, np.log(60000.0))))))
+        mode = ("accel", "step", "kdk", "layout")[int(rng.integers(4))]
+        path, split = PATHS[int(rng.integers(len(PATHS)))]
+        cases.append((k, n, mode, path, split, int(rng.integers(1, 5)), int(rng.integers(1, 3)),
+                      (1e-2, 1e-3, 1e-4)[int(rng.integers(3))]))
+    return cases
+
+
+@pytest.mark.parametrize("k,n,mode,path,split,steps,layout,eps2", _random_cases(24, 2026))
+def test_random_configurations(k, n, mode, path, split, steps, layout, eps2):
+    import torch
+    import all_pairs_body_gb300 as nb
+    pm = W.random_bodies(n, 8500 + k)
+    v = W.random_velocities(n, 8500 + k)
+    if mode == "accel":
+        a = gpu_accel(pm, eps2, path, split)
+        assert rel_err(a, oracle.accel(pm, eps2)) <= ACC_TOL
+        assert np.all(a[:, 3] == 0.0)
+        return
+    if mode == "layout":
+        tp = torch.from_numpy(pm).cuda()
+        tv = torch.from_numpy(_to_layout(v, layout)).cuda()
+        ta = torch.full_like(tv, float("nan"))
+        nb.leapfrog_step_layout(tp, tv, ta, eps2, 1e-3, steps, layout)
+        nb.sync()
+        p, vv, a = tp.cpu().numpy(), _from_layout(tv.cpu().numpy(), layout), \
+            _from_layout(ta.cpu().numpy(), layout)
+        rp, rv, ra = oracle.leapfrog(pm, v, eps2, 1e-3, steps)
+    elif mode == "kdk":
+        p, vv, a = gpu_kdk(pm, v, eps2, 1e-3, steps, path, split)
+        rp, rv, ra = oracle.leapfrog_kdk(pm, v, eps2, 1e-3, steps)
+        assert np.array_equal(vv[:, 3], v[:, 3])
+    else:
+        p, vv, a = gpu_leapfrog(pm, v, eps2, 1e-3, steps, path, split)
+        rp, rv, ra = oracle.leapfrog(pm, v, eps2, 1e-3, steps)
+        assert np.array_equal(vv[:, 3], v[:, 3])
+    assert rel_err(a, ra) <= ACC_TOL and rel_err(vv, rv) <= VEL_TOL
+    assert rel_err(p, rp) <= POS_TOL and displacement_err(p, rp, pm, steps) <= 1e-3
+    assert np.array_equal(p[:, 3], pm[:, 3])
+
+
+# ---------------------------------------------------------------------------
 # plain entry points (legacy default stream) and concurrent streams
 # ---------------------------------------------------------------------------
 
