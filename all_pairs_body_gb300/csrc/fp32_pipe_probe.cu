@@ -14,6 +14,12 @@
 //                          shared-memory tile, loads one step ahead, a scalar
 //                          carry per component, 8 packed target pairs, its
 //                          interaction (interact2_pair) unchanged
+//   pair step, u form     the same loop with the interaction's products
+//                          regrouped: u = q^3 r first, then the action m_j u
+//                          and the reaction m_i u (17 packed instructions
+//                          instead of 16, but the source mass, the target
+//                          mass and q^3 each repeat in three consecutive
+//                          instructions)
 //
 // Build and run: python -m all_pairs_body_gb300.build --probe
 #include <cmath>
@@ -64,8 +70,35 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_stream(float* out, long long
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// interact2_pair with the products regrouped: u = q^3 r, then a += m_j u and
+// the reaction b += (-m_i) u.
+__device__ __forceinline__ void interact2_pair_u(float2 X, float2 Y, float2 Z, float2 M, float2 nx,
+                                                 float2 ny, float2 nz, float2 nm, float2 e2,
+                                                 float2& ax, float2& ay, float2& az, float2& bx,
+                                                 float2& by, float2& bz) {
+  const float2 rx = __fadd2_rn(X, nx);
+  const float2 ry = __fadd2_rn(Y, ny);
+  const float2 rz = __fadd2_rn(Z, nz);
+  float2 d = __ffma2_rn(rx, rx, e2);
+  d = __ffma2_rn(ry, ry, d);
+  d = __ffma2_rn(rz, rz, d);
+  const float2 q = make_float2(nbody::rsqrt_approx(d.x), nbody::rsqrt_approx(d.y));
+  const float2 q3 = __fmul2_rn(__fmul2_rn(q, q), q);
+  const float2 ux = __fmul2_rn(q3, rx);
+  const float2 uy = __fmul2_rn(q3, ry);
+  const float2 uz = __fmul2_rn(q3, rz);
+  ax = __ffma2_rn(M, ux, ax);
+  ay = __ffma2_rn(M, uy, ay);
+  az = __ffma2_rn(M, uz, az);
+  bx = __ffma2_rn(nm, ux, bx);
+  by = __ffma2_rn(nm, uy, by);
+  bz = __ffma2_rn(nm, uz, bz);
+}
+
 // The steady state of the pair kernel's reaction scheme 3 over one tile,
-// repeated `iters` times (no TMA, no barriers, no per-tile work).
+// repeated `iters` times (no TMA, no barriers, no per-tile work).  FORM 0:
+// interact2_pair; FORM 1: interact2_pair_u.
+template <int FORM>
 __global__ void __launch_bounds__(kThreads, 1) pair_step(const float4* __restrict__ src, float* out,
                                                         long long* cycles, int iters, float eps2) {
   constexpr int P = 8;
@@ -110,10 +143,16 @@ __global__ void __launch_bounds__(kThreads, 1) pair_step(const float4* __restric
         bzs = __shfl_sync(0xffffffffu, bzs, from);
         float2 bx = make_float2(bxs, 0.f), by = make_float2(bys, 0.f), bz = make_float2(bzs, 0.f);
 #pragma unroll
-        for (int p = 0; p < P; ++p)
-          nbody::interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
-                                make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
-                                nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+        for (int p = 0; p < P; ++p) {
+          if (FORM == 0)
+            nbody::interact2_pair(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                                  make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                                  nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+          else
+            interact2_pair_u(make_float2(lo.x, lo.y), make_float2(lo.z, lo.w),
+                             make_float2(hi.x, hi.y), make_float2(hi.z, hi.w), nx[p], ny[p],
+                             nz[p], nm[p], e2, tx[p], ty[p], tz[p], bx, by, bz);
+        }
         bxs = bx.x + bx.y;
         bys = by.x + by.y;
         bzs = bz.x + bz.y;
@@ -180,13 +219,20 @@ int main() {
     std::printf("  %-24s %.4f\n", r.name, ffma_ops / (mean_cycles(cyc, sms) * 128.0));
   }
   const int piters = 100;
-  cudaFuncSetAttribute(pair_step, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  pair_step<<<sms, kThreads, smem>>>(src, out, cyc, 2, 1e-3f);
-  pair_step<<<sms, kThreads, smem>>>(src, out, cyc, piters, 1e-3f);
-  if (!check(cudaDeviceSynchronize(), "pair step")) return 1;
-  // per thread and step: 8 target pairs x 16 packed instructions (32 lane-ops) + 3 adds
+  // per thread and step: 8 target pairs x 16 packed instructions (32 lane-ops) + 3 adds; the
+  // u form does the same work in 17 packed instructions and is counted the same (per pair)
   const double pair_ops = (8.0 * 32 + 3) * kTile * piters * kThreads;
-  std::printf("  %-24s %.4f\n", "pair step", pair_ops / (mean_cycles(cyc, sms) * 128.0));
+  struct PairRun {
+    const char* name;
+    void (*k)(const float4*, float*, long long*, int, float);
+  } pruns[] = {{"pair step", pair_step<0>}, {"pair step, u form", pair_step<1>}};
+  for (const PairRun& r : pruns) {
+    cudaFuncSetAttribute(r.k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    r.k<<<sms, kThreads, smem>>>(src, out, cyc, 2, 1e-3f);
+    r.k<<<sms, kThreads, smem>>>(src, out, cyc, piters, 1e-3f);
+    if (!check(cudaDeviceSynchronize(), r.name)) return 1;
+    std::printf("  %-24s %.4f\n", r.name, pair_ops / (mean_cycles(cyc, sms) * 128.0));
+  }
   cudaFree(out);
   cudaFree(cyc);
   cudaFree(src);
