@@ -697,8 +697,11 @@ def run_ours(args):
                            "the 2-D neighbour list at 2^20, measured after the timed steps in "
                            "this process: device time per call between CUDA events (L2 flushed "
                            "before each call), the force kernel alone from a second, profiled "
-                           "run; R = the one-sided 12-op FP32 roofline at sm_max_mhz",
-                   "results": measure_configs(nb, torch, stream, flush, sms, f_max)}
+                           "run; R = the one-sided 12-op FP32 roofline at sm_max_mhz"}
+        try:
+            configs["results"] = measure_configs(nb, torch, stream, flush, sms, f_max)
+        except Exception as exc:  # noqa: BLE001 - reported in the line, never fatal
+            configs["error"] = f"{type(exc).__name__}: {exc}"
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
