@@ -830,6 +830,8 @@ void launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, size_t s
   cudaLaunchKernelEx(&cfg, kernel, args...);  // an error stays for launch_status()
 }
 
+// A per-body kernel (the finishing passes, copy_rows): `blocks` CTAs of
+// kFinishThreads threads, launched as above.
 template <typename... KArgs, typename... Args>
 void launch_second_pass(void (*kernel)(KArgs...), long long blocks, cudaStream_t st,
                         Args... args) {
