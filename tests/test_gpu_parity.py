@@ -119,6 +119,22 @@ def test_trajectory_10_steps(name):
     assert np.array_equal(v[:, 3], w.vel[:, 3]), "vel.w changed"
 
 
+@pytest.mark.parametrize("path", [0, 3])
+def test_trajectory_100_steps(path):
+    """C2's bodies for 100 steps in one call (200 kernels chained as
+    programmatic dependents on the pair path, 100 one-kernel passes and a copy
+    on the warp path), against the oracle's trajectory."""
+    w = W.plummer_16384()
+    p, v, a = gpu_leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, 100, path)
+    if "trajectory_100" not in _REF:
+        _REF["trajectory_100"] = oracle.leapfrog(w.pos_mass, w.vel, w.eps2, w.dt, 100)
+    rp, rv, ra = _REF["trajectory_100"]
+    assert rel_err(p, rp) <= POS_TOL
+    assert rel_err(v, rv) <= VEL_TOL
+    assert rel_err(a, ra) <= ACC_TOL
+    assert displacement_err(p, rp, w.pos_mass, 100) <= 1e-3
+
+
 # ---------------------------------------------------------------------------
 # every path on the same inputs
 # ---------------------------------------------------------------------------
